@@ -1,0 +1,344 @@
+"""CPU oracle of the CacheBlend blend step (plain numpy, float64 arithmetic).
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports this module;
+only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference legs may call it.  It shares no code with the CUDA library.
+
+Source of every step: the CacheBlend deep-dive page ("CacheBlend 完全拆解:RAG 多段
+KV 缓存拼接,为什么还要重算一小部分 token").  Section names are quoted in the
+docstrings below.
+
+Readings taken where the page leaves a step open (each is listed in the design doc):
+  R1  the check layer (full computation + deviation + selection) is layer index 1,
+      the first layer whose input has seen other chunks; layer 0 recomputes hidden
+      states for every row but reuses the (context-free) cached layer-0 K/V.
+  R2  deviation = squared L2 over all KV heads and dims, K and V with equal weight,
+      fresh (unrounded) K/V against the re-RoPE'd stored cache.
+  R3  k = ceil(ratio * n_ctx) (minus 1e-9 to absorb representation error), clamped
+      to [0, n_ctx]; query rows are always recomputed and never compete.
+  R4  the set is chosen once at the check layer and kept for every later layer.
+  R5  ties in deviation go to the lower position; the set is reported ascending.
+  R6  within a layer the selected rows' fresh K/V are stored before attention, so
+      selected queries see each other's fresh K/V ("assemble a complete K/V, then
+      attend", Figure 5 of the page).
+  R7  storage: out_kv is rounded once to the storage type (bf16 or f32, round to
+      nearest even); activations stay unrounded float64.  Mode 'f64' keeps
+      float64 storage for the exactness pins.
+  R8  RoPE pairs are adjacent dims (2i, 2i+1), angle m * theta^(-2i/hd) in float64
+      (the block-diagonal rotation of section "位置恢复、KV 存储与加载流水线").
+  R9  Llama-style pre-norm decoder without biases; RMSNorm eps 1e-5; SwiGLU MLP;
+      untied embedding / LM head.
+
+Parity pins (tests/test_oracle_*.py): RoPE composition and orthogonality,
+sequential-decode brute force, r = 1 equals a full joint prefill, r = 0 equals
+full KV reuse, causal-prefix exactness, the page's Δkv definition, top-k against a
+full sort, GQA against a library attention, bf16 rounding against a library cast.
+The selected set at 0 < r < 1 is pinned only through the Δkv identity (the pages
+print no worked example of a blend).
+"""
+from __future__ import annotations
+
+import math
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_POOL = None
+_Q_BLOCK = 512       # query rows per attention block (memory bound only; rows are independent)
+_ROW_BLOCK = 4096    # rows per MLP block (memory bound only)
+
+
+def _pool():
+    global _POOL
+    if _POOL is None:
+        _POOL = ThreadPoolExecutor(max_workers=16)
+    return _POOL
+
+
+# ----------------------------------------------------------------------------------------------
+# number formats
+# ----------------------------------------------------------------------------------------------
+def to_f64(a: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns (uint16) or float arrays -> float64 values (exact)."""
+    if a.dtype == np.uint16:
+        flat = a.reshape(-1)
+        out = np.empty(flat.shape, np.float64)
+        step = max(1 << 20, -(-flat.size // 16))
+
+        def conv(lo):
+            hi = min(lo + step, flat.size)
+            out[lo:hi] = (flat[lo:hi].astype(np.uint32) << 16).view(np.float32)
+
+        list(_pool().map(conv, range(0, flat.size, step)))
+        return out.reshape(a.shape)
+    return np.asarray(a, dtype=np.float64)
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest bfloat16 (8 significant bits), ties to even.
+
+    bfloat16 keeps float32's exponent range and 8 significand bits; x = m * 2^e with
+    m in [0.5, 1), so m * 2^8 rounded to an integer (np.rint: ties to even) is the
+    bfloat16 significand.  (Subnormals and overflow do not occur here.)"""
+    m, e = np.frexp(np.asarray(x, dtype=np.float64))
+    return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+
+
+def round_store(x: np.ndarray, store: str) -> np.ndarray:
+    if store == "bf16":
+        return round_bf16(x)
+    if store == "f32":
+        return np.asarray(x, np.float32).astype(np.float64)
+    if store == "f64":
+        return np.asarray(x, np.float64)
+    raise ValueError(store)
+
+
+# ----------------------------------------------------------------------------------------------
+# model pieces (section "问题:拼接的 KV 缓存到底少了什么": Q_i = h_i W_Q, K_i = h_i W_K,
+# V_i = h_i W_V, K rotated by position)
+# ----------------------------------------------------------------------------------------------
+def rope_freqs(head_dim: int, theta: float) -> np.ndarray:
+    """theta_i = theta^(-2i/hd), i < hd/2 (float64)."""
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    return np.power(float(theta), -2.0 * i / head_dim)
+
+
+def rope(x: np.ndarray, pos, theta: float) -> np.ndarray:
+    """Apply R_m to every head vector of x [n][H][hd] at positions pos [n].
+
+    R_m is block diagonal; block i rotates dims (2i, 2i+1) by angle m * theta_i
+    (section "位置恢复、KV 存储与加载流水线": q_m = R_m q, k_n = R_n k)."""
+    x = np.asarray(x, np.float64)
+    hd = x.shape[-1]
+    ang = np.asarray(pos, np.float64)[:, None] * rope_freqs(hd, theta)[None, :]
+    c = np.cos(ang)[:, None, :]
+    s = np.sin(ang)[:, None, :]
+    x0, x1 = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = x0 * c - x1 * s
+    out[..., 1::2] = x0 * s + x1 * c
+    return out
+
+
+def rmsnorm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x * g / np.sqrt(ms + eps)
+
+
+def silu(x: np.ndarray) -> np.ndarray:
+    return x / (1.0 + np.exp(-x))
+
+
+def attention(q, k, v, q_pos, k_pos, n_kv_heads: int) -> np.ndarray:
+    """Causal softmax attention with grouped KV heads.
+
+    q [M][Hq][hd]; k, v [Nk][Hkv][hd]; query a sees key j iff k_pos[j] <= q_pos[a].
+    q-head h reads KV head h // (Hq / Hkv); scores scaled by 1/sqrt(hd)."""
+    M, Hq, hd = q.shape
+    group = Hq // n_kv_heads
+    q_pos = np.asarray(q_pos)
+    k_pos = np.asarray(k_pos)
+    out = np.empty((M, Hq, hd), np.float64)
+    scale = 1.0 / math.sqrt(hd)
+    for b0 in range(0, M, _Q_BLOCK):
+        qp = q_pos[b0:b0 + _Q_BLOCK]
+        visible = k_pos[None, :] <= qp[:, None]                     # [b][Nk]
+        for h in range(Hq):
+            g = h // group
+            s = (q[b0:b0 + _Q_BLOCK, h, :] @ k[:, g, :].T) * scale  # [b][Nk]
+            s = np.where(visible, s, -np.inf)
+            s = s - s.max(axis=1, keepdims=True)
+            p = np.exp(s)
+            p /= p.sum(axis=1, keepdims=True)
+            out[b0:b0 + _Q_BLOCK, h, :] = p @ v[:, g, :]
+    return out
+
+
+class Model:
+    """Config dict + weights (as produced by the workload generator), widened to float64 per layer."""
+
+    def __init__(self, cfg: dict, weights: dict):
+        self.cfg = cfg
+        self.w = weights
+        self.L = cfg["n_layers"]
+        self.d = cfg["d_model"]
+        self.Hq = cfg["n_heads"]
+        self.Hkv = cfg["n_kv_heads"]
+        self.hd = cfg["head_dim"]
+        self.theta = cfg["rope_theta"]
+        self.eps = cfg.get("rms_eps", 1e-5)
+
+    def layer(self, i: int) -> dict:
+        return {k: to_f64(v) for k, v in self.w["layers"][i].items()}
+
+    def embed_rows(self, tokens) -> np.ndarray:
+        return to_f64(self.w["embed"][np.asarray(tokens)])
+
+    # -- one decoder layer, split where the blend needs to intervene --------------------------
+    def qkv(self, W: dict, h: np.ndarray, pos):
+        """x = RMSNorm(h); q, k rotated at their positions; v plain.  Shapes [n][H][hd]."""
+        n = h.shape[0]
+        x = rmsnorm(h, W["attn_norm"], self.eps)
+        q = rope((x @ W["wq"].T).reshape(n, self.Hq, self.hd), pos, self.theta)
+        k = rope((x @ W["wk"].T).reshape(n, self.Hkv, self.hd), pos, self.theta)
+        v = (x @ W["wv"].T).reshape(n, self.Hkv, self.hd)
+        return q, k, v
+
+    def q_only(self, W: dict, h: np.ndarray, pos):
+        n = h.shape[0]
+        x = rmsnorm(h, W["attn_norm"], self.eps)
+        return rope((x @ W["wq"].T).reshape(n, self.Hq, self.hd), pos, self.theta)
+
+    def finish(self, W: dict, h: np.ndarray, o: np.ndarray) -> np.ndarray:
+        """h + o W_O, then h + W_down(silu(W_gate x) * W_up x) with x = RMSNorm(h)."""
+        out = np.empty_like(h)
+        for b0 in range(0, h.shape[0], _ROW_BLOCK):
+            hb = h[b0:b0 + _ROW_BLOCK] + o[b0:b0 + _ROW_BLOCK].reshape(-1, self.Hq * self.hd) @ W["wo"].T
+            x = rmsnorm(hb, W["mlp_norm"], self.eps)
+            out[b0:b0 + _ROW_BLOCK] = hb + (silu(x @ W["w_gate"].T) * (x @ W["w_up"].T)) @ W["w_down"].T
+        return out
+
+    def logits(self, h_last: np.ndarray) -> np.ndarray:
+        x = rmsnorm(h_last, to_f64(self.w["final_norm"]), self.eps)
+        return to_f64(self.w["lm_head"]) @ x
+
+
+# ----------------------------------------------------------------------------------------------
+# the blend step
+# ----------------------------------------------------------------------------------------------
+def selected_count(n_ctx: int, ratio: float) -> int:
+    """k = ceil(ratio * n_ctx), clamped to [0, n_ctx] (reading R3)."""
+    k = math.ceil(float(ratio) * n_ctx - 1e-9)
+    return int(min(max(k, 0), n_ctx))
+
+
+def select_hkvd(dev: np.ndarray, k: int) -> np.ndarray:
+    """The k rows of largest deviation (HKVD tokens), ties to the lower row, ascending.
+
+    Section "选 token:HKVD、逐层过滤与 15% 这个经验值": rank tokens by KV deviation
+    and keep the top fraction."""
+    order = np.argsort(-np.asarray(dev, np.float64), kind="stable")
+    return np.sort(order[:k]).astype(np.int64)
+
+
+def rerope(cached_kv: np.ndarray, chunks, theta: float, store: str) -> np.ndarray:
+    """Place chunk caches at their new offsets: K <- R_{dst-src} K, V unchanged.
+
+    Section "位置恢复、KV 存储与加载流水线": a key cached at position p as k_p = R_p k
+    becomes R_{n-p} k_p = R_n k at its new position n; V carries no position.
+    cached_kv [L][2][n_ctx][Hkv][hd] holds the context rows in placed (dst) order.
+    Returns float64 values rounded to the storage type."""
+    kv = to_f64(cached_kv).copy()
+    for src, dst, ln in chunks:
+        delta = dst - src
+        rows = slice(dst, dst + ln)
+        for layer in range(kv.shape[0]):
+            kv[layer, 0, rows] = round_store(rope(kv[layer, 0, rows], np.full(ln, delta), theta), store)
+    return kv
+
+
+def deviation(k_new, v_new, k_pre, v_pre) -> np.ndarray:
+    """Δkv[j] = ||K_new[j] - K_pre[j]||^2 + ||V_new[j] - V_pre[j]||^2 over all KV heads/dims.
+
+    Section "核心思想:只重算偏差最大的那一小撮 token", KV-deviation formula (reading R2)."""
+    n, width = k_new.shape[0], int(np.prod(k_new.shape[1:]))
+    dk = (k_new - k_pre).reshape(n, width)
+    dv = (v_new - v_pre).reshape(n, width)
+    return np.sum(dk * dk, axis=1) + np.sum(dv * dv, axis=1)
+
+
+def validate_chunks(chunks, n_tokens: int) -> int:
+    """Chunks must tile [0, n_ctx) in dst order; src >= 0; at least one query row."""
+    at = 0
+    for src, dst, ln in chunks:
+        if src < 0 or ln <= 0 or dst != at:
+            raise ValueError("chunks must tile [0, n_ctx) in order with src >= 0")
+        at += ln
+    if at >= n_tokens:
+        raise ValueError("need at least one query token after the context")
+    return at
+
+
+def blend(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratio: float, store: str) -> dict:
+    """One CacheBlend blend (sections "核心思想" and "选 token", Figures 5 and 9).
+
+    1. re-RoPE the cached chunk K/V to their placed positions (V copied);
+    2. embed all rows;
+    3. layer 0: every row's hidden state is recomputed; context rows reuse their
+       cached (context-free) K/V, query rows get fresh K/V (stored);
+    4. check layer 1: fresh Q/K/V for every row; Δkv of each context row against
+       its re-RoPE'd cache; the top-k rows plus the query rows form the set A;
+       A's fresh K/V are stored; A attends over the blended K/V; O and MLP on A;
+    5. layers 2..L-1: only A's rows: QKV, store, attend, O, MLP;
+    6. logits of the last row.
+
+    Returns dict(out_kv [L][2][N][Hkv][hd] float64, logits [V], selected [k],
+    dev [n_ctx], k)."""
+    m = Model(cfg, weights)
+    tokens = np.asarray(tokens, np.int64)
+    N = tokens.shape[0]
+    n_ctx = validate_chunks(chunks, N)
+    L, Hkv, hd = m.L, m.Hkv, m.hd
+    pos = np.arange(N)
+
+    kv_dtype = np.float64 if store == "f64" else np.float32   # bf16/f32 values are exact in f32
+    out_kv = np.zeros((L, 2, N, Hkv, hd), kv_dtype)
+    if n_ctx:
+        out_kv[:, :, :n_ctx] = rerope(cached_kv, chunks, m.theta, store)
+
+    h = m.embed_rows(tokens)
+
+    # layer 0: all rows; context K/V reused, query K/V fresh
+    W = m.layer(0)
+    q = m.q_only(W, h, pos)
+    _, kq, vq = m.qkv(W, h[n_ctx:], pos[n_ctx:])
+    out_kv[0, 0, n_ctx:] = round_store(kq, store)
+    out_kv[0, 1, n_ctx:] = round_store(vq, store)
+    o = attention(q, out_kv[0, 0].astype(np.float64), out_kv[0, 1].astype(np.float64), pos, pos, Hkv)
+    h = m.finish(W, h, o)
+    del W
+
+    # check layer 1: all rows' fresh q/k/v; deviation; selection
+    W = m.layer(1)
+    q, k_new, v_new = m.qkv(W, h, pos)
+    dev = deviation(k_new[:n_ctx], v_new[:n_ctx], out_kv[1, 0, :n_ctx].astype(np.float64),
+                    out_kv[1, 1, :n_ctx].astype(np.float64))
+    kk = selected_count(n_ctx, ratio)
+    sel = select_hkvd(dev, kk)
+    A = np.concatenate([sel, np.arange(n_ctx, N)])
+    out_kv[1, 0, A] = round_store(k_new[A], store)
+    out_kv[1, 1, A] = round_store(v_new[A], store)
+    o = attention(q[A], out_kv[1, 0].astype(np.float64), out_kv[1, 1].astype(np.float64), A, pos, Hkv)
+    hA = m.finish(W, h[A], o)
+    del W, h, q, k_new, v_new
+
+    # layers 2..L-1: only the selected rows and the query
+    for layer in range(2, L):
+        W = m.layer(layer)
+        q, k_a, v_a = m.qkv(W, hA, A)
+        out_kv[layer, 0, A] = round_store(k_a, store)
+        out_kv[layer, 1, A] = round_store(v_a, store)
+        o = attention(q, out_kv[layer, 0].astype(np.float64), out_kv[layer, 1].astype(np.float64), A, pos, Hkv)
+        hA = m.finish(W, hA, o)
+        del W
+
+    logits = m.logits(hA[-1])
+    return dict(out_kv=out_kv, logits=logits, selected=sel, dev=dev, k=kk, rows=A)
+
+
+def prefill(cfg: dict, weights: dict, tokens, store: str) -> dict:
+    """Plain causal prefill at positions 0..N-1: the blend with no cached chunks."""
+    return blend(cfg, weights, tokens, None, [], 0.0, store)
+
+
+def chunk_caches(cfg: dict, weights: dict, chunk_tokens, chunks, store: str) -> np.ndarray:
+    """Each chunk prefilled alone at positions src..src+len-1, stored at the storage
+    type and concatenated in placed order: the cached_kv input of a blend."""
+    parts = []
+    for toks, (src, dst, ln) in zip(chunk_tokens, chunks):
+        assert len(toks) == ln
+        if src != 0:
+            raise NotImplementedError("chunk caches are prefilled from position 0")
+        parts.append(prefill(cfg, weights, toks, store)["out_kv"])
+    return np.concatenate(parts, axis=2)
