@@ -1,0 +1,229 @@
+"""Python binding of libcacheblend (the GB300 CacheBlend blend-step library).
+
+Argument marshalling only: every step of the blend runs in the CUDA library behind the C ABI
+declared in ``include/cacheblend.h``.  PyTorch is used for device memory and streams.  There is
+no fallback: if ``libcacheblend.so`` is missing or cannot be loaded, every call raises.
+
+Entry points (same names as the C ABI): ``cb_model_create``, ``cb_model_destroy``,
+``cb_rerope``, ``cb_blend``, ``cb_selected_count``, ``cb_last_error``; ``BlendModel`` bundles a
+handle with the device tensors it borrows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcacheblend.so")
+
+CB_OK, CB_ERR_INVALID_ARG, CB_ERR_UNSUPPORTED, CB_ERR_OOM, CB_ERR_CUDA, CB_ERR_INTERNAL = 0, -1, -2, -3, -4, -5
+CB_F32, CB_BF16 = 0, 1
+CB_MAX_CHUNKS = 1024
+EXPORTED = ("cb_model_create", "cb_model_destroy", "cb_rerope", "cb_blend", "cb_selected_count", "cb_last_error")
+
+
+class CbConfig(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("d_model", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("ffn_hidden", ctypes.c_int32),
+                ("vocab", ctypes.c_int32), ("rope_theta", ctypes.c_double), ("rms_eps", ctypes.c_float),
+                ("dtype", ctypes.c_int32), ("max_tokens", ctypes.c_int32), ("max_chunks", ctypes.c_int32)]
+
+
+_PP = ctypes.POINTER(ctypes.c_void_p)
+
+
+class CbWeights(ctypes.Structure):
+    _fields_ = [("embed", ctypes.c_void_p), ("final_norm", ctypes.c_void_p), ("lm_head", ctypes.c_void_p),
+                ("attn_norm", _PP), ("wq", _PP), ("wk", _PP), ("wv", _PP), ("wo", _PP), ("mlp_norm", _PP),
+                ("w_gate", _PP), ("w_up", _PP), ("w_down", _PP)]
+
+
+class CbChunk(ctypes.Structure):
+    _fields_ = [("src_pos", ctypes.c_int32), ("dst_pos", ctypes.c_int32), ("len", ctypes.c_int32)]
+
+
+class CbStats(ctypes.Structure):
+    _fields_ = [("n_tokens", ctypes.c_int32), ("n_ctx", ctypes.c_int32), ("n_selected", ctypes.c_int32),
+                ("n_recompute", ctypes.c_int32), ("kernel_launches", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("gemm_flops", ctypes.c_double), ("attn_flops", ctypes.c_double),
+                ("kv_bytes_moved", ctypes.c_double)]
+
+
+class CacheBlendError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    from . import buildlib
+    return buildlib.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """Load libcacheblend.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libcacheblend.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        L.cb_model_create.restype = ctypes.c_int
+        L.cb_model_create.argtypes = [ctypes.POINTER(CbConfig), ctypes.POINTER(CbWeights), ctypes.POINTER(vp)]
+        L.cb_model_destroy.restype = ctypes.c_int
+        L.cb_model_destroy.argtypes = [vp]
+        L.cb_rerope.restype = ctypes.c_int
+        L.cb_rerope.argtypes = [vp, vp, i64, ctypes.POINTER(CbChunk), i32, vp]
+        L.cb_blend.restype = ctypes.c_int
+        L.cb_blend.argtypes = [vp, vp, i32, vp, ctypes.POINTER(CbChunk), i32, ctypes.c_double, vp, vp, vp, vp,
+                               ctypes.POINTER(CbStats), vp]
+        L.cb_selected_count.restype = i32
+        L.cb_selected_count.argtypes = [i32, ctypes.c_double]
+        L.cb_last_error.restype = ctypes.c_char_p
+        L.cb_last_error.argtypes = []
+        _lib = L
+    return _lib
+
+
+def cb_last_error() -> str:
+    return lib().cb_last_error().decode()
+
+
+def _check(code: int):
+    if code != CB_OK:
+        raise CacheBlendError(code, cb_last_error())
+
+
+def cb_selected_count(n_ctx: int, ratio: float) -> int:
+    return int(lib().cb_selected_count(n_ctx, ratio))
+
+
+def _chunks(chunks):
+    arr = (CbChunk * max(1, len(chunks)))()
+    for i, (s, d, n) in enumerate(chunks):
+        arr[i] = CbChunk(int(s), int(d), int(n))
+    return arr
+
+
+def _ptr(t) -> int:
+    if t is None:
+        return 0
+    return t if isinstance(t, int) else int(t.data_ptr())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return stream if isinstance(stream, int) else int(stream.cuda_stream)
+
+
+def cb_model_create(config: dict, weights: dict) -> int:
+    """config: shape dict (n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn_hidden, vocab, rope_theta,
+    rms_eps, dtype 'bf16'|'f32', max_tokens, max_chunks); weights: device pointers / tensors with keys
+    embed, final_norm, lm_head and 'layers' (list of dicts of per-layer tensors)."""
+    cfg = CbConfig(config["n_layers"], config["d_model"], config["n_heads"], config["n_kv_heads"],
+                   config["head_dim"], config["ffn_hidden"], config["vocab"], float(config["rope_theta"]),
+                   float(config.get("rms_eps", 1e-5)), CB_BF16 if config["dtype"] == "bf16" else CB_F32,
+                   int(config["max_tokens"]), int(config.get("max_chunks", 256)))
+    L = config["n_layers"]
+    tabs = {}
+    for name in ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "w_down"):
+        tabs[name] = (ctypes.c_void_p * L)(*[_ptr(weights["layers"][i][name]) for i in range(L)])
+    w = CbWeights(_ptr(weights["embed"]), _ptr(weights["final_norm"]), _ptr(weights["lm_head"]),
+                  *[ctypes.cast(tabs[n], _PP) for n in ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm",
+                                                         "w_gate", "w_up", "w_down")])
+    h = ctypes.c_void_p()
+    _check(lib().cb_model_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)))
+    return h.value
+
+
+def cb_model_destroy(handle: int) -> None:
+    _check(lib().cb_model_destroy(handle))
+
+
+def cb_rerope(handle: int, kv, n_rows: int, chunks, stream=None) -> None:
+    _check(lib().cb_rerope(handle, _ptr(kv), int(n_rows), _chunks(chunks), len(chunks), _stream(stream)))
+
+
+def cb_blend(handle: int, tokens, n_tokens: int, cached_kv, chunks, ratio: float, out_kv, out_logits,
+             out_selected=None, out_dev=None, stream=None, stats: bool = False):
+    st = CbStats()
+    _check(lib().cb_blend(handle, _ptr(tokens), int(n_tokens), _ptr(cached_kv), _chunks(chunks), len(chunks),
+                          float(ratio), _ptr(out_kv), _ptr(out_logits), _ptr(out_selected), _ptr(out_dev),
+                          ctypes.byref(st) if stats else None, _stream(stream)))
+    if stats:
+        return {f: getattr(st, f) for f, _ in CbStats._fields_}
+    return None
+
+
+# ------------------------------------------------------------------------------------------------
+# convenience: a model handle that owns the device copies of its weights
+# ------------------------------------------------------------------------------------------------
+def to_device(a: np.ndarray, device="cuda"):
+    """numpy float32 or bfloat16-bit-pattern (uint16) array -> torch tensor on the device."""
+    import torch
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+class BlendModel:
+    """A cb_model handle plus the device weights it borrows."""
+
+    def __init__(self, shape: dict, weights: dict, max_tokens: int, max_chunks: int = 256, device="cuda"):
+        import torch
+        self.shape = dict(shape)
+        self.device = torch.device(device)
+        self.weights = {k: to_device(weights[k], device) for k in ("embed", "final_norm", "lm_head")}
+        self.weights["layers"] = [{k: to_device(v, device) for k, v in lw.items()} for lw in weights["layers"]]
+        cfg = dict(shape, max_tokens=max_tokens, max_chunks=max_chunks)
+        self.handle = cb_model_create(cfg, self.weights)
+        self.max_tokens = max_tokens
+        self.kv_dtype = torch.bfloat16 if shape["dtype"] == "bf16" else torch.float32
+
+    def close(self):
+        if self.handle:
+            cb_model_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def kv_buffer(self, n_rows: int):
+        import torch
+        s = self.shape
+        return torch.empty((s["n_layers"], 2, n_rows, s["n_kv_heads"], s["head_dim"]), dtype=self.kv_dtype,
+                           device=self.device)
+
+    def blend(self, tokens, cached_kv, chunks, ratio, out_kv=None, stream=None, want_dev=False, stats=False):
+        """Run cb_blend; returns dict(out_kv, logits, selected, dev?, stats?).  Asynchronous on `stream`."""
+        import torch
+        n = int(tokens.shape[0])
+        n_ctx = sum(c[2] for c in chunks)
+        k = cb_selected_count(n_ctx, ratio)
+        if out_kv is None:
+            out_kv = self.kv_buffer(n)
+        logits = torch.empty(self.shape["vocab"], dtype=torch.float32, device=self.device)
+        sel = torch.empty(max(k, 1), dtype=torch.int32, device=self.device)
+        dev = torch.empty(max(n_ctx, 1), dtype=torch.float32, device=self.device) if want_dev else None
+        st = cb_blend(self.handle, tokens, n, cached_kv, chunks, ratio, out_kv, logits,
+                      sel if k > 0 else None, dev, stream, stats)
+        out = dict(out_kv=out_kv, logits=logits, selected=sel[:k], k=k)
+        if want_dev:
+            out["dev"] = dev[:n_ctx]
+        if stats:
+            out["stats"] = st
+        return out
+
+    def prefill_chunk(self, tokens, stream=None):
+        """A chunk prefilled alone at positions 0..len-1 (cb_blend with no cached chunks): its K/V cache."""
+        return self.blend(tokens, None, [], 0.0, stream=stream)["out_kv"]

@@ -1,0 +1,161 @@
+// Internal declarations shared by the CUDA translation units of libcacheblend.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/cacheblend.h"
+
+namespace cb {
+
+// ------------------------------------------------------------------------------------------------
+// element types
+// ------------------------------------------------------------------------------------------------
+typedef __nv_bfloat16 bf16;
+
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<bf16>(bf16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// device status word bits (model->status); never trap, only record
+enum : unsigned {
+    ST_BAD_TOKEN = 1u,        // a token id outside [0, vocab) was read (embedding left zero)
+    ST_WAIT_TIMEOUT = 2u,     // a bounded mbarrier wait gave up (tensor-core kernels)
+    ST_BAD_ROW = 4u,          // a row index outside the buffer was seen and skipped
+};
+
+// ------------------------------------------------------------------------------------------------
+// GEMM operand description:  Y[r][c] = sum_k X[r][k] * W[c][k]
+//   X   token rows (activations), row-major [rows][K]
+//   W   weight rows, row-major [out][K]; the output columns may be split over up to three
+//       weight matrices ("segments"), e.g. wq | wk | wv.
+// ------------------------------------------------------------------------------------------------
+struct GemmW {
+    const void* w[3];   // segment weight pointers
+    int rows[3];        // rows (output columns) of each segment
+    int nseg;
+    const void* w_up;   // SwiGLU only: the up matrix (w[0] is the gate matrix)
+    int layer;          // layer index (selects tensor maps on the tensor-core path)
+    int which;          // WSEL_* below
+};
+enum { WSEL_QKV = 0, WSEL_Q = 1, WSEL_KV = 2, WSEL_O = 3, WSEL_GATEUP = 4, WSEL_DOWN = 5 };
+
+// epilogue kinds
+enum { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2 };
+
+struct EpiParams {
+    int kind;
+    int M;                 // token rows of this GEMM
+    const int* pos;        // global position of token row r (NULL: pos_offset + r)
+    int pos_offset;
+    // EPI_QKV: output column c is column (c + qkv_base) of the concatenated [q | k | v] space
+    int qkv_base;
+    int nq, nkv, head_dim;
+    void* q_out;           // [M][nq] activation type
+    void* k_dst;           // K rows: storage type at row pos(r) (kv_fresh == 0) or fp32 at row r
+    void* v_dst;
+    int kv_fresh;
+    const float2* rope;    // (cos, sin) [position][head_dim/2]
+    // EPI_RESID: h[r][c] += y  (fp32; atomic when the K range is split)
+    float* h;
+    int ldh;
+    int atomic;
+    // EPI_SWIGLU: act[r][f] = silu(gate) * up
+    void* act;
+    int ld_act;
+};
+
+// ------------------------------------------------------------------------------------------------
+// model
+// ------------------------------------------------------------------------------------------------
+struct TcMaps;   // tensor maps of the tensor-core path (defined in gemm_tc.cu)
+
+struct Model {
+    cb_config cfg;
+    int device;
+    int num_sms;
+    bool bf16;            // cfg.dtype == CB_BF16
+    // borrowed weights
+    const void* embed;
+    const void* final_norm;
+    const void* lm_head;
+    std::vector<const void*> attn_norm, wq, wk, wv, wo, mlp_norm, w_gate, w_up, w_down;
+    // workspace (device)
+    float* h;             // [max_tokens][d] residual stream, all rows
+    float* hA;            // [max_tokens][d] residual stream, recomputed rows
+    void* x;              // [max_tokens][d] normalised activations (activation type)
+    void* xA;             // [max_tokens][d]
+    void* q;              // [max_tokens][nq]
+    void* attn;           // [max_tokens][nq] attention output
+    void* act;            // [max_tokens][ffn] SwiGLU output
+    float* kf;            // [max_tokens][nkv] fresh K at the check layer (fp32)
+    float* vf;            // [max_tokens][nkv] fresh V at the check layer (fp32)
+    float* dev;           // [max_tokens] deviations
+    int* rows;            // [max_tokens] recomputed-row positions (selected ascending, then query)
+    int* iota;            // [max_tokens] 0, 1, 2, ...
+    float2* rope;         // [max_tokens][hd/2]
+    double* inv_freq;     // [hd/2] theta^(-2i/hd)
+    float2* delta_cs;     // [max_chunks][hd/2] rotation of each chunk's position delta
+    int* chunk_dst;       // [max_chunks]
+    int* chunk_delta;     // [max_chunks]
+    float* xfinal;        // [d] final-normed last row
+    unsigned* status;     // device status word (ST_* bits)
+    TcMaps* tc;           // tensor-core path state (NULL if unavailable)
+    size_t ws_bytes;
+};
+
+// ------------------------------------------------------------------------------------------------
+// kernel launchers (return cudaGetLastError())
+// ------------------------------------------------------------------------------------------------
+struct ChunkTable {
+    int n;
+    int dst[CB_MAX_CHUNKS];
+    int len[CB_MAX_CHUNKS];
+    int delta[CB_MAX_CHUNKS];
+};
+
+cudaError_t launch_delta_table(const Model& m, const ChunkTable& t, cudaStream_t s);
+cudaError_t launch_rerope(const Model& m, const void* src, void* dst, int64_t src_rows, int64_t dst_rows,
+                          int n_ctx, int n_chunks, bool copy_v, cudaStream_t s);
+cudaError_t launch_embed(const Model& m, const int* tokens, int n, float* h, cudaStream_t s);
+cudaError_t launch_rmsnorm(const Model& m, const float* h, const void* g, void* out, int n, cudaStream_t s);
+cudaError_t launch_deviation(const Model& m, const float* kf, const float* vf, const void* kv_layer, int64_t kv_rows,
+                             int n_ctx, float* dev, cudaStream_t s);
+cudaError_t launch_topk(const Model& m, const float* dev, int n_ctx, int k, int n_query, int* rows, int* out_sel,
+                        cudaStream_t s);
+cudaError_t launch_gather_scatter(const Model& m, const int* rows, int M, const float* h, float* hA, const void* x,
+                                  void* xA, const float* kf, const float* vf, void* kv_layer, int64_t kv_rows,
+                                  cudaStream_t s);
+cudaError_t launch_attention(const Model& m, const void* q, const int* qpos, int M, const void* kv_layer,
+                             int64_t kv_rows, int n_keys, void* out, cudaStream_t s);
+cudaError_t launch_logits(const Model& m, const float* h_last, float* logits, cudaStream_t s);
+cudaError_t launch_gemm_simt(const Model& m, const void* X, int M, int K, const GemmW& w, int N,
+                             const EpiParams& e, cudaStream_t s);
+
+// tensor-core path (gemm_tc.cu)
+bool tc_init(Model& m, std::string& err);
+void tc_destroy(Model& m);
+cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, const GemmW& w, int N,
+                           const EpiParams& e, cudaStream_t s, int* launches);
+enum { XBUF_X = 0, XBUF_XA = 1, XBUF_ATTN = 2, XBUF_ACT = 3 };
+
+}  // namespace cb

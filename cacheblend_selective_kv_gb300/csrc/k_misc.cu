@@ -1,0 +1,342 @@
+// Memory-bound kernels of the blend step: re-RoPE placement of chunk caches, embedding,
+// RMSNorm, the check-layer KV deviation, gather/scatter of the recomputed rows, and the
+// last-token logits.  All vector accesses are 16 bytes wide and consecutive threads touch
+// consecutive addresses.
+#include "cb_common.cuh"
+
+namespace cb {
+
+// 16-byte vector of 8 storage elements, widened to fp32
+template <typename T> struct Vec8;
+template <> struct Vec8<bf16> {
+    static __device__ __forceinline__ void load(const bf16* p, float* f) {
+        uint4 u = *reinterpret_cast<const uint4*>(p);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 t = __bfloat1622float2(h[i]);
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
+    }
+    static __device__ __forceinline__ void store(bf16* p, const float* f) {
+        uint4 u;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+        *reinterpret_cast<uint4*>(p) = u;
+    }
+};
+template <> struct Vec8<float> {
+    static __device__ __forceinline__ void load(const float* p, float* f) {
+        float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    }
+    static __device__ __forceinline__ void store(float* p, const float* f) {
+        reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+        reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
+};
+
+static inline int grid_for(int64_t items, int threads, int sms, int per_sm = 8) {
+    int64_t b = (items + threads - 1) / threads;
+    int64_t cap = (int64_t)sms * per_sm;
+    return (int)(b < cap ? (b > 0 ? b : 1) : cap);
+}
+
+// ------------------------------------------------------------------------------------------------
+// (cos, sin) of each chunk's position delta, in float64, and the chunk tables.
+// ------------------------------------------------------------------------------------------------
+__global__ void delta_table_kernel(ChunkTable t, const double* inv_freq, int half, float2* cs, int* dst,
+                                   int* delta) {
+    const int c = blockIdx.x;
+    if (c >= t.n) return;
+    if (threadIdx.x == 0) {
+        dst[c] = t.dst[c];
+        delta[c] = t.delta[c];
+    }
+    for (int i = threadIdx.x; i < half; i += blockDim.x) {
+        double s, co;
+        sincos((double)t.delta[c] * inv_freq[i], &s, &co);
+        cs[(size_t)c * half + i] = make_float2((float)co, (float)s);
+    }
+}
+
+cudaError_t launch_delta_table(const Model& m, const ChunkTable& t, cudaStream_t s) {
+    const int half = m.cfg.head_dim / 2;
+    delta_table_kernel<<<t.n, 64, 0, s>>>(t, m.inv_freq, half, m.delta_cs, m.chunk_dst, m.chunk_delta);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------------
+// Re-RoPE placement: dst K row j = R_{delta(chunk of j)} src K row j; dst V row j = src V row j.
+// src and dst are [L][2][rows][W]; they may be the same buffer with the same row count.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ int chunk_of(const int* dst, int n, int j) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {                       // last chunk with dst <= j
+        int mid = (lo + hi + 1) >> 1;
+        if (dst[mid] <= j) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <typename T>
+__global__ void rerope_kernel(const T* __restrict__ src, T* __restrict__ dst, int64_t src_rows, int64_t dst_rows,
+                              int n_ctx, int W, int hd, int L, int kv_count, const int* __restrict__ cdst,
+                              const float2* __restrict__ cs, int n_chunks) {
+    const int W8 = W / 8, half = hd / 2;
+    const int64_t per_lk = (int64_t)n_ctx * W8;
+    const int64_t total = (int64_t)L * kv_count * per_lk;
+    for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+         it += (int64_t)gridDim.x * blockDim.x) {
+        const int lk = (int)(it / per_lk);
+        const int rem = (int)(it - (int64_t)lk * per_lk);
+        const int j = rem / W8, e = (rem - j * W8) * 8;
+        const int layer = lk / kv_count, kv = lk - layer * kv_count;
+        const T* sp = src + (((int64_t)layer * 2 + kv) * src_rows + j) * W + e;
+        T* dp = dst + (((int64_t)layer * 2 + kv) * dst_rows + j) * W + e;
+        float f[8];
+        Vec8<T>::load(sp, f);
+        if (kv == 0) {
+            const int c = chunk_of(cdst, n_chunks, j);
+            const float2* t = cs + (size_t)c * half + (e % hd) / 2;
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const float2 r = t[p];
+                const float x0 = f[2 * p], x1 = f[2 * p + 1];
+                f[2 * p] = x0 * r.x - x1 * r.y;
+                f[2 * p + 1] = x0 * r.y + x1 * r.x;
+            }
+        }
+        Vec8<T>::store(dp, f);
+    }
+}
+
+cudaError_t launch_rerope(const Model& m, const void* src, void* dst, int64_t src_rows, int64_t dst_rows, int n_ctx,
+                          int n_chunks, bool copy_v, cudaStream_t s) {
+    const cb_config& c = m.cfg;
+    const int W = c.n_kv_heads * c.head_dim, kvc = copy_v ? 2 : 1;
+    const int64_t items = (int64_t)c.n_layers * kvc * n_ctx * (W / 8);
+    if (items == 0) return cudaSuccess;
+    const int grid = grid_for(items, 256, m.num_sms, 16);
+    if (m.bf16)
+        rerope_kernel<bf16><<<grid, 256, 0, s>>>((const bf16*)src, (bf16*)dst, src_rows, dst_rows, n_ctx, W,
+                                                 c.head_dim, c.n_layers, kvc, m.chunk_dst, m.delta_cs, n_chunks);
+    else
+        rerope_kernel<float><<<grid, 256, 0, s>>>((const float*)src, (float*)dst, src_rows, dst_rows, n_ctx, W,
+                                                  c.head_dim, c.n_layers, kvc, m.chunk_dst, m.delta_cs, n_chunks);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------------
+// embedding: h[r] = E[token r] (fp32)
+// ------------------------------------------------------------------------------------------------
+template <typename T>
+__global__ void embed_kernel(const int* __restrict__ tokens, const T* __restrict__ E, int vocab, int d, float* h,
+                             unsigned* status) {
+    const int r = blockIdx.x;
+    const int t = tokens[r];
+    float* out = h + (size_t)r * d;
+    if (t < 0 || t >= vocab) {
+        if (threadIdx.x == 0) atomicOr(status, ST_BAD_TOKEN);
+        for (int e = threadIdx.x; e < d; e += blockDim.x) out[e] = 0.f;
+        return;
+    }
+    const T* row = E + (size_t)t * d;
+    for (int e = threadIdx.x * 8; e < d; e += blockDim.x * 8) {
+        float f[8];
+        Vec8<T>::load(row + e, f);
+        reinterpret_cast<float4*>(out + e)[0] = make_float4(f[0], f[1], f[2], f[3]);
+        reinterpret_cast<float4*>(out + e)[1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
+}
+
+cudaError_t launch_embed(const Model& m, const int* tokens, int n, float* h, cudaStream_t s) {
+    if (m.bf16)
+        embed_kernel<bf16><<<n, 128, 0, s>>>(tokens, (const bf16*)m.embed, m.cfg.vocab, m.cfg.d_model, h, m.status);
+    else
+        embed_kernel<float><<<n, 128, 0, s>>>(tokens, (const float*)m.embed, m.cfg.vocab, m.cfg.d_model, h, m.status);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------------
+// RMSNorm: out[r] = g * h[r] / sqrt(mean(h[r]^2) + eps), stored in the activation type
+// ------------------------------------------------------------------------------------------------
+template <typename T>
+__global__ void rmsnorm_kernel(const float* __restrict__ h, const T* __restrict__ g, T* __restrict__ out, int d,
+                               float eps) {
+    const int r = blockIdx.x;
+    const float* row = h + (size_t)r * d;
+    __shared__ float red[32];
+    float ss = 0.f;
+    for (int e = threadIdx.x * 4; e < d; e += blockDim.x * 4) {
+        float4 v = *reinterpret_cast<const float4*>(row + e);
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+        v = warp_sum(v);
+        if (threadIdx.x == 0) red[0] = v;
+    }
+    __syncthreads();
+    const float scale = 1.0f / sqrtf(red[0] / (float)d + eps);
+    T* o = out + (size_t)r * d;
+    for (int e = threadIdx.x * 8; e < d; e += blockDim.x * 8) {
+        float f[8], gg[8];
+        float4 a = *reinterpret_cast<const float4*>(row + e), b = *reinterpret_cast<const float4*>(row + e + 4);
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+        Vec8<T>::load(g + e, gg);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = f[i] * scale * gg[i];
+        Vec8<T>::store(o + e, f);
+    }
+}
+
+cudaError_t launch_rmsnorm(const Model& m, const float* h, const void* g, void* out, int n, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    if (m.bf16)
+        rmsnorm_kernel<bf16><<<n, 256, 0, s>>>(h, (const bf16*)g, (bf16*)out, m.cfg.d_model, m.cfg.rms_eps);
+    else
+        rmsnorm_kernel<float><<<n, 256, 0, s>>>(h, (const float*)g, (float*)out, m.cfg.d_model, m.cfg.rms_eps);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------------
+// KV deviation at the check layer (CacheBlend deep-dive page, section "核心思想", Δkv formula):
+// dev[j] = sum over KV heads and dims of (k_new - k_pre)^2 + (v_new - v_pre)^2,
+// with fresh fp32 K/V and the re-RoPE'd stored cache.  One warp per row.
+// ------------------------------------------------------------------------------------------------
+template <typename T>
+__global__ void deviation_kernel(const float* __restrict__ kf, const float* __restrict__ vf,
+                                 const T* __restrict__ kv_layer, int64_t kv_rows, int n_ctx, int W, float* dev) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (warp >= n_ctx) return;
+    const T* kc = kv_layer + (int64_t)warp * W;
+    const T* vc = kv_layer + (kv_rows + warp) * (int64_t)W;
+    const float* kn = kf + (int64_t)warp * W;
+    const float* vn = vf + (int64_t)warp * W;
+    float acc = 0.f;
+    for (int e = lane * 8; e < W; e += 256) {
+        float a[8], b[8];
+        Vec8<T>::load(kc + e, a);
+        Vec8<float>::load(kn + e, b);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { float t = b[i] - a[i]; acc += t * t; }
+        Vec8<T>::load(vc + e, a);
+        Vec8<float>::load(vn + e, b);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { float t = b[i] - a[i]; acc += t * t; }
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) dev[warp] = acc;
+}
+
+cudaError_t launch_deviation(const Model& m, const float* kf, const float* vf, const void* kv_layer, int64_t kv_rows,
+                             int n_ctx, float* dev, cudaStream_t s) {
+    if (n_ctx <= 0) return cudaSuccess;
+    const int W = m.cfg.n_kv_heads * m.cfg.head_dim;
+    const int grid = (n_ctx + 7) / 8;
+    if (m.bf16)
+        deviation_kernel<bf16><<<grid, 256, 0, s>>>(kf, vf, (const bf16*)kv_layer, kv_rows, n_ctx, W, dev);
+    else
+        deviation_kernel<float><<<grid, 256, 0, s>>>(kf, vf, (const float*)kv_layer, kv_rows, n_ctx, W, dev);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------------
+// Recomputed rows at the check layer: compact their hidden state and normalised input, and store
+// their fresh K/V into the blended cache before attention (Figure 5: assemble the complete K/V).
+// ------------------------------------------------------------------------------------------------
+template <typename T>
+__global__ void gather_scatter_kernel(const int* __restrict__ rows, const float* __restrict__ h, float* __restrict__ hA,
+                                      const T* __restrict__ x, T* __restrict__ xA, const float* __restrict__ kf,
+                                      const float* __restrict__ vf, T* kv_layer, int64_t kv_rows, int d, int W) {
+    const int i = blockIdx.x;
+    const int r = rows[i];
+    for (int e = threadIdx.x * 4; e < d; e += blockDim.x * 4)
+        *reinterpret_cast<float4*>(hA + (size_t)i * d + e) = *reinterpret_cast<const float4*>(h + (size_t)r * d + e);
+    for (int e = threadIdx.x * 8; e < d; e += blockDim.x * 8) {
+        float f[8];
+        Vec8<T>::load(x + (size_t)r * d + e, f);
+        Vec8<T>::store(xA + (size_t)i * d + e, f);
+    }
+    for (int e = threadIdx.x * 8; e < W; e += blockDim.x * 8) {
+        float f[8];
+        Vec8<float>::load(kf + (size_t)r * W + e, f);
+        Vec8<T>::store(kv_layer + (int64_t)r * W + e, f);
+        Vec8<float>::load(vf + (size_t)r * W + e, f);
+        Vec8<T>::store(kv_layer + (kv_rows + r) * (int64_t)W + e, f);
+    }
+}
+
+cudaError_t launch_gather_scatter(const Model& m, const int* rows, int M, const float* h, float* hA, const void* x,
+                                  void* xA, const float* kf, const float* vf, void* kv_layer, int64_t kv_rows,
+                                  cudaStream_t s) {
+    const int d = m.cfg.d_model, W = m.cfg.n_kv_heads * m.cfg.head_dim;
+    if (m.bf16)
+        gather_scatter_kernel<bf16><<<M, 256, 0, s>>>(rows, h, hA, (const bf16*)x, (bf16*)xA, kf, vf, (bf16*)kv_layer,
+                                                      kv_rows, d, W);
+    else
+        gather_scatter_kernel<float><<<M, 256, 0, s>>>(rows, h, hA, (const float*)x, (float*)xA, kf, vf,
+                                                       (float*)kv_layer, kv_rows, d, W);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------------
+// Logits of the last row: final RMSNorm (recomputed per block, d floats) then a GEMV over the
+// vocabulary; one warp per vocabulary row, 16-byte loads.  HBM-bound on the LM-head read.
+// ------------------------------------------------------------------------------------------------
+template <typename T>
+__global__ void logits_kernel(const float* __restrict__ hl, const T* __restrict__ g, const T* __restrict__ Wh,
+                              int d, int vocab, float eps, float* __restrict__ out) {
+    extern __shared__ float xs[];
+    __shared__ float red[32];
+    float ss = 0.f;
+    for (int e = threadIdx.x; e < d; e += blockDim.x) { float v = hl[e]; ss += v * v; }
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+        v = warp_sum(v);
+        if (threadIdx.x == 0) red[0] = v;
+    }
+    __syncthreads();
+    const float scale = 1.0f / sqrtf(red[0] / (float)d + eps);
+    for (int e = threadIdx.x; e < d; e += blockDim.x) xs[e] = hl[e] * scale * to_f(g[e]);
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int warps = (gridDim.x * blockDim.x) >> 5;
+    for (int v = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; v < vocab; v += warps) {
+        const T* row = Wh + (size_t)v * d;
+        float acc = 0.f;
+        for (int e = lane * 8; e < d; e += 256) {
+            float f[8];
+            Vec8<T>::load(row + e, f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc += f[i] * xs[e + i];
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) out[v] = acc;
+    }
+}
+
+cudaError_t launch_logits(const Model& m, const float* h_last, float* logits, cudaStream_t s) {
+    const int d = m.cfg.d_model;
+    const int grid = m.num_sms * 4;
+    if (m.bf16)
+        logits_kernel<bf16><<<grid, 256, d * sizeof(float), s>>>(h_last, (const bf16*)m.final_norm,
+                                                                 (const bf16*)m.lm_head, d, m.cfg.vocab,
+                                                                 m.cfg.rms_eps, logits);
+    else
+        logits_kernel<float><<<grid, 256, d * sizeof(float), s>>>(h_last, (const float*)m.final_norm,
+                                                                  (const float*)m.lm_head, d, m.cfg.vocab,
+                                                                  m.cfg.rms_eps, logits);
+    return cudaGetLastError();
+}
+
+}  // namespace cb

@@ -1,0 +1,162 @@
+/*
+ * cacheblend.h -- C ABI of the GB300 CacheBlend blend-step library (libcacheblend.so).
+ *
+ * The library computes the per-request blend step of CacheBlend for non-prefix KV
+ * reuse, as described on the CacheBlend deep-dive page ("CacheBlend 完全拆解:RAG 多段
+ * KV 缓存拼接,为什么还要重算一小部分 token"):
+ *   - precomputed chunk caches are placed at new offsets and their K re-rotated
+ *     (section "位置恢复、KV 存储与加载流水线", re-RoPE identity k' = R_{n-p} k_p = R_n k);
+ *   - the check layer is computed for every token and each token's KV deviation
+ *     ||KV_new[j] - KV_pre[j]||^2 ranks the tokens (section "核心思想", Δkv formula);
+ *   - the top-r fraction (HKVD tokens) plus the query are recomputed in every later
+ *     layer against the blended K/V (section "选 token", Figure 5 and Figure 9).
+ *
+ * Conventions for every entry point:
+ *   - Pointers documented as "device" must be CUDA device (or managed) memory on the
+ *     current device; "host" pointers are ordinary host memory read during the call.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).  All
+ *     GPU work is enqueued on it; calls return without synchronising the host.
+ *   - Arguments are validated on the host before anything is enqueued; on any error
+ *     nothing is enqueued, the return code is negative and cb_last_error() describes it.
+ *   - No entry point aborts or throws; CUDA launch failures map to CB_ERR_CUDA.
+ *   - Calls on one model handle must not run concurrently (they share its workspace).
+ */
+#ifndef CACHEBLEND_H
+#define CACHEBLEND_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CB_OK = 0,
+    CB_ERR_INVALID_ARG = -1,   /* a pointer, size, layout or ratio is out of range */
+    CB_ERR_UNSUPPORTED = -2,   /* valid but not supported by this build (e.g. head_dim) */
+    CB_ERR_OOM = -3,           /* workspace allocation failed at model creation */
+    CB_ERR_CUDA = -4,          /* a CUDA call or kernel launch failed */
+    CB_ERR_INTERNAL = -5
+} cb_status;
+
+typedef enum { CB_F32 = 0, CB_BF16 = 1 } cb_dtype;
+
+/* Llama-style pre-norm decoder shape.  Supported: head_dim in {64, 128},
+ * n_heads % n_kv_heads == 0, n_layers >= 2, d_model and ffn_hidden multiples of 64. */
+typedef struct {
+    int32_t n_layers;
+    int32_t d_model;
+    int32_t n_heads;         /* query heads */
+    int32_t n_kv_heads;      /* K/V heads (GQA: q-head h reads KV head h / (n_heads/n_kv_heads)) */
+    int32_t head_dim;
+    int32_t ffn_hidden;      /* SwiGLU hidden width */
+    int32_t vocab;
+    double rope_theta;       /* RoPE base: dims (2i, 2i+1) rotate by angle pos * theta^(-2i/head_dim) */
+    float rms_eps;           /* RMSNorm epsilon */
+    int32_t dtype;           /* cb_dtype of weights, K/V caches and tensor-core operands */
+    int32_t max_tokens;      /* largest n_tokens (context + query) a blend may use; sizes the workspace */
+    int32_t max_chunks;      /* largest n_chunks a call may pass (<= CB_MAX_CHUNKS) */
+} cb_config;
+
+#define CB_MAX_CHUNKS 1024
+
+/* Weights, borrowed (not copied): they must stay valid until cb_model_destroy.
+ * Every matrix is row-major [out_features][in_features] in cfg.dtype ("nn.Linear" layout):
+ *   embed, lm_head [vocab][d_model]; wq [n_heads*head_dim][d_model];
+ *   wk, wv [n_kv_heads*head_dim][d_model]; wo [d_model][n_heads*head_dim];
+ *   w_gate, w_up [ffn_hidden][d_model]; w_down [d_model][ffn_hidden];
+ *   attn_norm, mlp_norm, final_norm [d_model] (RMSNorm gains).
+ * The per-layer members are HOST arrays of n_layers DEVICE pointers; the arrays are
+ * copied at creation.  Device pointers must be 16-byte aligned. */
+typedef struct {
+    const void* embed;
+    const void* final_norm;
+    const void* lm_head;
+    const void* const* attn_norm;
+    const void* const* wq;
+    const void* const* wk;
+    const void* const* wv;
+    const void* const* wo;
+    const void* const* mlp_norm;
+    const void* const* w_gate;
+    const void* const* w_up;
+    const void* const* w_down;
+} cb_weights;
+
+/* One placed chunk: its cache rows were computed at positions src_pos .. src_pos+len-1
+ * (the chunk's old start) and now sit at dst_pos .. dst_pos+len-1 (its current start).
+ * A negative src_pos means "position unknown" and is rejected: rotating from a wrong
+ * source position would silently produce wrong keys. */
+typedef struct {
+    int32_t src_pos;
+    int32_t dst_pos;
+    int32_t len;
+} cb_chunk;
+
+/* Host-side accounting of one blend (filled when `stats` is non-NULL). */
+typedef struct {
+    int32_t n_tokens;        /* N = n_ctx + n_query */
+    int32_t n_ctx;           /* context rows (sum of chunk lengths) */
+    int32_t n_selected;      /* k = HKVD rows chosen at the check layer */
+    int32_t n_recompute;     /* M = k + n_query rows recomputed in layers >= 1 */
+    int32_t kernel_launches; /* kernels enqueued by this call */
+    int32_t reserved;
+    double gemm_flops;       /* algorithmic FLOPs of all projections */
+    double attn_flops;       /* algorithmic FLOPs of attention (causal key counts) */
+    double kv_bytes_moved;   /* algorithmic bytes of re-RoPE/placement, deviation and K/V scatter */
+} cb_stats;
+
+typedef struct cb_model cb_model;
+
+/* Create a model handle: copies the config and the weight pointer tables, allocates the
+ * device workspace for cfg.max_tokens rows and the RoPE tables (computed in float64 on
+ * the host, stored as float32) on the current device.  Synchronous.
+ * Errors: CB_ERR_INVALID_ARG (bad shape / null pointer), CB_ERR_UNSUPPORTED,
+ * CB_ERR_OOM (workspace), CB_ERR_CUDA. */
+cb_status cb_model_create(const cb_config* cfg, const cb_weights* weights, cb_model** out);
+
+/* Free the workspace (synchronises the device).  NULL is accepted. */
+cb_status cb_model_destroy(cb_model* model);
+
+/* In-place re-RoPE of a chunk-cache buffer (re-RoPE identity, section
+ * "位置恢复、KV 存储与加载流水线"): for every chunk c and every layer, the K rows
+ * dst_pos_c .. dst_pos_c+len_c-1 are rotated by R_{dst_pos_c - src_pos_c}; V is untouched.
+ *   kv      device, [n_layers][2][n_rows][n_kv_heads][head_dim] in cfg.dtype (2 = K, V)
+ *   chunks  host, n_chunks entries; they must tile [0, sum len) in dst order and
+ *           sum len <= n_rows.
+ * Async on `stream`. */
+cb_status cb_rerope(cb_model* model, void* kv, int64_t n_rows, const cb_chunk* chunks, int32_t n_chunks,
+                    void* stream);
+
+/* One blend (sections "核心思想" and "选 token"; Figures 5 and 9):
+ *   tokens       device int32 [n_tokens]: the context tokens in placed order, then the query.
+ *   cached_kv    device [n_layers][2][n_ctx][n_kv_heads][head_dim] (cfg.dtype): the chunk
+ *                caches concatenated in placed order, K still rotated at each chunk's src_pos.
+ *                May be NULL when n_chunks == 0.
+ *   chunks       host, n_chunks entries tiling [0, n_ctx) in dst order (n_ctx = sum len).
+ *                n_chunks == 0 makes the call a plain causal prefill of `tokens`.
+ *   ratio        fraction r in [0, 1]; k = ceil(r * n_ctx) context rows are recomputed.
+ *   out_kv       device [n_layers][2][n_tokens][n_kv_heads][head_dim] (cfg.dtype): the blended
+ *                K/V.  out_kv == cached_kv is allowed (in-place blend, rows 0..n_ctx-1).
+ *                Other overlap between the two is not.
+ *   out_logits   device float32 [vocab]: logits of the last token.
+ *   out_selected device int32 [k] or NULL: the chosen context rows, ascending.
+ *   out_dev      device float32 [n_ctx] or NULL: every context row's deviation at the check layer.
+ *   stats        host or NULL: accounting of the call.
+ * Requires 0 < n_tokens <= max_tokens and n_tokens > n_ctx (at least one query token).
+ * Async on `stream`; no device memory is allocated. */
+cb_status cb_blend(cb_model* model, const int32_t* tokens, int32_t n_tokens, const void* cached_kv,
+                   const cb_chunk* chunks, int32_t n_chunks, double ratio, void* out_kv, float* out_logits,
+                   int32_t* out_selected, float* out_dev, cb_stats* stats, void* stream);
+
+/* k = ceil(ratio * n_ctx - 1e-9) clamped to [0, n_ctx]; -1 if ratio is outside [0, 1] or NaN. */
+int32_t cb_selected_count(int32_t n_ctx, double ratio);
+
+/* Description of the last error on the calling thread ("" if none). */
+const char* cb_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CACHEBLEND_H */

@@ -260,7 +260,7 @@ def validate_chunks(chunks, n_tokens: int) -> int:
     return at
 
 
-def blend(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratio: float, store: str) -> dict:
+def blend(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratio: float, store: str, selected=None) -> dict:
     """One CacheBlend blend (sections "核心思想" and "选 token", Figures 5 and 9).
 
     1. re-RoPE the cached chunk K/V to their placed positions (V copied);
@@ -272,6 +272,9 @@ def blend(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratio: float, sto
        A's fresh K/V are stored; A attends over the blended K/V; O and MLP on A;
     5. layers 2..L-1: only A's rows: QKV, store, attend, O, MLP;
     6. logits of the last row.
+
+    ``selected`` (optional) replaces the top-k choice by a given set of k rows -- used only
+    to follow another implementation through a tie inside the comparison band.
 
     Returns dict(out_kv [L][2][N][Hkv][hd] float64, logits [V], selected [k],
     dev [n_ctx], k)."""
@@ -305,7 +308,8 @@ def blend(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratio: float, sto
     dev = deviation(k_new[:n_ctx], v_new[:n_ctx], out_kv[1, 0, :n_ctx].astype(np.float64),
                     out_kv[1, 1, :n_ctx].astype(np.float64))
     kk = selected_count(n_ctx, ratio)
-    sel = select_hkvd(dev, kk)
+    sel = select_hkvd(dev, kk) if selected is None else np.sort(np.asarray(selected, np.int64))
+    assert len(sel) == kk
     A = np.concatenate([sel, np.arange(n_ctx, N)])
     out_kv[1, 0, A] = round_store(k_new[A], store)
     out_kv[1, 1, A] = round_store(v_new[A], store)

@@ -1,0 +1,189 @@
+"""GPU parity: the CUDA library, called through its C ABI, against the CPU oracle on the same seeded
+inputs.  Tolerances are in tests/parity.py."""
+import numpy as np
+import pytest
+
+import oracle
+import parity
+import workload
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def cb():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import cacheblend_selective_kv_gb300 as cbm
+    return cbm
+
+
+_cache = {}
+
+
+def setup_case(name, seed=None, ratio=None, synthetic=False):
+    """Weights, request and chunk caches for a named workload (cached per module)."""
+    spec = workload.WORKLOADS[name]
+    seed = spec.seeds[0] if seed is None else seed
+    ratio = spec.ratios[0] if ratio is None else ratio
+    key = (name, seed, synthetic)
+    if key not in _cache:
+        shape = spec.shape
+        w = workload.make_weights(shape, seed)
+        req = workload.make_request(spec, seed, ratio)
+        if synthetic:
+            caches = workload.synthetic_cache(shape, seed, spec.n_ctx, workload.kv_std(shape))
+        else:
+            caches = oracle.chunk_caches(shape.as_dict(), w, req.chunk_tokens, req.chunks, shape.dtype)
+            if shape.dtype == "bf16":
+                caches = caches.astype(np.float32)
+        _cache.clear()
+        _cache[key] = (spec, w, req, caches)
+    spec, w, req, caches = _cache[key]
+    return spec, w, req, caches, ratio
+
+
+def cached_tensor(caches, dtype):
+    if caches.dtype == np.uint16:
+        return torch.from_numpy(caches.view(np.int16)).cuda().view(torch.bfloat16)
+    t = torch.from_numpy(np.ascontiguousarray(caches, dtype=np.float32)).cuda()
+    return t.to(torch.bfloat16) if dtype == "bf16" else t
+
+
+def run_and_compare(cb, name, ratio=None, synthetic=False, seed=None, model=None):
+    spec, w, req, caches, ratio = setup_case(name, seed, ratio, synthetic)
+    shape = spec.shape.as_dict()
+    store = spec.shape.dtype
+    own = model is None
+    if own:
+        model = cb.BlendModel(shape, w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks)
+    tokens = torch.from_numpy(req.tokens).cuda()
+    out = model.blend(tokens, cached_tensor(caches, store), req.chunks, ratio, want_dev=True)
+    torch.cuda.synchronize()
+    ref = oracle.blend(shape, w, req.tokens, caches, req.chunks, ratio, store)
+    g_sel = out["selected"].cpu().numpy()
+    g_dev = out["dev"].cpu().numpy().astype(np.float64)
+    diff = parity.assert_selection(g_sel, ref["selected"], ref["dev"], ref["k"])
+    if diff:   # follow the GPU through a tie inside the band
+        ref = oracle.blend(shape, w, req.tokens, caches, req.chunks, ratio, store, selected=g_sel)
+    rel_dev = np.max(np.abs(g_dev - ref["dev"]) / (np.abs(ref["dev"]) + 1e-6 * ref["dev"].max()))
+    kv_err = parity.assert_kv(parity.bf16_to_f64(out["out_kv"]), ref["out_kv"], store)
+    lg_err = parity.assert_logits(parity.bf16_to_f64(out["logits"]), ref["logits"], store)
+    if own:
+        model.close()
+    return dict(kv_err=kv_err, logits_err=lg_err, dev_rel=float(rel_dev), n_diff=len(diff), k=ref["k"])
+
+
+def test_tiny_fp32_blend(cb):
+    r = run_and_compare(cb, "tiny-fp32")
+    print(r)
+    assert r["dev_rel"] < 1e-4
+
+
+@pytest.mark.parametrize("ratio", [0.0, 0.01, 0.5, 1.0])
+def test_tiny_fp32_ratio_extremes(cb, ratio):
+    run_and_compare(cb, "tiny-fp32", ratio=ratio)
+
+
+def test_small_bf16_blend(cb):
+    r = run_and_compare(cb, "small-bf16")
+    print(r)
+
+
+def test_tiny_prefill_matches_oracle(cb):
+    spec, w, req, _, _ = setup_case("tiny-fp32")
+    shape = spec.shape.as_dict()
+    model = cb.BlendModel(shape, w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks)
+    toks = req.chunk_tokens[1]
+    kv = model.prefill_chunk(torch.from_numpy(toks).cuda())
+    torch.cuda.synchronize()
+    ref = oracle.prefill(shape, w, toks, "f32")
+    parity.assert_kv(parity.bf16_to_f64(kv), ref["out_kv"], "f32", "prefill K/V")
+    model.close()
+
+
+def test_inplace_blend_equals_out_of_place(cb):
+    spec, w, req, caches, ratio = setup_case("small-bf16")
+    shape = spec.shape.as_dict()
+    model = cb.BlendModel(shape, w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks)
+    tokens = torch.from_numpy(req.tokens).cuda()
+    cached = cached_tensor(caches, "bf16")
+    a = model.blend(tokens, cached, req.chunks, ratio)
+    buf = model.kv_buffer(spec.n_tokens)
+    buf[:, :, :spec.n_ctx] = cached
+    b = model.blend(tokens, buf, req.chunks, ratio, out_kv=buf)
+    torch.cuda.synchronize()
+    assert torch.equal(a["selected"], b["selected"])
+    assert torch.equal(a["out_kv"], b["out_kv"])
+    assert torch.equal(a["logits"], b["logits"])
+    model.close()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_rerope_in_place(cb, dtype):
+    """cb_rerope rotates K of every layer by each chunk's delta and leaves V alone."""
+    shape = dict(workload.TINY.as_dict(), dtype=dtype)
+    ms = workload.ModelShape(**{k: v for k, v in shape.items()})
+    w = workload.make_weights(ms, 0)
+    model = cb.BlendModel(shape, w, max_tokens=64, max_chunks=8)
+    chunks = [(0, 0, 5), (100, 5, 17), (3, 22, 9), (40000, 31, 1), (7, 32, 30)]   # ragged, src past dst
+    n_rows = 70
+    raw = workload.normal(5, 77, (2, 2, n_rows, 2, 64), 1.0, dtype)
+    ref = oracle.rerope(raw, chunks, shape["rope_theta"], dtype)
+    kv = cb.to_device(raw)
+    cb.cb_rerope(model.handle, kv, n_rows, chunks)
+    torch.cuda.synchronize()
+    got = parity.bf16_to_f64(kv)
+    n_ctx = sum(c[2] for c in chunks)
+    base = oracle.to_f64(raw)
+    assert np.array_equal(got[:, 1], base[:, 1]), "V changed"
+    assert np.array_equal(got[:, :, n_ctx:], base[:, :, n_ctx:]), "rows past the chunks changed"
+    tol = 1e-5 if dtype == "f32" else 0.0
+    err = np.abs(got[:, 0, :n_ctx] - ref[:, 0, :n_ctx])
+    if dtype == "bf16":   # a rotation rounded once to bf16: allow one ulp of the result
+        ulp = np.ldexp(1.0, np.frexp(np.abs(ref[:, 0, :n_ctx]))[1] - 8)
+        assert np.all(err <= ulp), float(err.max())
+    else:
+        assert err.max() <= tol, float(err.max())
+    model.close()
+
+
+def test_topk_is_exact_on_gpu_deviations(cb):
+    """The GPU's set is exactly the top-k (ties to the lower row) of the GPU's own deviations."""
+    spec, w, req, caches, _ = setup_case("small-bf16")
+    shape = spec.shape.as_dict()
+    model = cb.BlendModel(shape, w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks)
+    tokens = torch.from_numpy(req.tokens).cuda()
+    for ratio in (0.0, 0.001, 0.15, 0.5, 0.999, 1.0):
+        out = model.blend(tokens, cached_tensor(caches, "bf16"), req.chunks, ratio, want_dev=True)
+        torch.cuda.synchronize()
+        dev = out["dev"].cpu().numpy()
+        assert list(out["selected"].cpu().numpy()) == list(oracle.select_hkvd(dev.astype(np.float64), out["k"]))
+    model.close()
+
+
+def test_validation_errors_enqueue_nothing(cb):
+    spec, w, req, caches, _ = setup_case("tiny-fp32")
+    shape = spec.shape.as_dict()
+    model = cb.BlendModel(shape, w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks)
+    tokens = torch.from_numpy(req.tokens).cuda()
+    cached = cached_tensor(caches, "f32")
+    bad = [
+        dict(ratio=1.5), dict(ratio=-0.1), dict(ratio=float("nan")),
+        dict(chunks=[(0, 0, 64), (0, 65, 64), (0, 129, 63)]),           # gap
+        dict(chunks=[(0, 0, 64), (-1, 64, 64), (0, 128, 64)]),          # unknown source position
+        dict(chunks=[(0, 0, 64), (0, 32, 64), (0, 96, 96)]),            # overlap
+        dict(chunks=[(0, 0, 208)]),                                      # no query token
+    ]
+    for b in bad:
+        with pytest.raises(cb.CacheBlendError) as ei:
+            model.blend(tokens, cached, b.get("chunks", req.chunks), b.get("ratio", 0.25))
+        assert ei.value.code == cb.CB_ERR_INVALID_ARG
+    with pytest.raises(cb.CacheBlendError):
+        big = torch.zeros(spec.n_tokens + 1, dtype=torch.int32, device="cuda")
+        model.blend(big, cached, req.chunks, 0.25)
+    torch.cuda.synchronize()
+    model.close()

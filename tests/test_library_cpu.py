@@ -1,0 +1,99 @@
+"""The C-ABI library builds, loads and exports every symbol the header declares; host-side
+validation that needs no GPU."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import cacheblend_selective_kv_gb300 as cb
+from oracle import selected_count
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    return cb.lib()
+
+
+def declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(cb_[a-z_0-9]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for n in cb.EXPORTED:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_symbols():
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_selected_count_matches_oracle(lib):
+    for n in (0, 1, 7, 192, 2048, 3072, 8192, 32768):
+        for r in (0.0, 0.05, 0.1, 0.15, 0.25, 0.3, 0.5, 0.999, 1.0):
+            assert cb.cb_selected_count(n, r) == selected_count(n, r), (n, r)
+    assert cb.cb_selected_count(10, -0.1) == -1
+    assert cb.cb_selected_count(10, 1.5) == -1
+    assert cb.cb_selected_count(10, float("nan")) == -1
+
+
+def _cfg(**kw):
+    c = dict(n_layers=2, d_model=256, n_heads=4, n_kv_heads=2, head_dim=64, ffn_hidden=512, vocab=1024,
+             rope_theta=1e4, rms_eps=1e-5, dtype="f32", max_tokens=256, max_chunks=8)
+    c.update(kw)
+    return c
+
+
+def _fake_weights(L, ptr=4096):
+    layer = {k: ptr for k in ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "w_down")}
+    return dict(embed=ptr, final_norm=ptr, lm_head=ptr, layers=[dict(layer) for _ in range(L)])
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(head_dim=96), cb.CB_ERR_UNSUPPORTED),
+    (dict(n_heads=6, n_kv_heads=4), cb.CB_ERR_INVALID_ARG),
+    (dict(n_layers=1), cb.CB_ERR_INVALID_ARG),
+    (dict(d_model=200), cb.CB_ERR_UNSUPPORTED),
+    (dict(max_tokens=0), cb.CB_ERR_INVALID_ARG),
+    (dict(max_chunks=cb.CB_MAX_CHUNKS + 1), cb.CB_ERR_INVALID_ARG),
+    (dict(rope_theta=0.0), cb.CB_ERR_INVALID_ARG),
+])
+def test_create_rejects_bad_config_before_touching_the_gpu(lib, bad, code):
+    with pytest.raises(cb.CacheBlendError) as ei:
+        cb.cb_model_create(_cfg(**bad), _fake_weights(_cfg(**bad)["n_layers"]))
+    assert ei.value.code == code
+    assert cb.cb_last_error()
+
+
+def test_create_rejects_null_and_misaligned_weights(lib):
+    w = _fake_weights(2)
+    w["layers"][1]["wo"] = 0
+    with pytest.raises(cb.CacheBlendError) as ei:
+        cb.cb_model_create(_cfg(), w)
+    assert ei.value.code == cb.CB_ERR_INVALID_ARG
+    w = _fake_weights(2)
+    w["layers"][0]["w_up"] = 4096 + 8
+    with pytest.raises(cb.CacheBlendError) as ei:
+        cb.cb_model_create(_cfg(), w)
+    assert "aligned" in cb.cb_last_error()
+
+
+def test_calls_reject_null_model(lib):
+    with pytest.raises(cb.CacheBlendError):
+        cb.cb_blend(0, 4096, 10, 0, [], 0.1, 4096, 4096, stream=0)
+    with pytest.raises(cb.CacheBlendError):
+        cb.cb_rerope(0, 4096, 10, [(0, 0, 10)], stream=0)
+    assert lib.cb_model_destroy(None) == cb.CB_OK

@@ -25,6 +25,7 @@
  *
  * Build: gcc -O2 -fopenmp -fPIC -shared (portable C99, no ISA intrinsics).
  */
+#define _GNU_SOURCE
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
@@ -60,33 +61,33 @@ static inline void cbgen_normal_pair(uint64_t key, uint64_t p, double* z0, doubl
     const double two_pi = 6.283185307179586476925286766559;
     double u1 = 1.0 - cbgen_unif(cbgen_draw(key, 2 * p));
     double u2 = cbgen_unif(cbgen_draw(key, 2 * p + 1));
-    double r = sqrt(-2.0 * log(u1));
-    *z0 = r * cos(two_pi * u2);
-    *z1 = r * sin(two_pi * u2);
+    double r = sqrt(-2.0 * log(u1)), s, c;
+    sincos(two_pi * u2, &s, &c);
+    *z0 = r * c;
+    *z1 = r * s;
 }
 
-/* Elements [first, first + n) of stream (seed, stream), std * N(0,1), as fp32. */
-void cbgen_normal_f32(uint64_t seed, uint64_t stream, int64_t first, int64_t n, double std, float* out) {
-    const uint64_t key = cbgen_key(seed, stream);
-    #pragma omp parallel for schedule(static)
-    for (int64_t e = 0; e < n; ++e) {
-        uint64_t i = (uint64_t)(first + e);
-        double z0, z1;
-        cbgen_normal_pair(key, i >> 1, &z0, &z1);
-        out[e] = (float)(std * ((i & 1) ? z1 : z0));
+/* Elements [first, first + n) of stream (seed, stream), std * N(0,1): one Box-Muller pair per step. */
+#define CBGEN_NORMAL_LOOP(STORE)                                                      \
+    const uint64_t key = cbgen_key(seed, stream);                                     \
+    const int64_t p0 = first >> 1, p1 = (first + n + 1) >> 1;                         \
+    _Pragma("omp parallel for schedule(static)")                                      \
+    for (int64_t p = p0; p < p1; ++p) {                                               \
+        double z[2];                                                                  \
+        cbgen_normal_pair(key, (uint64_t)p, &z[0], &z[1]);                            \
+        for (int h = 0; h < 2; ++h) {                                                 \
+            int64_t e = 2 * p + h - first;                                            \
+            if (e >= 0 && e < n) STORE;                                               \
+        }                                                                             \
     }
+
+void cbgen_normal_f32(uint64_t seed, uint64_t stream, int64_t first, int64_t n, double std, float* out) {
+    CBGEN_NORMAL_LOOP(out[e] = (float)(std * z[h]))
 }
 
 /* Same values, rounded once more to bfloat16 (bit patterns). */
 void cbgen_normal_bf16(uint64_t seed, uint64_t stream, int64_t first, int64_t n, double std, uint16_t* out) {
-    const uint64_t key = cbgen_key(seed, stream);
-    #pragma omp parallel for schedule(static)
-    for (int64_t e = 0; e < n; ++e) {
-        uint64_t i = (uint64_t)(first + e);
-        double z0, z1;
-        cbgen_normal_pair(key, i >> 1, &z0, &z1);
-        out[e] = cbgen_f32_to_bf16_rne((float)(std * ((i & 1) ? z1 : z0)));
-    }
+    CBGEN_NORMAL_LOOP(out[e] = cbgen_f32_to_bf16_rne((float)(std * z[h])))
 }
 
 /* Constant fill (norm gains), bf16 bit patterns. */
