@@ -1,0 +1,411 @@
+#!/usr/bin/env python
+"""Benchmark of the CacheBlend blend step on one GB300.
+
+One step = one cb_blend call: re-RoPE placement of the chunk caches, layer 0 over every row, the
+check layer (deviation + top-k), selective recompute of the chosen rows in every later layer and
+the last-token logits.  Workload (default): the Llama-3-8B shape (32 layers, d 4096, 32/8 heads,
+head_dim 128, SwiGLU 14336, vocab 128256), random-init N(0, 0.02) weights, 6 chunks of 512 uniform
+random tokens, each prefilled alone on the GPU, placed back to back, plus a 64-token query, r = 0.15.
+
+Metric: blended context tokens per second (n_ctx / blend time); blend latency is reported beside
+it.  Inputs are resident in HBM when the timed region starts; the weights (16 GB) and chunk caches
+(384 MiB) exceed L2, and an L2-sized buffer is rewritten between steps (outside the timed events).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workload  # noqa: E402
+
+METRIC = "blended context tokens/sec & blend latency ms at r=0.15 (1×GB300), % of roofline"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle sample (cpu_baseline leg and the reference arm)
+# ------------------------------------------------------------------------------------------------
+def blend_flops(shape: workload.ModelShape, n_layers: int, n_ctx: int, n_query: int, k: int) -> float:
+    """Algorithmic FLOPs of a blend with `n_layers` layers (projections, attention, logits)."""
+    d, hd, Hq, Hkv, F = shape.d_model, shape.head_dim, shape.n_heads, shape.n_kv_heads, shape.ffn_hidden
+    N, M = n_ctx + n_query, k + n_query
+    per_row = 2 * d * (Hq * hd + 2 * Hkv * hd + Hq * hd + 3 * F)
+    keys0 = N * (N + 1) / 2
+    keysA = n_query * (n_ctx + 1) + n_query * (n_query - 1) / 2 + k * (n_ctx + 1) / 2
+    attn = lambda keys: 4 * hd * Hq * keys
+    f = N * per_row + attn(keys0)                                  # layer 0 (context K/V projections skipped
+    f -= n_ctx * 2 * d * 2 * Hkv * hd                              # for reused rows)
+    f += N * 2 * d * 2 * Hkv * hd + M * (per_row - 2 * d * 2 * Hkv * hd) + attn(keysA)   # check layer
+    f += (n_layers - 2) * (M * per_row + attn(keysA))
+    return f + 2 * d * shape.vocab
+
+
+_SAMPLE = {}
+
+
+def oracle_sample(spec: workload.WorkloadSpec, seed: int, ratio: float, sample_layers: int = 3):
+    """Time the CPU oracle on the workload truncated to its first `sample_layers` layers (same
+    request, same rows); return (seconds, full/sample FLOP ratio, description).  Inputs are made
+    once and kept; only the oracle's blend is timed."""
+    import oracle
+    shape = spec.shape
+    trunc = workload.ModelShape(**dict(shape.as_dict(), n_layers=sample_layers))
+    key = (spec.name, seed, ratio, sample_layers)
+    if key not in _SAMPLE:
+        _SAMPLE.clear()
+        _SAMPLE[key] = (workload.make_weights(trunc, seed), workload.make_request(spec, seed, ratio),
+                        workload.synthetic_cache(trunc, seed, spec.n_ctx, workload.kv_std(shape)))
+    w, req, caches = _SAMPLE[key]
+    k = oracle.selected_count(spec.n_ctx, ratio)
+    t0 = time.perf_counter()
+    oracle.blend(trunc.as_dict(), w, req.tokens, caches, req.chunks, ratio, shape.dtype)
+    dt = time.perf_counter() - t0
+    scale = blend_flops(shape, shape.n_layers, spec.n_ctx, spec.n_query, k) / \
+        blend_flops(shape, sample_layers, spec.n_ctx, spec.n_query, k)
+    desc = (f"fp64 numpy oracle, {spec.name} request (r={ratio}) on the first {sample_layers} of "
+            f"{shape.n_layers} layers; time scaled to the full blend by the FLOP ratio {scale:.2f}")
+    return dt, scale, desc
+
+
+def cpu_cores():
+    n = os.cpu_count() or 1
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(v, "").isdigit():
+            n = min(n, int(os.environ[v]))
+    return n
+
+
+# ------------------------------------------------------------------------------------------------
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(ws, v):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, spec, ws, rank):
+    """The reference arm: the CPU oracle, as it stands, on host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    ratio = args.ratio if args.ratio is not None else spec.ratios[0]
+    seed = spec.seeds[0]
+    for _ in range(min(args.warmup, 1)):
+        oracle_sample(spec, seed, ratio)
+    times, scale, desc = [], 1.0, ""
+    for _ in range(args.steps):
+        dt, scale, desc = oracle_sample(spec, seed, ratio)
+        times.append(dt * scale)
+    t = float(np.sum(times))
+    value = spec.n_ctx * args.steps / t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": min(args.warmup, 1), "ms_per_step": 1e3 * t / args.steps,
+            "latency_ms": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": spec.name, "n_ctx": spec.n_ctx, "n_query": spec.n_query, "ratio": ratio,
+                       "seed": seed, "parallelism": "cpu"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": desc + "; warm-up capped at one sample (nothing to warm on a CPU)"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama8b-3k", choices=sorted(workload.WORKLOADS))
+    ap.add_argument("--ratio", type=float, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-profile", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+
+    spec = workload.WORKLOADS[args.workload]
+    ws, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, spec, ws, rank)
+        return
+
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import cacheblend_selective_kv_gb300 as cb
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    shape = spec.shape
+    seed = spec.seeds[0]
+    ratio = args.ratio if args.ratio is not None else spec.ratios[0]
+    req = workload.make_request(spec, seed, ratio)
+
+    t_setup = time.perf_counter()
+    weights = workload.make_weights(shape, seed)
+    model = cb.BlendModel(shape.as_dict(), weights, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks, device=dev)
+    del weights
+    stream = torch.cuda.current_stream(dev)
+    # chunk caches: each chunk prefilled alone at positions 0..len-1 by the library itself
+    parts = [model.prefill_chunk(torch.from_numpy(t).to(dev)).clone() for t in req.chunk_tokens]
+    cached = torch.cat(parts, dim=2).contiguous()
+    del parts
+    tokens = torch.from_numpy(req.tokens).to(dev)
+    n = spec.n_tokens
+    out_kv = model.kv_buffer(n)
+    logits = torch.empty(shape.vocab, dtype=torch.float32, device=dev)
+    k = cb.cb_selected_count(spec.n_ctx, ratio)
+    sel = torch.empty(max(k, 1), dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # > L2 (129 MB)
+    torch.cuda.synchronize()
+    setup_s = time.perf_counter() - t_setup
+
+    def step():
+        return cb.cb_blend(model.handle, tokens, n, cached, req.chunks, ratio, out_kv, logits, sel, None, stream,
+                           stats=True)
+
+    st = None
+    for _ in range(args.warmup):
+        st = step()
+    torch.cuda.synchronize()
+
+    # ---- timed region --------------------------------------------------------------------------
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        time.sleep(0.25)
+        w0 = time.perf_counter()
+        torch.cuda.nvtx.range_push("timed_steps")
+        for i in range(args.steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - w0
+    barrier(ws)
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = max_over_ranks(ws, float(np.sum(step_ms)))
+    ms_per_step = total_ms / args.steps
+    value = ws * spec.n_ctx * args.steps / (total_ms / 1e3)
+
+    # ---- per-kernel-class device time (CUDA events around each launch, a separate pass) -------
+    kernels, roofline = {}, None
+    peaks, peak_src = load_peaks()
+    if not args.no_profile:
+        cb.cb_profile_enable(model.handle, True, 8192)
+        for _ in range(args.steps):
+            flush.zero_()
+            step()
+        prof = cb.cb_profile_read(model.handle)
+        cb.cb_profile_enable(model.handle, False)
+        tensor_peak = peaks["bf16_tflops_sustained"] if shape.dtype == "bf16" else None
+        for p in prof:
+            ms = p["ms"]
+            is_mma = p["name"].startswith("gemm") or p["name"] == "attention"
+            ent = {"launches": p["launches"], "ms_total": ms, "ms_per_step": ms / args.steps,
+                   "share": None}
+            if ms > 0 and is_mma and p["flops"] > 0:
+                ent["tflops"] = p["flops"] / (ms / 1e3) / 1e12
+                if tensor_peak:
+                    ent["frac_tensor"] = ent["tflops"] / tensor_peak
+            if ms > 0 and p["bytes"] > 0:
+                ent["gbs"] = p["bytes"] / (ms / 1e3) / 1e9
+                ent["frac_hbm"] = ent["gbs"] / peaks["hbm_gbs"]
+            kernels[p["name"]] = ent
+        tot = sum(e["ms_total"] for e in kernels.values()) or 1.0
+        for e in kernels.values():
+            e["share"] = e["ms_total"] / tot
+        top = max(kernels, key=lambda n_: kernels[n_]["ms_total"])
+        e = kernels[top]
+        pinfo = next(p for p in prof if p["name"] == top)
+        traffic = load_traffic(top)
+        if (top.startswith("gemm") or top == "attention") and shape.dtype == "bf16":
+            ach = pinfo["flops"] / pinfo["launches"] / (e["ms_total"] / e["launches"] / 1e3) / 1e12
+            roofline = {"kernel": top, "bound": "tensor", "achieved": ach, "peak": tensor_peak, "unit": "TFLOP/s",
+                        "frac": ach / tensor_peak, "traffic": traffic,
+                        "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)"}
+        else:
+            ach = pinfo["bytes"] / pinfo["launches"] / (e["ms_total"] / e["launches"] / 1e3) / 1e9
+            roofline = {"kernel": top, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": ach / peaks["hbm_gbs"], "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs"}
+
+    # ---- end to end through the public API with host buffers ----------------------------------
+    e2e = None
+    if not args.no_e2e:
+        h_tokens = torch.from_numpy(req.tokens).pin_memory()
+        h_cached = cached.cpu().pin_memory()
+        h_out = torch.empty(out_kv.shape, dtype=out_kv.dtype).pin_memory()
+        h_logits = torch.empty(shape.vocab, dtype=torch.float32).pin_memory()
+        d_tokens = torch.empty_like(tokens)
+        d_cached = torch.empty_like(cached)
+
+        def e2e_step():
+            d_tokens.copy_(h_tokens, non_blocking=True)
+            d_cached.copy_(h_cached, non_blocking=True)
+            cb.cb_blend(model.handle, d_tokens, n, d_cached, req.chunks, ratio, out_kv, logits, sel, None, stream)
+            h_out.copy_(out_kv, non_blocking=True)
+            h_logits.copy_(logits, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            e2e_step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(ws, float(np.sum([a.elapsed_time(b) for a, b in ev])))
+        bi = h_tokens.numel() * 4 + h_cached.numel() * h_cached.element_size()
+        bo = h_out.numel() * h_out.element_size() + h_logits.numel() * 4
+        e2e = {"value": ws * spec.n_ctx * args.steps / (e_ms / 1e3), "unit": "tokens/s",
+               "latency_ms": e_ms / args.steps, "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo)}
+
+    # ---- CPU oracle baseline (rank 0, N = 1 only) ----------------------------------------------
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        dt, scale, desc = oracle_sample(spec, seed, ratio)
+        cpu = {"value": spec.n_ctx / (dt * scale), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": desc, "sample_seconds": dt}
+
+    clocks = clk.summary()
+    model.close()
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "latency_ms": ms_per_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": shape.dtype, "data": "synthetic (seeded random-init weights and uniform random tokens)",
+                "config": {"workload": spec.name, "n_layers": shape.n_layers, "d_model": shape.d_model,
+                           "n_ctx": spec.n_ctx, "n_query": spec.n_query, "n_chunks": spec.n_chunks,
+                           "chunk_len": spec.chunk_len, "ratio": ratio, "k": k, "recomputed_rows": k + spec.n_query,
+                           "seed": seed, "parallelism": "replicas" if ws > 1 else "single",
+                           "l2": "inputs exceed L2 (16 GB weights, 384 MiB caches) and a 256 MiB buffer is "
+                                 "rewritten between steps outside the timed events",
+                           "timing": "CUDA events around each step on the launching stream, summed over the steps",
+                           "setup_s": round(setup_s, 1), "wall_s_timed": round(wall, 4)},
+                "gpu_launches": int(st["kernel_launches"]) * args.steps if st else None,
+                "clocks": clocks, "roofline": roofline, "kernels": kernels, "e2e": e2e, "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+
+
+def load_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it still matches the
+    source it was taken from (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        ent = d.get(kernel)
+        if not ent:
+            return None
+        import hashlib
+        src = os.path.join(ROOT, ent["source"])
+        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != ent["source_sha"]:
+            return None
+        return ent["dram_bytes_per_launch_full"]
+    except Exception:
+        return None
+
+
+if __name__ == "__main__":
+    main()

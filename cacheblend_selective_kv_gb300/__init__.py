@@ -21,7 +21,8 @@ LIB_PATH = os.path.join(_HERE, "libcacheblend.so")
 CB_OK, CB_ERR_INVALID_ARG, CB_ERR_UNSUPPORTED, CB_ERR_OOM, CB_ERR_CUDA, CB_ERR_INTERNAL = 0, -1, -2, -3, -4, -5
 CB_F32, CB_BF16 = 0, 1
 CB_MAX_CHUNKS = 1024
-EXPORTED = ("cb_model_create", "cb_model_destroy", "cb_rerope", "cb_blend", "cb_selected_count", "cb_last_error")
+EXPORTED = ("cb_model_create", "cb_model_destroy", "cb_rerope", "cb_blend", "cb_selected_count", "cb_last_error",
+            "cb_profile_enable", "cb_profile_read")
 
 
 class CbConfig(ctypes.Structure):
@@ -49,6 +50,11 @@ class CbStats(ctypes.Structure):
                 ("n_recompute", ctypes.c_int32), ("kernel_launches", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("gemm_flops", ctypes.c_double), ("attn_flops", ctypes.c_double),
                 ("kv_bytes_moved", ctypes.c_double)]
+
+
+class CbKernelProfile(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 24), ("launches", ctypes.c_int32), ("ms", ctypes.c_double),
+                ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
 
 
 class CacheBlendError(RuntimeError):
@@ -84,6 +90,10 @@ def lib() -> ctypes.CDLL:
                                ctypes.POINTER(CbStats), vp]
         L.cb_selected_count.restype = i32
         L.cb_selected_count.argtypes = [i32, ctypes.c_double]
+        L.cb_profile_enable.restype = ctypes.c_int
+        L.cb_profile_enable.argtypes = [vp, i32, i32]
+        L.cb_profile_read.restype = i32
+        L.cb_profile_read.argtypes = [vp, ctypes.POINTER(CbKernelProfile), i32]
         L.cb_last_error.restype = ctypes.c_char_p
         L.cb_last_error.argtypes = []
         _lib = L
@@ -160,6 +170,20 @@ def cb_blend(handle: int, tokens, n_tokens: int, cached_kv, chunks, ratio: float
     if stats:
         return {f: getattr(st, f) for f, _ in CbStats._fields_}
     return None
+
+
+def cb_profile_enable(handle: int, enable: bool = True, max_launches: int = 65536) -> None:
+    _check(lib().cb_profile_enable(handle, 1 if enable else 0, int(max_launches)))
+
+
+def cb_profile_read(handle: int) -> list:
+    """Per kernel class: name, launches, ms, flops, bytes since the last read (synchronises)."""
+    arr = (CbKernelProfile * 32)()
+    n = lib().cb_profile_read(handle, arr, 32)
+    if n < 0:
+        raise CacheBlendError(n, cb_last_error())
+    return [dict(name=arr[i].name.decode(), launches=arr[i].launches, ms=arr[i].ms, flops=arr[i].flops,
+                 bytes=arr[i].bytes) for i in range(n)]
 
 
 # ------------------------------------------------------------------------------------------------

@@ -175,6 +175,7 @@ cb_status cb_model_destroy(cb_model* m) {
     g_err[0] = 0;
     if (!m) return CB_OK;
     cudaDeviceSynchronize();
+    for (auto e : m->prof.ev) cudaEventDestroy(e);
     tc_destroy(*m);
     free_ws(*m);
     delete m;
@@ -206,17 +207,36 @@ cb_status check_chunks(const cb_chunk* chunks, int32_t n_chunks, int max_chunks,
     return CB_OK;
 }
 
+const char* const kClassName[K_NCLASS] = {"rerope", "embed", "rmsnorm", "gemm_q", "gemm_kv", "gemm_qkv", "gemm_o",
+                                         "gemm_gateup", "gemm_down", "attention", "deviation", "topk",
+                                         "gather_scatter", "logits", "delta_table"};
+
+// Enqueues launches on one stream; counts them and, when profiling is on, brackets each with events.
 struct Sched {
     Model& m;
     cudaStream_t s;
     int launches = 0;
     double gemm_flops = 0;
     cudaError_t err = cudaSuccess;
-    void ok(cudaError_t e, int n = 1) {
-        launches += n;
+
+    template <typename F>
+    void k(int cls, double flops, double bytes, F&& launch, int n_launch = 1) {
+        Profile& p = m.prof;
+        const bool timed = p.on && (int)p.rec_class.size() < p.cap;
+        if (timed) cudaEventRecord(p.ev[2 * p.rec_class.size()], s);
+        cudaError_t e = launch();
+        if (timed) {
+            cudaEventRecord(p.ev[2 * p.rec_class.size() + 1], s);
+            p.rec_class.push_back(cls);
+        }
+        if (p.on) {
+            p.launches[cls] += n_launch;
+            p.flops[cls] += flops;
+            p.bytes[cls] += bytes;
+        }
+        launches += n_launch;
         if (e != cudaSuccess && err == cudaSuccess) err = e;
     }
-    // activation buffer id -> device pointer
     void* xbuf(int id) const {
         switch (id) {
             case XBUF_X: return m.x;
@@ -225,16 +245,18 @@ struct Sched {
             default: return m.act;
         }
     }
-    void gemm(int xb, int row0, int M, int K, const GemmW& w, int N, const EpiParams& e) {
+    void gemm(int cls, int xb, int row0, int M, int K, const GemmW& w, int N, const EpiParams& e) {
         if (M <= 0 || N <= 0) return;
-        gemm_flops += 2.0 * M * (double)N * K * (e.kind == EPI_SWIGLU ? 2 : 1);
+        const double es = act_size(m);
+        const double f = 2.0 * M * (double)N * K * (e.kind == EPI_SWIGLU ? 2 : 1);
+        const double wbytes = (double)N * K * es * (e.kind == EPI_SWIGLU ? 2 : 1);
+        gemm_flops += f;
         if (m.tc) {
-            int n = 0;
-            ok(launch_gemm_tc(m, xb, row0, M, K, w, N, e, s, &n), 0);
-            launches += n;
+            int n = 1;
+            k(cls, f, wbytes, [&] { return launch_gemm_tc(m, xb, row0, M, K, w, N, e, s, &n); });
         } else {
             const char* base = (const char*)xbuf(xb) + (size_t)row0 * K * act_size(m);
-            ok(launch_gemm_simt(m, base, M, K, w, N, e, s));
+            k(cls, f, wbytes, [&] { return launch_gemm_simt(m, base, M, K, w, N, e, s); });
         }
     }
 };
@@ -284,8 +306,12 @@ cb_status cb_rerope(cb_model* m, void* kv, int64_t n_rows, const cb_chunk* chunk
     if (n_ctx > n_rows) return fail(CB_ERR_INVALID_ARG, "chunks cover %d rows but the buffer has %lld", n_ctx, (long long)n_rows);
     if (n_chunks == 0) return CB_OK;
     cudaStream_t s = (cudaStream_t)stream;
-    CB_CUDA(launch_delta_table(*m, t, s));
-    CB_CUDA(launch_rerope(*m, kv, kv, n_rows, n_rows, n_ctx, n_chunks, false, s));
+    Sched S{*m, s};
+    const double row = (double)m->cfg.n_kv_heads * m->cfg.head_dim * act_size(*m);
+    S.k(K_DELTA, 0, 0, [&] { return launch_delta_table(*m, t, s); });
+    S.k(K_REROPE, 0, 2.0 * m->cfg.n_layers * n_ctx * row,
+        [&] { return launch_rerope(*m, kv, kv, n_rows, n_rows, n_ctx, n_chunks, false, s); });
+    if (S.err != cudaSuccess) return fail(CB_ERR_CUDA, "cb_rerope: %s", cudaGetErrorString(S.err));
     return CB_OK;
 }
 
@@ -325,87 +351,103 @@ cb_status cb_blend(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const 
     char* kvb = (char*)out_kv;
     auto layer_kv = [&](int l) { return (void*)(kvb + (size_t)l * 2 * N * nkv * es); };
     auto layer_v = [&](int l) { return (void*)(kvb + ((size_t)l * 2 + 1) * N * nkv * es); };
+    const double row = (double)nkv * es;             // bytes of one token's K (or V) in one layer
+    const double hd = c.head_dim, Hq = c.n_heads;
+    auto attn_flops = [&](double keys) { return 4.0 * hd * Hq * keys; };
+    // causal key counts of the recomputed rows (selected rows at the mean context position)
+    const double keys0 = (double)N * (N + 1) / 2.0;
+    const double keysA = (double)Q * (n_ctx + 1) + (double)Q * (Q - 1) / 2.0 + (double)k * (n_ctx + 1) / 2.0;
 
     // re-RoPE placement of the chunk caches (section "位置恢复、KV 存储与加载流水线")
     if (n_chunks > 0) {
-        S.ok(launch_delta_table(m, t, s));
-        S.ok(launch_rerope(m, cached_kv, out_kv, inplace ? N : n_ctx, N, n_ctx, n_chunks, !inplace, s));
+        S.k(K_DELTA, 0, 0, [&] { return launch_delta_table(m, t, s); });
+        S.k(K_REROPE, 0, (inplace ? 2.0 : 4.0) * L * n_ctx * row,
+            [&] { return launch_rerope(m, cached_kv, out_kv, inplace ? N : n_ctx, N, n_ctx, n_chunks, !inplace, s); });
     }
-    S.ok(launch_embed(m, tokens, N, m.h, s));
+    S.k(K_EMBED, 0, (double)N * d * (es + 4), [&] { return launch_embed(m, tokens, N, m.h, s); });
+    auto norm = [&](const float* h, const void* g, void* out, int n) {
+        S.k(K_RMSNORM, 0, (double)n * d * (4 + es), [&] { return launch_rmsnorm(m, h, g, out, n, s); });
+    };
 
     // ---- layer 0: every row's hidden state; context K/V reused, query K/V fresh --------------
     {
-        S.ok(launch_rmsnorm(m, m.h, m.attn_norm[0], m.x, N, s));
+        norm(m.h, m.attn_norm[0], m.x, N);
         EpiParams e = epi_base(m, EPI_QKV, N);
         e.qkv_base = 0;
         e.q_out = m.q;
-        S.gemm(XBUF_X, 0, N, d, wsel(m, 0, WSEL_Q), nq, e);
+        S.gemm(K_GEMM_Q, XBUF_X, 0, N, d, wsel(m, 0, WSEL_Q), nq, e);
         EpiParams ekv = epi_base(m, EPI_QKV, Q);
         ekv.qkv_base = nq;
         ekv.pos_offset = n_ctx;
         ekv.k_dst = layer_kv(0);
         ekv.v_dst = layer_v(0);
-        S.gemm(XBUF_X, n_ctx, Q, d, wsel(m, 0, WSEL_KV), 2 * nkv, ekv);
-        S.ok(launch_attention(m, m.q, nullptr, N, layer_kv(0), N, N, m.attn, s));
+        S.gemm(K_GEMM_KV, XBUF_X, n_ctx, Q, d, wsel(m, 0, WSEL_KV), 2 * nkv, ekv);
+        S.k(K_ATTENTION, attn_flops(keys0), 2.0 * N * row,
+            [&] { return launch_attention(m, m.q, nullptr, N, layer_kv(0), N, N, m.attn, s); });
         EpiParams er = epi_base(m, EPI_RESID, N);
         er.h = m.h;
         er.ldh = d;
-        S.gemm(XBUF_ATTN, 0, N, nq, wsel(m, 0, WSEL_O), d, er);
-        S.ok(launch_rmsnorm(m, m.h, m.mlp_norm[0], m.x, N, s));
+        S.gemm(K_GEMM_O, XBUF_ATTN, 0, N, nq, wsel(m, 0, WSEL_O), d, er);
+        norm(m.h, m.mlp_norm[0], m.x, N);
         EpiParams eg = epi_base(m, EPI_SWIGLU, N);
         eg.act = m.act;
         eg.ld_act = F;
-        S.gemm(XBUF_X, 0, N, d, wsel(m, 0, WSEL_GATEUP), F, eg);
-        S.gemm(XBUF_ACT, 0, N, F, wsel(m, 0, WSEL_DOWN), d, er);
+        S.gemm(K_GEMM_GATEUP, XBUF_X, 0, N, d, wsel(m, 0, WSEL_GATEUP), F, eg);
+        S.gemm(K_GEMM_DOWN, XBUF_ACT, 0, N, F, wsel(m, 0, WSEL_DOWN), d, er);
     }
 
     // ---- check layer 1: fresh K/V of every row, deviation, top-k, then the chosen rows --------
     float* devp = out_dev ? out_dev : m.dev;
     {
-        S.ok(launch_rmsnorm(m, m.h, m.attn_norm[1], m.x, N, s));
+        norm(m.h, m.attn_norm[1], m.x, N);
         EpiParams ekv = epi_base(m, EPI_QKV, N);
         ekv.qkv_base = nq;
         ekv.kv_fresh = 1;
         ekv.k_dst = m.kf;
         ekv.v_dst = m.vf;
-        S.gemm(XBUF_X, 0, N, d, wsel(m, 1, WSEL_KV), 2 * nkv, ekv);
-        if (n_ctx > 0) S.ok(launch_deviation(m, m.kf, m.vf, layer_kv(1), N, n_ctx, devp, s));
-        S.ok(launch_topk(m, devp, n_ctx, k, Q, m.rows, out_selected, s));
-        S.ok(launch_gather_scatter(m, m.rows, M, m.h, m.hA, m.x, m.xA, m.kf, m.vf, layer_kv(1), N, s));
+        S.gemm(K_GEMM_KV, XBUF_X, 0, N, d, wsel(m, 1, WSEL_KV), 2 * nkv, ekv);
+        if (n_ctx > 0)
+            S.k(K_DEVIATION, 0, (double)n_ctx * 2 * nkv * (4 + es),
+                [&] { return launch_deviation(m, m.kf, m.vf, layer_kv(1), N, n_ctx, devp, s); });
+        S.k(K_TOPK, 0, (double)n_ctx * 4, [&] { return launch_topk(m, devp, n_ctx, k, Q, m.rows, out_selected, s); });
+        S.k(K_GATHER, 0, (double)M * (8.0 * d + 2.0 * d * es + 2.0 * nkv * (4 + es)),
+            [&] { return launch_gather_scatter(m, m.rows, M, m.h, m.hA, m.x, m.xA, m.kf, m.vf, layer_kv(1), N, s); });
         EpiParams e = epi_base(m, EPI_QKV, M);
         e.qkv_base = 0;
         e.pos = m.rows;
         e.q_out = m.q;
-        S.gemm(XBUF_XA, 0, M, d, wsel(m, 1, WSEL_Q), nq, e);
+        S.gemm(K_GEMM_Q, XBUF_XA, 0, M, d, wsel(m, 1, WSEL_Q), nq, e);
     }
 
     // ---- layers >= 1: attention of the recomputed rows over the blended K/V, O, MLP ------------
     for (int l = 1; l < L; ++l) {
         if (l >= 2) {
-            S.ok(launch_rmsnorm(m, m.hA, m.attn_norm[l], m.xA, M, s));
+            norm(m.hA, m.attn_norm[l], m.xA, M);
             EpiParams e = epi_base(m, EPI_QKV, M);
             e.qkv_base = 0;
             e.pos = m.rows;
             e.q_out = m.q;
             e.k_dst = layer_kv(l);
             e.v_dst = layer_v(l);
-            S.gemm(XBUF_XA, 0, M, d, wsel(m, l, WSEL_QKV), nq + 2 * nkv, e);
+            S.gemm(K_GEMM_QKV, XBUF_XA, 0, M, d, wsel(m, l, WSEL_QKV), nq + 2 * nkv, e);
         }
-        S.ok(launch_attention(m, m.q, m.rows, M, layer_kv(l), N, N, m.attn, s));
+        S.k(K_ATTENTION, attn_flops(keysA), 2.0 * N * row,
+            [&] { return launch_attention(m, m.q, m.rows, M, layer_kv(l), N, N, m.attn, s); });
         EpiParams er = epi_base(m, EPI_RESID, M);
         er.h = m.hA;
         er.ldh = d;
-        S.gemm(XBUF_ATTN, 0, M, nq, wsel(m, l, WSEL_O), d, er);
-        S.ok(launch_rmsnorm(m, m.hA, m.mlp_norm[l], m.xA, M, s));
+        S.gemm(K_GEMM_O, XBUF_ATTN, 0, M, nq, wsel(m, l, WSEL_O), d, er);
+        norm(m.hA, m.mlp_norm[l], m.xA, M);
         EpiParams eg = epi_base(m, EPI_SWIGLU, M);
         eg.act = m.act;
         eg.ld_act = F;
-        S.gemm(XBUF_XA, 0, M, d, wsel(m, l, WSEL_GATEUP), F, eg);
-        S.gemm(XBUF_ACT, 0, M, F, wsel(m, l, WSEL_DOWN), d, er);
+        S.gemm(K_GEMM_GATEUP, XBUF_XA, 0, M, d, wsel(m, l, WSEL_GATEUP), F, eg);
+        S.gemm(K_GEMM_DOWN, XBUF_ACT, 0, M, F, wsel(m, l, WSEL_DOWN), d, er);
     }
 
     // ---- logits of the last row --------------------------------------------------------------
-    S.ok(launch_logits(m, m.hA + (size_t)(M - 1) * d, out_logits, s));
+    S.k(K_LOGITS, 2.0 * d * c.vocab, (double)c.vocab * d * es,
+        [&] { return launch_logits(m, m.hA + (size_t)(M - 1) * d, out_logits, s); });
 
     if (S.err != cudaSuccess) return fail(CB_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(S.err));
     if (stats) {
@@ -416,16 +458,52 @@ cb_status cb_blend(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const 
         stats->kernel_launches = S.launches;
         stats->reserved = 0;
         stats->gemm_flops = S.gemm_flops + 2.0 * d * (double)c.vocab;
-        // causal key counts: layer 0 sees sum_{r<N}(r+1); later layers the query rows exactly and
-        // the selected rows at the mean context position (their exact positions stay on the device)
-        const double l0 = (double)N * (N + 1) / 2.0;
-        const double qk = (double)Q * (n_ctx + 1) + (double)Q * (Q - 1) / 2.0 + (double)k * (n_ctx + 1) / 2.0;
-        stats->attn_flops = 4.0 * c.head_dim * c.n_heads * (l0 + (L - 1) * qk);
-        const double row = (double)nkv * es;
+        stats->attn_flops = attn_flops(keys0) + (L - 1) * attn_flops(keysA);
         stats->kv_bytes_moved = (n_chunks ? (inplace ? 2.0 * L * n_ctx * row : 4.0 * L * n_ctx * row) : 0) +
                                 (double)n_ctx * 2 * nkv * (4 + es) + (double)(L - 1) * M * 2 * row;
     }
     return CB_OK;
+}
+
+cb_status cb_profile_enable(cb_model* m, int32_t enable, int32_t max_launches) {
+    g_err[0] = 0;
+    if (!m) return fail(CB_ERR_INVALID_ARG, "cb_profile_enable: null model");
+    Profile& p = m->prof;
+    if (enable && p.cap == 0) {
+        if (max_launches <= 0) return fail(CB_ERR_INVALID_ARG, "max_launches must be > 0");
+        p.ev.resize(2 * (size_t)max_launches);
+        for (auto& e : p.ev)
+            if (cudaEventCreate(&e) != cudaSuccess) return fail(CB_ERR_CUDA, "cudaEventCreate failed");
+        p.cap = max_launches;
+    }
+    p.on = enable != 0;
+    return CB_OK;
+}
+
+int32_t cb_profile_read(cb_model* m, cb_kernel_profile* out, int32_t max_entries) {
+    g_err[0] = 0;
+    if (!m || (!out && max_entries > 0)) return fail(CB_ERR_INVALID_ARG, "cb_profile_read: null argument");
+    Profile& p = m->prof;
+    if (cudaDeviceSynchronize() != cudaSuccess) return fail(CB_ERR_CUDA, "cb_profile_read: device error");
+    double ms[K_NCLASS] = {};
+    for (size_t i = 0; i < p.rec_class.size(); ++i) {
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, p.ev[2 * i], p.ev[2 * i + 1]) == cudaSuccess) ms[p.rec_class[i]] += t;
+    }
+    int n = 0;
+    for (int c = 0; c < K_NCLASS && n < max_entries; ++c) {
+        if (!p.launches[c]) continue;
+        memset(&out[n], 0, sizeof out[n]);
+        snprintf(out[n].name, sizeof out[n].name, "%s", kClassName[c]);
+        out[n].launches = p.launches[c];
+        out[n].ms = ms[c];
+        out[n].flops = p.flops[c];
+        out[n].bytes = p.bytes[c];
+        ++n;
+    }
+    p.rec_class.clear();
+    for (int c = 0; c < K_NCLASS; ++c) { p.launches[c] = 0; p.flops[c] = 0; p.bytes[c] = 0; }
+    return n;
 }
 
 }  // extern "C"

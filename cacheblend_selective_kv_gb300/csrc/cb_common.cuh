@@ -89,6 +89,20 @@ struct EpiParams {
 // ------------------------------------------------------------------------------------------------
 struct TcMaps;   // tensor maps of the tensor-core path (defined in gemm_tc.cu)
 
+// kernel classes for the opt-in per-class timing
+enum KClass { K_REROPE, K_EMBED, K_RMSNORM, K_GEMM_Q, K_GEMM_KV, K_GEMM_QKV, K_GEMM_O, K_GEMM_GATEUP, K_GEMM_DOWN,
+              K_ATTENTION, K_DEVIATION, K_TOPK, K_GATHER, K_LOGITS, K_DELTA, K_NCLASS };
+
+struct Profile {
+    bool on = false;
+    int cap = 0;                       // event pairs in the pool
+    std::vector<cudaEvent_t> ev;       // 2 * cap
+    std::vector<int> rec_class;        // class of each recorded pair
+    int launches[K_NCLASS] = {};
+    double flops[K_NCLASS] = {};
+    double bytes[K_NCLASS] = {};
+};
+
 struct Model {
     cb_config cfg;
     int device;
@@ -121,6 +135,7 @@ struct Model {
     unsigned* status;     // device status word (ST_* bits)
     TcMaps* tc;           // tensor-core path state (NULL if unavailable)
     size_t ws_bytes;
+    Profile prof;
 };
 
 // ------------------------------------------------------------------------------------------------

@@ -137,8 +137,9 @@ cb_status cb_rerope(cb_model* model, void* kv, int64_t n_rows, const cb_chunk* c
  *                n_chunks == 0 makes the call a plain causal prefill of `tokens`.
  *   ratio        fraction r in [0, 1]; k = ceil(r * n_ctx) context rows are recomputed.
  *   out_kv       device [n_layers][2][n_tokens][n_kv_heads][head_dim] (cfg.dtype): the blended
- *                K/V.  out_kv == cached_kv is allowed (in-place blend, rows 0..n_ctx-1).
- *                Other overlap between the two is not.
+ *                K/V.  out_kv == cached_kv is allowed (in-place blend): cached_kv is then read with
+ *                out_kv's layout, the chunk caches sitting in rows 0..n_ctx-1 of every (layer, K/V)
+ *                block.  Any other overlap between the two buffers is rejected.
  *   out_logits   device float32 [vocab]: logits of the last token.
  *   out_selected device int32 [k] or NULL: the chosen context rows, ascending.
  *   out_dev      device float32 [n_ctx] or NULL: every context row's deviation at the check layer.
@@ -148,6 +149,28 @@ cb_status cb_rerope(cb_model* model, void* kv, int64_t n_rows, const cb_chunk* c
 cb_status cb_blend(cb_model* model, const int32_t* tokens, int32_t n_tokens, const void* cached_kv,
                    const cb_chunk* chunks, int32_t n_chunks, double ratio, void* out_kv, float* out_logits,
                    int32_t* out_selected, float* out_dev, cb_stats* stats, void* stream);
+
+/* Per-kernel-class timing of later cb_blend / cb_rerope calls on this model.  While enabled, each
+ * launch is bracketed by CUDA events recorded on the call's stream (this serialises nothing that was
+ * not already serial on that stream, but adds event records between kernels).  Classes: "rerope",
+ * "embed", "rmsnorm", "gemm_q", "gemm_kv", "gemm_qkv", "gemm_o", "gemm_gateup", "gemm_down",
+ * "attention", "deviation", "topk", "gather_scatter", "logits", "delta_table". */
+typedef struct {
+    char name[24];
+    int32_t launches;        /* launches recorded since the last read */
+    double ms;               /* summed device time of those launches (CUDA events) */
+    double flops;            /* summed algorithmic FLOPs (matrix and attention classes) */
+    double bytes;            /* summed algorithmic HBM bytes (memory-bound classes; weights for GEMMs) */
+} cb_kernel_profile;
+
+/* enable != 0 starts recording (allocating an event pool of `max_launches` pairs on first use);
+ * enable == 0 stops.  Synchronous.  Errors: CB_ERR_INVALID_ARG, CB_ERR_CUDA. */
+cb_status cb_profile_enable(cb_model* model, int32_t enable, int32_t max_launches);
+
+/* Synchronises the device, writes up to max_entries classes (those with launches) to `out`, resets
+ * the accumulators and returns the number written (negative cb_status on error).  Launches beyond
+ * the event pool are counted but not timed (their ms is then a lower bound). */
+int32_t cb_profile_read(cb_model* model, cb_kernel_profile* out, int32_t max_entries);
 
 /* k = ceil(ratio * n_ctx - 1e-9) clamped to [0, n_ctx]; -1 if ratio is outside [0, 1] or NaN. */
 int32_t cb_selected_count(int32_t n_ctx, double ratio);
