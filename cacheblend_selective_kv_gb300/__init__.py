@@ -20,16 +20,19 @@ LIB_PATH = os.path.join(_HERE, "libcacheblend.so")
 
 CB_OK, CB_ERR_INVALID_ARG, CB_ERR_UNSUPPORTED, CB_ERR_OOM, CB_ERR_CUDA, CB_ERR_INTERNAL = 0, -1, -2, -3, -4, -5
 CB_F32, CB_BF16 = 0, 1
+CB_PREC_SPLIT, CB_PREC_BF16 = 0, 1
 CB_MAX_CHUNKS = 1024
 EXPORTED = ("cb_model_create", "cb_model_destroy", "cb_rerope", "cb_blend", "cb_selected_count", "cb_last_error",
-            "cb_profile_enable", "cb_profile_read")
+            "cb_profile_enable", "cb_profile_read", "cb_model_status")
+CB_STATUS_BAD_TOKEN, CB_STATUS_WAIT_TIMEOUT, CB_STATUS_BAD_ROW = 1, 2, 4
 
 
 class CbConfig(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("d_model", ctypes.c_int32), ("n_heads", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("ffn_hidden", ctypes.c_int32),
                 ("vocab", ctypes.c_int32), ("rope_theta", ctypes.c_double), ("rms_eps", ctypes.c_float),
-                ("dtype", ctypes.c_int32), ("max_tokens", ctypes.c_int32), ("max_chunks", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("max_tokens", ctypes.c_int32), ("max_chunks", ctypes.c_int32),
+                ("precision", ctypes.c_int32)]
 
 
 _PP = ctypes.POINTER(ctypes.c_void_p)
@@ -94,6 +97,8 @@ def lib() -> ctypes.CDLL:
         L.cb_profile_enable.argtypes = [vp, i32, i32]
         L.cb_profile_read.restype = i32
         L.cb_profile_read.argtypes = [vp, ctypes.POINTER(CbKernelProfile), i32]
+        L.cb_model_status.restype = ctypes.c_int
+        L.cb_model_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), i32]
         L.cb_last_error.restype = ctypes.c_char_p
         L.cb_last_error.argtypes = []
         _lib = L
@@ -135,12 +140,13 @@ def _stream(stream) -> int:
 
 def cb_model_create(config: dict, weights: dict) -> int:
     """config: shape dict (n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn_hidden, vocab, rope_theta,
-    rms_eps, dtype 'bf16'|'f32', max_tokens, max_chunks); weights: device pointers / tensors with keys
+    rms_eps, dtype 'bf16'|'f32', max_tokens, max_chunks, precision 'split'|'bf16'); weights: device pointers / tensors with keys
     embed, final_norm, lm_head and 'layers' (list of dicts of per-layer tensors)."""
     cfg = CbConfig(config["n_layers"], config["d_model"], config["n_heads"], config["n_kv_heads"],
                    config["head_dim"], config["ffn_hidden"], config["vocab"], float(config["rope_theta"]),
                    float(config.get("rms_eps", 1e-5)), CB_BF16 if config["dtype"] == "bf16" else CB_F32,
-                   int(config["max_tokens"]), int(config.get("max_chunks", 256)))
+                   int(config["max_tokens"]), int(config.get("max_chunks", 256)),
+                   CB_PREC_BF16 if config.get("precision", "split") == "bf16" else CB_PREC_SPLIT)
     L = config["n_layers"]
     tabs = {}
     for name in ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "w_down"):
@@ -172,6 +178,13 @@ def cb_blend(handle: int, tokens, n_tokens: int, cached_kv, chunks, ratio: float
     return None
 
 
+def cb_model_status(handle: int, clear: bool = False) -> int:
+    """Device status bits (CB_STATUS_*) recorded by the kernels; synchronises."""
+    v = ctypes.c_uint32()
+    _check(lib().cb_model_status(handle, ctypes.byref(v), 1 if clear else 0))
+    return v.value
+
+
 def cb_profile_enable(handle: int, enable: bool = True, max_launches: int = 65536) -> None:
     _check(lib().cb_profile_enable(handle, 1 if enable else 0, int(max_launches)))
 
@@ -200,16 +213,20 @@ def to_device(a: np.ndarray, device="cuda"):
 class BlendModel:
     """A cb_model handle plus the device weights it borrows."""
 
-    def __init__(self, shape: dict, weights: dict, max_tokens: int, max_chunks: int = 256, device="cuda"):
+    def __init__(self, shape: dict, weights: dict, max_tokens: int, max_chunks: int = 256, device="cuda",
+                 precision: str = "split"):
         import torch
         self.shape = dict(shape)
         self.device = torch.device(device)
         self.weights = {k: to_device(weights[k], device) for k in ("embed", "final_norm", "lm_head")}
         self.weights["layers"] = [{k: to_device(v, device) for k, v in lw.items()} for lw in weights["layers"]]
-        cfg = dict(shape, max_tokens=max_tokens, max_chunks=max_chunks)
+        cfg = dict(shape, max_tokens=max_tokens, max_chunks=max_chunks, precision=precision)
         self.handle = cb_model_create(cfg, self.weights)
         self.max_tokens = max_tokens
         self.kv_dtype = torch.bfloat16 if shape["dtype"] == "bf16" else torch.float32
+
+    def status(self, clear: bool = False) -> int:
+        return cb_model_status(self.handle, clear)
 
     def close(self):
         if self.handle:

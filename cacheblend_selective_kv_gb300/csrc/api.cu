@@ -39,7 +39,8 @@ size_t act_size(const Model& m) { return m.bf16 ? 2 : 4; }
 
 void free_ws(Model& m) {
     void* ptrs[] = {m.h, m.hA, m.x, m.xA, m.q, m.attn, m.act, m.kf, m.vf, m.dev, m.rows, m.iota,
-                    m.rope, m.inv_freq, m.delta_cs, m.chunk_dst, m.chunk_delta, m.xfinal, m.status};
+                    m.rope, m.inv_freq, m.delta_cs, m.chunk_dst, m.chunk_delta, m.xfinal, m.status,
+                    m.x_lo, m.xA_lo, m.attn_lo, m.act_lo, m.q_lo};
     for (void* p : ptrs)
         if (p) cudaFree(p);
 }
@@ -76,6 +77,8 @@ cb_status cb_model_create(const cb_config* cfg, const cb_weights* w, cb_model** 
     if (c.d_model % 64 || c.ffn_hidden % 64) return fail(CB_ERR_UNSUPPORTED, "d_model and ffn_hidden must be multiples of 64");
     if (c.n_heads / c.n_kv_heads > 8) return fail(CB_ERR_UNSUPPORTED, "at most 8 query heads per KV head");
     if (c.dtype != CB_F32 && c.dtype != CB_BF16) return fail(CB_ERR_INVALID_ARG, "dtype must be CB_F32 or CB_BF16");
+    if (c.precision != CB_PREC_SPLIT && c.precision != CB_PREC_BF16)
+        return fail(CB_ERR_INVALID_ARG, "precision must be CB_PREC_SPLIT or CB_PREC_BF16");
     if (c.max_chunks > CB_MAX_CHUNKS) return fail(CB_ERR_INVALID_ARG, "max_chunks exceeds CB_MAX_CHUNKS");
     if (!(c.rope_theta > 0) || !(c.rms_eps >= 0)) return fail(CB_ERR_INVALID_ARG, "rope_theta must be > 0, rms_eps >= 0");
     if (!w->embed || !w->final_norm || !w->lm_head || !w->attn_norm || !w->wq || !w->wk || !w->wv || !w->wo ||
@@ -94,6 +97,8 @@ cb_status cb_model_create(const cb_config* cfg, const cb_weights* w, cb_model** 
     if (!m) return fail(CB_ERR_OOM, "host allocation failed");
     m->cfg = c;
     m->bf16 = c.dtype == CB_BF16;
+    m->split = m->bf16 && c.precision == CB_PREC_SPLIT;
+    m->x_lo = m->xA_lo = m->attn_lo = m->act_lo = m->q_lo = nullptr;
     if (cudaGetDevice(&m->device) != cudaSuccess) { delete m; return fail(CB_ERR_CUDA, "no CUDA device"); }
     cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device);
     m->embed = w->embed;
@@ -124,9 +129,13 @@ cb_status cb_model_create(const cb_config* cfg, const cb_weights* w, cb_model** 
         {(void**)&m->iota, T * 4}, {(void**)&m->rope, T * half * sizeof(float2)},
         {(void**)&m->inv_freq, half * sizeof(double)}, {(void**)&m->delta_cs, mc * half * sizeof(float2)},
         {(void**)&m->chunk_dst, mc * 4}, {(void**)&m->chunk_delta, mc * 4}, {(void**)&m->xfinal, d * 4},
-        {(void**)&m->status, 16}};
+        {(void**)&m->status, 16},
+        {&m->x_lo, m->split ? T * d * as : 0}, {&m->xA_lo, m->split ? T * d * as : 0},
+        {&m->attn_lo, m->split ? T * nq * as : 0}, {&m->act_lo, m->split ? T * F * as : 0},
+        {&m->q_lo, m->split ? T * nq * as : 0}};
     size_t total = 0;
     for (auto& a : allocs) {
+        if (a.bytes == 0) continue;
         if (fault_injected("alloc") || cudaMalloc(a.p, a.bytes) != cudaSuccess) {
             cudaGetLastError();
             free_ws(*m);
@@ -156,9 +165,14 @@ cb_status cb_model_create(const cb_config* cfg, const cb_weights* w, cb_model** 
         delete m;
         return fail(CB_ERR_CUDA, "table upload failed");
     }
+    m->attn_tc = false;
     if (m->bf16) {
         std::string err;
         if (!tc_init(*m, err)) m->tc = nullptr;   // CUDA-core path only
+        const char* off = getenv("CB_DISABLE_TC_ATTN");
+        if (m->tc && !(off && off[0] == '1') && attn_tc_supported(*m) && attn_make_qmap(*m, m->q, m->qmap) &&
+            (!m->split || attn_make_qmap(*m, m->q_lo, m->qmap_lo)))
+            m->attn_tc = true;
     }
     if (cudaDeviceSynchronize() != cudaSuccess) {
         cudaError_t e = cudaGetLastError();
@@ -245,9 +259,18 @@ struct Sched {
             default: return m.act;
         }
     }
+    void* xbuf_lo(int id) const {
+        switch (id) {
+            case XBUF_X: return m.x_lo;
+            case XBUF_XA: return m.xA_lo;
+            case XBUF_ATTN: return m.attn_lo;
+            default: return m.act_lo;
+        }
+    }
     void gemm(int cls, int xb, int row0, int M, int K, const GemmW& w, int N, const EpiParams& e) {
         if (M <= 0 || N <= 0) return;
         const double es = act_size(m);
+        // algorithmic FLOPs of the projection (the split's second MMA is not counted as work)
         const double f = 2.0 * M * (double)N * K * (e.kind == EPI_SWIGLU ? 2 : 1);
         const double wbytes = (double)N * K * es * (e.kind == EPI_SWIGLU ? 2 : 1);
         gemm_flops += f;
@@ -256,7 +279,8 @@ struct Sched {
             k(cls, f, wbytes, [&] { return launch_gemm_tc(m, xb, row0, M, K, w, N, e, s, &n); });
         } else {
             const char* base = (const char*)xbuf(xb) + (size_t)row0 * K * act_size(m);
-            k(cls, f, wbytes, [&] { return launch_gemm_simt(m, base, M, K, w, N, e, s); });
+            const char* lo = m.split ? (const char*)xbuf_lo(xb) + (size_t)row0 * K * act_size(m) : nullptr;
+            k(cls, f, wbytes, [&] { return launch_gemm_simt(m, base, lo, M, K, w, N, e, s); });
         }
     }
 };
@@ -283,6 +307,7 @@ GemmW wsel(const Model& m, int layer, int which) {
 EpiParams epi_base(const Model& m, int kind, int M) {
     EpiParams e;
     memset(&e, 0, sizeof e);
+    e.q_out_lo = m.q_lo;
     e.kind = kind;
     e.M = M;
     e.nq = m.cfg.n_heads * m.cfg.head_dim;
@@ -365,8 +390,17 @@ cb_status cb_blend(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const 
             [&] { return launch_rerope(m, cached_kv, out_kv, inplace ? N : n_ctx, N, n_ctx, n_chunks, !inplace, s); });
     }
     S.k(K_EMBED, 0, (double)N * d * (es + 4), [&] { return launch_embed(m, tokens, N, m.h, s); });
+    alignas(64) unsigned char kvmap[128];
+    const bool attn_tc = m.attn_tc && attn_make_kvmap(m, out_kv, N, kvmap);
+    auto attend = [&](int l, const int* qpos, int rowsq, double keys) {
+        S.k(K_ATTENTION, attn_flops(keys), 2.0 * N * row, [&] {
+            return attn_tc ? launch_attention_tc(m, m.qmap, m.qmap_lo, kvmap, l, qpos, rowsq, N, m.attn, m.attn_lo, s)
+                           : launch_attention(m, m.q, m.q_lo, qpos, rowsq, layer_kv(l), N, N, m.attn, m.attn_lo, s);
+        });
+    };
     auto norm = [&](const float* h, const void* g, void* out, int n) {
-        S.k(K_RMSNORM, 0, (double)n * d * (4 + es), [&] { return launch_rmsnorm(m, h, g, out, n, s); });
+        void* lo = !m.split ? nullptr : (out == m.x ? m.x_lo : m.xA_lo);
+        S.k(K_RMSNORM, 0, (double)n * d * (4 + es), [&] { return launch_rmsnorm(m, h, g, out, lo, n, s); });
     };
 
     // ---- layer 0: every row's hidden state; context K/V reused, query K/V fresh --------------
@@ -382,8 +416,7 @@ cb_status cb_blend(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const 
         ekv.k_dst = layer_kv(0);
         ekv.v_dst = layer_v(0);
         S.gemm(K_GEMM_KV, XBUF_X, n_ctx, Q, d, wsel(m, 0, WSEL_KV), 2 * nkv, ekv);
-        S.k(K_ATTENTION, attn_flops(keys0), 2.0 * N * row,
-            [&] { return launch_attention(m, m.q, nullptr, N, layer_kv(0), N, N, m.attn, s); });
+        attend(0, m.iota, N, keys0);
         EpiParams er = epi_base(m, EPI_RESID, N);
         er.h = m.h;
         er.ldh = d;
@@ -391,6 +424,7 @@ cb_status cb_blend(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const 
         norm(m.h, m.mlp_norm[0], m.x, N);
         EpiParams eg = epi_base(m, EPI_SWIGLU, N);
         eg.act = m.act;
+        eg.act_lo = m.act_lo;
         eg.ld_act = F;
         S.gemm(K_GEMM_GATEUP, XBUF_X, 0, N, d, wsel(m, 0, WSEL_GATEUP), F, eg);
         S.gemm(K_GEMM_DOWN, XBUF_ACT, 0, N, F, wsel(m, 0, WSEL_DOWN), d, er);
@@ -411,7 +445,8 @@ cb_status cb_blend(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const 
                 [&] { return launch_deviation(m, m.kf, m.vf, layer_kv(1), N, n_ctx, devp, s); });
         S.k(K_TOPK, 0, (double)n_ctx * 4, [&] { return launch_topk(m, devp, n_ctx, k, Q, m.rows, out_selected, s); });
         S.k(K_GATHER, 0, (double)M * (8.0 * d + 2.0 * d * es + 2.0 * nkv * (4 + es)),
-            [&] { return launch_gather_scatter(m, m.rows, M, m.h, m.hA, m.x, m.xA, m.kf, m.vf, layer_kv(1), N, s); });
+            [&] { return launch_gather_scatter(m, m.rows, M, m.h, m.hA, m.x, m.xA, m.x_lo, m.xA_lo, m.kf, m.vf,
+                                               layer_kv(1), N, s); });
         EpiParams e = epi_base(m, EPI_QKV, M);
         e.qkv_base = 0;
         e.pos = m.rows;
@@ -431,8 +466,7 @@ cb_status cb_blend(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const 
             e.v_dst = layer_v(l);
             S.gemm(K_GEMM_QKV, XBUF_XA, 0, M, d, wsel(m, l, WSEL_QKV), nq + 2 * nkv, e);
         }
-        S.k(K_ATTENTION, attn_flops(keysA), 2.0 * N * row,
-            [&] { return launch_attention(m, m.q, m.rows, M, layer_kv(l), N, N, m.attn, s); });
+        attend(l, m.rows, M, keysA);
         EpiParams er = epi_base(m, EPI_RESID, M);
         er.h = m.hA;
         er.ldh = d;
@@ -440,6 +474,7 @@ cb_status cb_blend(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const 
         norm(m.hA, m.mlp_norm[l], m.xA, M);
         EpiParams eg = epi_base(m, EPI_SWIGLU, M);
         eg.act = m.act;
+        eg.act_lo = m.act_lo;
         eg.ld_act = F;
         S.gemm(K_GEMM_GATEUP, XBUF_XA, 0, M, d, wsel(m, l, WSEL_GATEUP), F, eg);
         S.gemm(K_GEMM_DOWN, XBUF_ACT, 0, M, F, wsel(m, l, WSEL_DOWN), d, er);
@@ -462,6 +497,17 @@ cb_status cb_blend(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const 
         stats->kv_bytes_moved = (n_chunks ? (inplace ? 2.0 * L * n_ctx * row : 4.0 * L * n_ctx * row) : 0) +
                                 (double)n_ctx * 2 * nkv * (4 + es) + (double)(L - 1) * M * 2 * row;
     }
+    return CB_OK;
+}
+
+cb_status cb_model_status(cb_model* m, uint32_t* bits, int32_t clear) {
+    g_err[0] = 0;
+    if (!m || !bits) return fail(CB_ERR_INVALID_ARG, "cb_model_status: null argument");
+    if (cudaDeviceSynchronize() != cudaSuccess) return fail(CB_ERR_CUDA, "cb_model_status: device error");
+    unsigned v = 0;
+    CB_CUDA(cudaMemcpy(&v, m->status, sizeof v, cudaMemcpyDeviceToHost));
+    *bits = v;
+    if (clear) CB_CUDA(cudaMemset(m->status, 0, sizeof v));
     return CB_OK;
 }
 

@@ -25,6 +25,12 @@ template <typename T> __device__ __forceinline__ T from_f(float x);
 template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
 template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
 
+// split of an fp32 value into two bf16 numbers: hi = rn(v), lo = rn(v - hi)
+__device__ __forceinline__ void split_bf16(float v, bf16& hi, bf16& lo) {
+    hi = __float2bfloat16_rn(v);
+    lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -71,6 +77,8 @@ struct EpiParams {
     int qkv_base;
     int nq, nkv, head_dim;
     void* q_out;           // [M][nq] activation type
+    void* act_lo;          // EPI_SWIGLU, split precision: low bf16 part of act (NULL otherwise)
+    void* q_out_lo;        // EPI_QKV, split precision: low bf16 part of q (NULL otherwise)
     void* k_dst;           // K rows: storage type at row pos(r) (kv_fresh == 0) or fp32 at row r
     void* v_dst;
     int kv_fresh;
@@ -121,6 +129,12 @@ struct Model {
     void* q;              // [max_tokens][nq]
     void* attn;           // [max_tokens][nq] attention output
     void* act;            // [max_tokens][ffn] SwiGLU output
+    bool split;           // split-bf16 activations (hi + lo)
+    void* x_lo;           // low parts of x, xA, attn, act (split precision only)
+    void* xA_lo;
+    void* attn_lo;
+    void* act_lo;
+    void* q_lo;           // low part of q (split precision only)
     float* kf;            // [max_tokens][nkv] fresh K at the check layer (fp32)
     float* vf;            // [max_tokens][nkv] fresh V at the check layer (fp32)
     float* dev;           // [max_tokens] deviations
@@ -134,6 +148,9 @@ struct Model {
     float* xfinal;        // [d] final-normed last row
     unsigned* status;     // device status word (ST_* bits)
     TcMaps* tc;           // tensor-core path state (NULL if unavailable)
+    bool attn_tc;         // tensor-core attention usable
+    alignas(64) unsigned char qmap[128];   // tensor map of the q workspace (attention)
+    alignas(64) unsigned char qmap_lo[128];
     size_t ws_bytes;
     Profile prof;
 };
@@ -152,18 +169,19 @@ cudaError_t launch_delta_table(const Model& m, const ChunkTable& t, cudaStream_t
 cudaError_t launch_rerope(const Model& m, const void* src, void* dst, int64_t src_rows, int64_t dst_rows,
                           int n_ctx, int n_chunks, bool copy_v, cudaStream_t s);
 cudaError_t launch_embed(const Model& m, const int* tokens, int n, float* h, cudaStream_t s);
-cudaError_t launch_rmsnorm(const Model& m, const float* h, const void* g, void* out, int n, cudaStream_t s);
+cudaError_t launch_rmsnorm(const Model& m, const float* h, const void* g, void* out, void* out_lo, int n,
+                           cudaStream_t s);
 cudaError_t launch_deviation(const Model& m, const float* kf, const float* vf, const void* kv_layer, int64_t kv_rows,
                              int n_ctx, float* dev, cudaStream_t s);
 cudaError_t launch_topk(const Model& m, const float* dev, int n_ctx, int k, int n_query, int* rows, int* out_sel,
                         cudaStream_t s);
 cudaError_t launch_gather_scatter(const Model& m, const int* rows, int M, const float* h, float* hA, const void* x,
-                                  void* xA, const float* kf, const float* vf, void* kv_layer, int64_t kv_rows,
-                                  cudaStream_t s);
-cudaError_t launch_attention(const Model& m, const void* q, const int* qpos, int M, const void* kv_layer,
-                             int64_t kv_rows, int n_keys, void* out, cudaStream_t s);
+                                  void* xA, const void* x_lo, void* xA_lo, const float* kf, const float* vf,
+                                  void* kv_layer, int64_t kv_rows, cudaStream_t s);
+cudaError_t launch_attention(const Model& m, const void* q, const void* q_lo, const int* qpos, int M,
+                             const void* kv_layer, int64_t kv_rows, int n_keys, void* out, void* out_lo, cudaStream_t s);
 cudaError_t launch_logits(const Model& m, const float* h_last, float* logits, cudaStream_t s);
-cudaError_t launch_gemm_simt(const Model& m, const void* X, int M, int K, const GemmW& w, int N,
+cudaError_t launch_gemm_simt(const Model& m, const void* X, const void* X_lo, int M, int K, const GemmW& w, int N,
                              const EpiParams& e, cudaStream_t s);
 
 // tensor-core path (gemm_tc.cu)
@@ -172,5 +190,12 @@ void tc_destroy(Model& m);
 cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, const GemmW& w, int N,
                            const EpiParams& e, cudaStream_t s, int* launches);
 enum { XBUF_X = 0, XBUF_XA = 1, XBUF_ATTN = 2, XBUF_ACT = 3 };
+
+// tensor-core attention (attn_tc.cu); maps are CUtensorMap (128 bytes, 64-byte aligned)
+bool attn_tc_supported(const Model& m);
+bool attn_make_qmap(const Model& m, const void* q, void* map_out);
+bool attn_make_kvmap(const Model& m, const void* kv, int64_t rows, void* map_out);
+cudaError_t launch_attention_tc(const Model& m, const void* qmap, const void* qmap_lo, const void* kvmap, int layer,
+                                const int* qpos, int M, int n_keys, void* out, void* out_lo, cudaStream_t s);
 
 }  // namespace cb

@@ -27,7 +27,9 @@ __device__ __forceinline__ void rope_pair(const EpiParams& e, int p, int off, fl
 template <typename T>
 __device__ __forceinline__ void qkv_store(const EpiParams& e, int reg, int r, int p, int off, float v) {
     if (reg == 0) {
-        reinterpret_cast<T*>(e.q_out)[(size_t)r * e.nq + off] = from_f<T>(v);
+        const T h = from_f<T>(v);
+        reinterpret_cast<T*>(e.q_out)[(size_t)r * e.nq + off] = h;
+        if (e.q_out_lo) reinterpret_cast<T*>(e.q_out_lo)[(size_t)r * e.nq + off] = from_f<T>(v - to_f(h));
     } else {
         void* dst = reg == 1 ? e.k_dst : e.v_dst;
         if (e.kv_fresh)

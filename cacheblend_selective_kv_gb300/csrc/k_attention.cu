@@ -13,9 +13,11 @@ namespace {
 constexpr int KB = 128;   // keys per step (= threads)
 
 template <typename T>
-__global__ void __launch_bounds__(KB) attn_simt_kernel(const T* __restrict__ q, const int* __restrict__ qpos,
+__global__ void __launch_bounds__(KB) attn_simt_kernel(const T* __restrict__ q, const T* __restrict__ q_lo,
+                                                       const int* __restrict__ qpos,
                                                        const T* __restrict__ kv, int64_t kv_rows, int n_keys,
-                                                       T* __restrict__ out, int Hq, int Hkv, int hd, float scale) {
+                                                       T* __restrict__ out, T* __restrict__ out_lo, int Hq, int Hkv,
+                                                       int hd, float scale) {
     extern __shared__ float sm[];
     const int i = blockIdx.x, g = blockIdx.y, G = Hq / Hkv, tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -29,7 +31,8 @@ __global__ void __launch_bounds__(KB) attn_simt_kernel(const T* __restrict__ q, 
     const int p = qpos ? qpos[i] : i;
     const int nk = min(p + 1, n_keys);
     const T* qrow = q + (size_t)i * Hq * hd + (size_t)g * G * hd;
-    for (int t = tid; t < G * hd; t += KB) qs[t] = to_f(qrow[t]) * scale;
+    const T* qlrow = q_lo ? q_lo + (size_t)i * Hq * hd + (size_t)g * G * hd : nullptr;
+    for (int t = tid; t < G * hd; t += KB) qs[t] = (to_f(qrow[t]) + (qlrow ? to_f(qlrow[t]) : 0.f)) * scale;
     if (tid < G) { mrun[tid] = -INFINITY; lrun[tid] = 0.f; }
     const int nslot = (G * hd + KB - 1) / KB;   // <= 8
     float acc[8];
@@ -90,13 +93,16 @@ __global__ void __launch_bounds__(KB) attn_simt_kernel(const T* __restrict__ q, 
     for (int s = 0; s < nslot; ++s) {
         const int idx = tid + s * KB;
         if (idx >= G * hd) break;
-        orow[idx] = from_f<T>(acc[s] / lrun[idx / hd]);
+        const float o = acc[s] / lrun[idx / hd];
+        const T oh = from_f<T>(o);
+        orow[idx] = oh;
+        if (out_lo) out_lo[(size_t)i * Hq * hd + (size_t)g * G * hd + idx] = from_f<T>(o - to_f(oh));
     }
 }
 }  // namespace
 
-cudaError_t launch_attention(const Model& m, const void* q, const int* qpos, int M, const void* kv_layer,
-                             int64_t kv_rows, int n_keys, void* out, cudaStream_t s) {
+cudaError_t launch_attention(const Model& m, const void* q, const void* q_lo, const int* qpos, int M,
+                             const void* kv_layer, int64_t kv_rows, int n_keys, void* out, void* out_lo, cudaStream_t s) {
     const cb_config& c = m.cfg;
     const int G = c.n_heads / c.n_kv_heads, hd = c.head_dim;
     const size_t smem = sizeof(float) * ((size_t)G * hd + (size_t)G * KB + (size_t)KB * hd + 3 * G);
@@ -104,12 +110,12 @@ cudaError_t launch_attention(const Model& m, const void* q, const int* qpos, int
     dim3 grid(M, c.n_kv_heads);
     if (m.bf16) {
         cudaFuncSetAttribute(attn_simt_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        attn_simt_kernel<bf16><<<grid, KB, smem, s>>>((const bf16*)q, qpos, (const bf16*)kv_layer, kv_rows, n_keys,
-                                                      (bf16*)out, c.n_heads, c.n_kv_heads, hd, scale);
+        attn_simt_kernel<bf16><<<grid, KB, smem, s>>>((const bf16*)q, (const bf16*)q_lo, qpos, (const bf16*)kv_layer, kv_rows, n_keys,
+                                                      (bf16*)out, (bf16*)out_lo, c.n_heads, c.n_kv_heads, hd, scale);
     } else {
         cudaFuncSetAttribute(attn_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        attn_simt_kernel<float><<<grid, KB, smem, s>>>((const float*)q, qpos, (const float*)kv_layer, kv_rows, n_keys,
-                                                       (float*)out, c.n_heads, c.n_kv_heads, hd, scale);
+        attn_simt_kernel<float><<<grid, KB, smem, s>>>((const float*)q, nullptr, qpos, (const float*)kv_layer, kv_rows, n_keys,
+                                                       (float*)out, nullptr, c.n_heads, c.n_kv_heads, hd, scale);
     }
     return cudaGetLastError();
 }

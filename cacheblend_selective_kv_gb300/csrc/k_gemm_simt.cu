@@ -20,8 +20,8 @@ __device__ __forceinline__ const T* weight_row(const GemmW& w, int c, int K) {
 }
 
 template <typename T, int EPI>
-__global__ void __launch_bounds__(256) gemm_simt_kernel(const T* __restrict__ X, int M, int K, GemmW w, int N,
-                                                        EpiParams e) {
+__global__ void __launch_bounds__(256) gemm_simt_kernel(const T* __restrict__ X, const T* __restrict__ X_lo, int M,
+                                                        int K, GemmW w, int N, EpiParams e) {
     __shared__ float Xs[BK][BM + 4];
     __shared__ float Ws[BK][BN + 4];
     __shared__ float Us[EPI == EPI_SWIGLU ? BK : 1][BN + 4];
@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const T* __restrict__ X,
     const int lr = tid >> 2, lk = (tid & 3) * 4;
     const int xr = r0 + lr;
     const T* xrow = xr < M ? X + (size_t)xr * K : nullptr;
+    const T* xlow = (xr < M && X_lo) ? X_lo + (size_t)xr * K : nullptr;
     const T* wrow = (c0 + lr < N) ? weight_row<T>(w, c0 + lr, K) : nullptr;
     const T* urow = nullptr;
     if (EPI == EPI_SWIGLU && c0 + lr < N) urow = reinterpret_cast<const T*>(w.w_up) + (size_t)(c0 + lr) * K;
@@ -43,7 +44,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const T* __restrict__ X,
     for (int k0 = 0; k0 < K; k0 += BK) {
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-            Xs[lk + t][lr] = xrow ? to_f(xrow[k0 + lk + t]) : 0.f;
+            Xs[lk + t][lr] = xrow ? to_f(xrow[k0 + lk + t]) + (xlow ? to_f(xlow[k0 + lk + t]) : 0.f) : 0.f;
             Ws[lk + t][lr] = wrow ? to_f(wrow[k0 + lk + t]) : 0.f;
             if (EPI == EPI_SWIGLU) Us[lk + t][lr] = urow ? to_f(urow[k0 + lk + t]) : 0.f;
         }
@@ -97,29 +98,34 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const T* __restrict__ X,
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 if (c + j >= N) continue;
-                reinterpret_cast<T*>(e.act)[(size_t)r * e.ld_act + c + j] = from_f<T>(silu_mul(acc[i][j], accu[i][j]));
+                const float a = silu_mul(acc[i][j], accu[i][j]);
+                const T ah = from_f<T>(a);
+                reinterpret_cast<T*>(e.act)[(size_t)r * e.ld_act + c + j] = ah;
+                if (e.act_lo) reinterpret_cast<T*>(e.act_lo)[(size_t)r * e.ld_act + c + j] = from_f<T>(a - to_f(ah));
             }
         }
     }
 }
 
 template <typename T>
-cudaError_t launch_t(const void* X, int M, int K, const GemmW& w, int N, const EpiParams& e, cudaStream_t s) {
+cudaError_t launch_t(const void* X, const void* X_lo, int M, int K, const GemmW& w, int N, const EpiParams& e,
+                     cudaStream_t s) {
     dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
     const T* x = reinterpret_cast<const T*>(X);
+    const T* xl = reinterpret_cast<const T*>(X_lo);
     switch (e.kind) {
-        case EPI_QKV: gemm_simt_kernel<T, EPI_QKV><<<grid, 256, 0, s>>>(x, M, K, w, N, e); break;
-        case EPI_RESID: gemm_simt_kernel<T, EPI_RESID><<<grid, 256, 0, s>>>(x, M, K, w, N, e); break;
-        default: gemm_simt_kernel<T, EPI_SWIGLU><<<grid, 256, 0, s>>>(x, M, K, w, N, e); break;
+        case EPI_QKV: gemm_simt_kernel<T, EPI_QKV><<<grid, 256, 0, s>>>(x, xl, M, K, w, N, e); break;
+        case EPI_RESID: gemm_simt_kernel<T, EPI_RESID><<<grid, 256, 0, s>>>(x, xl, M, K, w, N, e); break;
+        default: gemm_simt_kernel<T, EPI_SWIGLU><<<grid, 256, 0, s>>>(x, xl, M, K, w, N, e); break;
     }
     return cudaGetLastError();
 }
 }  // namespace
 
-cudaError_t launch_gemm_simt(const Model& m, const void* X, int M, int K, const GemmW& w, int N, const EpiParams& e,
-                             cudaStream_t s) {
+cudaError_t launch_gemm_simt(const Model& m, const void* X, const void* X_lo, int M, int K, const GemmW& w, int N,
+                             const EpiParams& e, cudaStream_t s) {
     if (M <= 0 || N <= 0) return cudaSuccess;
-    return m.bf16 ? launch_t<bf16>(X, M, K, w, N, e, s) : launch_t<float>(X, M, K, w, N, e, s);
+    return m.bf16 ? launch_t<bf16>(X, X_lo, M, K, w, N, e, s) : launch_t<float>(X, nullptr, M, K, w, N, e, s);
 }
 
 }  // namespace cb

@@ -164,8 +164,8 @@ cudaError_t launch_embed(const Model& m, const int* tokens, int n, float* h, cud
 // RMSNorm: out[r] = g * h[r] / sqrt(mean(h[r]^2) + eps), stored in the activation type
 // ------------------------------------------------------------------------------------------------
 template <typename T>
-__global__ void rmsnorm_kernel(const float* __restrict__ h, const T* __restrict__ g, T* __restrict__ out, int d,
-                               float eps) {
+__global__ void rmsnorm_kernel(const float* __restrict__ h, const T* __restrict__ g, T* __restrict__ out,
+                               T* __restrict__ out_lo, int d, float eps) {
     const int r = blockIdx.x;
     const float* row = h + (size_t)r * d;
     __shared__ float red[32];
@@ -193,15 +193,25 @@ __global__ void rmsnorm_kernel(const float* __restrict__ h, const T* __restrict_
 #pragma unroll
         for (int i = 0; i < 8; ++i) f[i] = f[i] * scale * gg[i];
         Vec8<T>::store(o + e, f);
+        if (out_lo) {            // remainder after rounding to T (split precision)
+            float r[8];
+            Vec8<T>::load(o + e, r);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) r[i] = f[i] - r[i];
+            Vec8<T>::store(out_lo + (size_t)blockIdx.x * d + e, r);
+        }
     }
 }
 
-cudaError_t launch_rmsnorm(const Model& m, const float* h, const void* g, void* out, int n, cudaStream_t s) {
+cudaError_t launch_rmsnorm(const Model& m, const float* h, const void* g, void* out, void* out_lo, int n,
+                           cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
     if (m.bf16)
-        rmsnorm_kernel<bf16><<<n, 256, 0, s>>>(h, (const bf16*)g, (bf16*)out, m.cfg.d_model, m.cfg.rms_eps);
+        rmsnorm_kernel<bf16><<<n, 256, 0, s>>>(h, (const bf16*)g, (bf16*)out, (bf16*)out_lo, m.cfg.d_model,
+                                               m.cfg.rms_eps);
     else
-        rmsnorm_kernel<float><<<n, 256, 0, s>>>(h, (const float*)g, (float*)out, m.cfg.d_model, m.cfg.rms_eps);
+        rmsnorm_kernel<float><<<n, 256, 0, s>>>(h, (const float*)g, (float*)out, nullptr, m.cfg.d_model,
+                                                m.cfg.rms_eps);
     return cudaGetLastError();
 }
 
@@ -253,7 +263,8 @@ cudaError_t launch_deviation(const Model& m, const float* kf, const float* vf, c
 // ------------------------------------------------------------------------------------------------
 template <typename T>
 __global__ void gather_scatter_kernel(const int* __restrict__ rows, const float* __restrict__ h, float* __restrict__ hA,
-                                      const T* __restrict__ x, T* __restrict__ xA, const float* __restrict__ kf,
+                                      const T* __restrict__ x, T* __restrict__ xA, const T* __restrict__ x_lo,
+                                      T* __restrict__ xA_lo, const float* __restrict__ kf,
                                       const float* __restrict__ vf, T* kv_layer, int64_t kv_rows, int d, int W) {
     const int i = blockIdx.x;
     const int r = rows[i];
@@ -263,6 +274,10 @@ __global__ void gather_scatter_kernel(const int* __restrict__ rows, const float*
         float f[8];
         Vec8<T>::load(x + (size_t)r * d + e, f);
         Vec8<T>::store(xA + (size_t)i * d + e, f);
+        if (x_lo) {
+            Vec8<T>::load(x_lo + (size_t)r * d + e, f);
+            Vec8<T>::store(xA_lo + (size_t)i * d + e, f);
+        }
     }
     for (int e = threadIdx.x * 8; e < W; e += blockDim.x * 8) {
         float f[8];
@@ -274,15 +289,15 @@ __global__ void gather_scatter_kernel(const int* __restrict__ rows, const float*
 }
 
 cudaError_t launch_gather_scatter(const Model& m, const int* rows, int M, const float* h, float* hA, const void* x,
-                                  void* xA, const float* kf, const float* vf, void* kv_layer, int64_t kv_rows,
-                                  cudaStream_t s) {
+                                  void* xA, const void* x_lo, void* xA_lo, const float* kf, const float* vf,
+                                  void* kv_layer, int64_t kv_rows, cudaStream_t s) {
     const int d = m.cfg.d_model, W = m.cfg.n_kv_heads * m.cfg.head_dim;
     if (m.bf16)
-        gather_scatter_kernel<bf16><<<M, 256, 0, s>>>(rows, h, hA, (const bf16*)x, (bf16*)xA, kf, vf, (bf16*)kv_layer,
-                                                      kv_rows, d, W);
+        gather_scatter_kernel<bf16><<<M, 256, 0, s>>>(rows, h, hA, (const bf16*)x, (bf16*)xA, (const bf16*)x_lo,
+                                                      (bf16*)xA_lo, kf, vf, (bf16*)kv_layer, kv_rows, d, W);
     else
-        gather_scatter_kernel<float><<<M, 256, 0, s>>>(rows, h, hA, (const float*)x, (float*)xA, kf, vf,
-                                                       (float*)kv_layer, kv_rows, d, W);
+        gather_scatter_kernel<float><<<M, 256, 0, s>>>(rows, h, hA, (const float*)x, (float*)xA, nullptr, nullptr, kf,
+                                                       vf, (float*)kv_layer, kv_rows, d, W);
     return cudaGetLastError();
 }
 

@@ -56,7 +56,17 @@ typedef struct {
     int32_t dtype;           /* cb_dtype of weights, K/V caches and tensor-core operands */
     int32_t max_tokens;      /* largest n_tokens (context + query) a blend may use; sizes the workspace */
     int32_t max_chunks;      /* largest n_chunks a call may pass (<= CB_MAX_CHUNKS) */
+    int32_t precision;       /* cb_precision: how bf16 models feed activations to the tensor cores */
 } cb_config;
+
+/* Activation precision of bf16 models (fp32 models compute in fp32 throughout).
+ *   CB_PREC_SPLIT: every activation operand of a projection is carried as two bf16 numbers
+ *                  (hi + lo, about 16 significant bits) and multiplied with both; the weights are
+ *                  exact bf16 values, so the products carry fp32-like activation precision.  Two
+ *                  MMAs per k-step.  Default.
+ *   CB_PREC_BF16:  activations rounded once to bf16 (one MMA per k-step; faster, and over a deep
+ *                  stack the K/V and logits drift by a few bf16 ulps from an exact computation). */
+typedef enum { CB_PREC_SPLIT = 0, CB_PREC_BF16 = 1 } cb_precision;
 
 #define CB_MAX_CHUNKS 1024
 
@@ -149,6 +159,16 @@ cb_status cb_rerope(cb_model* model, void* kv, int64_t n_rows, const cb_chunk* c
 cb_status cb_blend(cb_model* model, const int32_t* tokens, int32_t n_tokens, const void* cached_kv,
                    const cb_chunk* chunks, int32_t n_chunks, double ratio, void* out_kv, float* out_logits,
                    int32_t* out_selected, float* out_dev, cb_stats* stats, void* stream);
+
+/* Device status bits recorded by the kernels instead of trapping (cumulative since creation). */
+#define CB_STATUS_BAD_TOKEN    1u  /* a token id outside [0, vocab) was read; its embedding was zeroed */
+#define CB_STATUS_WAIT_TIMEOUT 2u  /* a bounded barrier wait in a tensor-core kernel gave up (~2 s); the
+                                      kernel unwound and its outputs are invalid */
+#define CB_STATUS_BAD_ROW      4u  /* a row index outside its buffer was seen and skipped */
+
+/* Synchronises the device and returns the status bits in *bits; clear != 0 resets them.
+ * Errors: CB_ERR_INVALID_ARG, CB_ERR_CUDA. */
+cb_status cb_model_status(cb_model* model, uint32_t* bits, int32_t clear);
 
 /* Per-kernel-class timing of later cb_blend / cb_rerope calls on this model.  While enabled, each
  * launch is bracketed by CUDA events recorded on the call's stream (this serialises nothing that was

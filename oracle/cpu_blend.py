@@ -260,7 +260,8 @@ def validate_chunks(chunks, n_tokens: int) -> int:
     return at
 
 
-def blend(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratio: float, store: str, selected=None) -> dict:
+def blend(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratio: float, store: str, selected=None,
+          keep_exact: bool = False) -> dict:
     """One CacheBlend blend (sections "核心思想" and "选 token", Figures 5 and 9).
 
     1. re-RoPE the cached chunk K/V to their placed positions (V copied);
@@ -273,6 +274,8 @@ def blend(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratio: float, sto
     5. layers 2..L-1: only A's rows: QKV, store, attend, O, MLP;
     6. logits of the last row.
 
+    ``keep_exact`` also returns ``out_kv_exact``: the values before their rounding to the
+    storage type (used to compare another implementation's rounded output against them).
     ``selected`` (optional) replaces the top-k choice by a given set of k rows -- used only
     to follow another implementation through a tie inside the comparison band.
 
@@ -289,6 +292,10 @@ def blend(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratio: float, sto
     out_kv = np.zeros((L, 2, N, Hkv, hd), kv_dtype)
     if n_ctx:
         out_kv[:, :, :n_ctx] = rerope(cached_kv, chunks, m.theta, store)
+    # unrounded values of everything stored (re-RoPE'd rows: the rotation before rounding)
+    exact = np.zeros((L, 2, N, Hkv, hd), np.float64) if keep_exact else None
+    if keep_exact and n_ctx:
+        exact[:, :, :n_ctx] = rerope(cached_kv, chunks, m.theta, "f64")
 
     h = m.embed_rows(tokens)
 
@@ -298,6 +305,8 @@ def blend(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratio: float, sto
     _, kq, vq = m.qkv(W, h[n_ctx:], pos[n_ctx:])
     out_kv[0, 0, n_ctx:] = round_store(kq, store)
     out_kv[0, 1, n_ctx:] = round_store(vq, store)
+    if keep_exact:
+        exact[0, 0, n_ctx:], exact[0, 1, n_ctx:] = kq, vq
     o = attention(q, out_kv[0, 0].astype(np.float64), out_kv[0, 1].astype(np.float64), pos, pos, Hkv)
     h = m.finish(W, h, o)
     del W
@@ -313,6 +322,8 @@ def blend(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratio: float, sto
     A = np.concatenate([sel, np.arange(n_ctx, N)])
     out_kv[1, 0, A] = round_store(k_new[A], store)
     out_kv[1, 1, A] = round_store(v_new[A], store)
+    if keep_exact:
+        exact[1, 0, A], exact[1, 1, A] = k_new[A], v_new[A]
     o = attention(q[A], out_kv[1, 0].astype(np.float64), out_kv[1, 1].astype(np.float64), A, pos, Hkv)
     hA = m.finish(W, h[A], o)
     del W, h, q, k_new, v_new
@@ -323,12 +334,14 @@ def blend(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratio: float, sto
         q, k_a, v_a = m.qkv(W, hA, A)
         out_kv[layer, 0, A] = round_store(k_a, store)
         out_kv[layer, 1, A] = round_store(v_a, store)
+        if keep_exact:
+            exact[layer, 0, A], exact[layer, 1, A] = k_a, v_a
         o = attention(q, out_kv[layer, 0].astype(np.float64), out_kv[layer, 1].astype(np.float64), A, pos, Hkv)
         hA = m.finish(W, hA, o)
         del W
 
     logits = m.logits(hA[-1])
-    return dict(out_kv=out_kv, logits=logits, selected=sel, dev=dev, k=kk, rows=A)
+    return dict(out_kv=out_kv, out_kv_exact=exact, logits=logits, selected=sel, dev=dev, k=kk, rows=A)
 
 
 def prefill(cfg: dict, weights: dict, tokens, store: str) -> dict:
