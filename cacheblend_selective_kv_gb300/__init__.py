@@ -23,7 +23,8 @@ CB_F32, CB_BF16 = 0, 1
 CB_PREC_SPLIT, CB_PREC_BF16 = 0, 1
 CB_MAX_CHUNKS = 1024
 EXPORTED = ("cb_model_create", "cb_model_destroy", "cb_rerope", "cb_blend", "cb_selected_count", "cb_last_error",
-            "cb_profile_enable", "cb_profile_read", "cb_model_status")
+            "cb_profile_enable", "cb_profile_read", "cb_model_status", "cb_rerope_static")
+CB_STATIC_MAX_CHUNKS = 256
 CB_STATUS_BAD_TOKEN, CB_STATUS_WAIT_TIMEOUT, CB_STATUS_BAD_ROW = 1, 2, 4
 
 
@@ -97,6 +98,8 @@ def lib() -> ctypes.CDLL:
         L.cb_profile_enable.argtypes = [vp, i32, i32]
         L.cb_profile_read.restype = i32
         L.cb_profile_read.argtypes = [vp, ctypes.POINTER(CbKernelProfile), i32]
+        L.cb_rerope_static.restype = ctypes.c_int
+        L.cb_rerope_static.argtypes = [vp, i64, i32, i32, i32, ctypes.c_double, i32, ctypes.POINTER(CbChunk), i32, vp]
         L.cb_model_status.restype = ctypes.c_int
         L.cb_model_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), i32]
         L.cb_last_error.restype = ctypes.c_char_p
@@ -165,6 +168,14 @@ def cb_model_destroy(handle: int) -> None:
 
 def cb_rerope(handle: int, kv, n_rows: int, chunks, stream=None) -> None:
     _check(lib().cb_rerope(handle, _ptr(kv), int(n_rows), _chunks(chunks), len(chunks), _stream(stream)))
+
+
+def cb_rerope_static(kv, n_rows: int, n_layers: int, n_kv_heads: int, head_dim: int, rope_theta: float, dtype: str,
+                     chunks, stream=None) -> None:
+    """In-place re-RoPE without a model handle and without any device allocation (see the header)."""
+    _check(lib().cb_rerope_static(_ptr(kv), int(n_rows), int(n_layers), int(n_kv_heads), int(head_dim),
+                                  float(rope_theta), CB_BF16 if dtype == "bf16" else CB_F32, _chunks(chunks),
+                                  len(chunks), _stream(stream)))
 
 
 def cb_blend(handle: int, tokens, n_tokens: int, cached_kv, chunks, ratio: float, out_kv, out_logits,

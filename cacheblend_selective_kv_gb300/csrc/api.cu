@@ -52,6 +52,8 @@ bool fault_injected(const char* what) {
 
 }  // namespace
 
+void cb::set_last_error(const char* msg) { snprintf(g_err, sizeof g_err, "%s", msg); }
+
 extern "C" {
 
 const char* cb_last_error(void) { return g_err; }

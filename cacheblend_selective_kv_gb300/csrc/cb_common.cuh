@@ -191,6 +191,9 @@ cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, c
                            const EpiParams& e, cudaStream_t s, int* launches);
 enum { XBUF_X = 0, XBUF_XA = 1, XBUF_ATTN = 2, XBUF_ACT = 3 };
 
+// records a message for cb_last_error() on the calling thread
+void set_last_error(const char* msg);
+
 // tensor-core attention (attn_tc.cu); maps are CUtensorMap (128 bytes, 64-byte aligned)
 bool attn_tc_supported(const Model& m);
 bool attn_make_qmap(const Model& m, const void* q, void* map_out);

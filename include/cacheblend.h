@@ -192,6 +192,27 @@ cb_status cb_profile_enable(cb_model* model, int32_t enable, int32_t max_launche
  * the event pool are counted but not timed (their ms is then a lower bound). */
 int32_t cb_profile_read(cb_model* model, cb_kernel_profile* out, int32_t max_entries);
 
+/* Re-RoPE with no device allocation.  The pages have no counterpart for this entry point: it serves
+ * deployment, not the method.
+ * Some callers cannot call cudaMalloc.  A KV-cache manager that has reserved nearly all device memory
+ * for its own block pool is one: creating a model (which allocates a workspace sized for whole blends,
+ * and needs the weights) would fail or fragment that pool, yet moving cached chunks to new positions
+ * needs neither.  This call rotates the K rows of a chunk-cache buffer in place exactly as cb_rerope
+ * does, without a model handle.  Its small per-call table (each chunk's start and the cos/sin of its
+ * position delta) lives in a file-scope device array with room for CB_STATIC_MAX_CHUNKS chunks: about
+ * 129 KiB on every device that loads the library, held until the process exits.
+ *   kv, n_rows, chunks, n_chunks, stream: as for cb_rerope.  n_layers, n_kv_heads, head_dim (64 or
+ *   128), rope_theta and dtype (cb_dtype) describe the buffer [n_layers][2][n_rows][n_kv_heads][head_dim].
+ *   More than CB_STATIC_MAX_CHUNKS chunks -> CB_ERR_INVALID_ARG, with nothing enqueued.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress, with that
+ * device current); make that first call before any stream capture.  No call allocates or frees device
+ * memory.  All calls share the one array; each call writes every entry it reads before reading it, so
+ * nothing needs clearing, but calls whose GPU work may overlap (other streams, other threads) race on
+ * it and must be serialised by the caller.  Errors are reported through cb_last_error(). */
+#define CB_STATIC_MAX_CHUNKS 256
+cb_status cb_rerope_static(void* kv, int64_t n_rows, int32_t n_layers, int32_t n_kv_heads, int32_t head_dim,
+                           double rope_theta, int32_t dtype, const cb_chunk* chunks, int32_t n_chunks, void* stream);
+
 /* k = ceil(ratio * n_ctx - 1e-9) clamped to [0, n_ctx]; -1 if ratio is outside [0, 1] or NaN. */
 int32_t cb_selected_count(int32_t n_ctx, double ratio);
 
