@@ -214,11 +214,21 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-profile", action="store_true")
+    # profiling-capture helpers: a smaller case with the same per-layer kernel shapes
+    ap.add_argument("--layers", type=int, default=None, help="truncate the model to its first N layers")
+    ap.add_argument("--vocab", type=int, default=None, help="override the vocabulary size")
+    ap.add_argument("--synthetic-cache", action="store_true",
+                    help="draw the chunk caches from the generator instead of prefilling them on the GPU")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
 
     spec = workload.WORKLOADS[args.workload]
+    if args.layers or args.vocab:
+        import dataclasses
+        shape = dataclasses.replace(spec.shape, n_layers=args.layers or spec.shape.n_layers,
+                                    vocab=args.vocab or spec.shape.vocab)
+        spec = dataclasses.replace(spec, shape=shape, name=f"{spec.name}-L{shape.n_layers}-V{shape.vocab}")
     ws, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, spec, ws, rank)
@@ -241,10 +251,15 @@ def main():
     model = cb.BlendModel(shape.as_dict(), weights, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks, device=dev)
     del weights
     stream = torch.cuda.current_stream(dev)
-    # chunk caches: each chunk prefilled alone at positions 0..len-1 by the library itself
-    parts = [model.prefill_chunk(torch.from_numpy(t).to(dev)).clone() for t in req.chunk_tokens]
-    cached = torch.cat(parts, dim=2).contiguous()
-    del parts
+    if args.synthetic_cache:
+        raw = workload.synthetic_cache(shape, seed, spec.n_ctx, workload.kv_std(shape))
+        cached = cb.to_device(raw, dev)
+        del raw
+    else:
+        # chunk caches: each chunk prefilled alone at positions 0..len-1 by the library itself
+        parts = [model.prefill_chunk(torch.from_numpy(t).to(dev)).clone() for t in req.chunk_tokens]
+        cached = torch.cat(parts, dim=2).contiguous()
+        del parts
     tokens = torch.from_numpy(req.tokens).to(dev)
     n = spec.n_tokens
     out_kv = model.kv_buffer(n)
