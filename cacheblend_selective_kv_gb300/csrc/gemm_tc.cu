@@ -16,6 +16,10 @@
 // with atomic adds.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <cstdlib>
+#include <map>
+
 #include "cb_epilogue.cuh"
 #include "cb_ptx.cuh"
 
@@ -23,19 +27,23 @@ namespace cb {
 
 struct TcMaps {
     std::vector<CUtensorMap> wq, wk, wv, wo, wg, wu, wd;   // per layer, box {64, 128}
-    CUtensorMap xb[4];                                      // activation buffers, box {64, 16}
-    CUtensorMap xb_lo[4];                                   // their low parts (split precision)
+    const void* xptr[4];                                    // activation buffers (hi) and their row widths
+    const void* xptr_lo[4];                                 // low parts (split precision) or NULL
+    int xcols[4];
+    int rows;
+    // token-tile maps, one box of {64, BN} rows per (buffer, BN), made on first use
+    mutable std::map<int, CUtensorMap> xb[4], xb_lo[4];
 };
 
 namespace {
 
 constexpr int BM = 128, BK = 64, TMEM_COLS = 512, NUM_THREADS = 192;
 constexpr int A_BYTES = BM * BK * 2;        // 16 KB per weight tile
-constexpr int B_BOX_ROWS = 16;
 constexpr int MAX_STAGES = 8;
+constexpr int EPI_SMEM = 4 * 32 * 17 * 4;   // per-epilogue-warp staging (token positions / transposes)
 
 struct TcArgs {
-    int M, K, x_row0, kb_total, splits, ttiles, BN, stages, units;
+    int M, K, x_row0, kb_total, splits, ttiles, BN, stages, units, prefetch;
     int nseg;
     int seg_tiles[3], seg_rows[3], seg_base[3];
     uint32_t idesc;
@@ -83,7 +91,12 @@ __device__ __forceinline__ void store_pair<bf16>(bf16* p, float a, float b) {
     *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
 }
 
-__device__ __forceinline__ void epi_qkv(const TcArgs& a, const Unit& w, int row, int lane, int tok0, const float* v) {
+// QKV epilogue of one tile: RoPE of q/k pairs (partner feature = lane ^ 1), q as bf16 (hi and, in split
+// precision, lo), k/v either into the blended cache at each token's position or as fp32 rows.
+// Positions come from a per-warp shared-memory copy; the (cos, sin) loads of the next 16 tokens are
+// issued before the current 16 are processed.
+__device__ __forceinline__ void qkv_tile(const TcArgs& a, const Unit& w, int row, int lane, int tok0, int ntok,
+                                         uint32_t tbase, const int* wpos) {
     const EpiParams& e = a.e;
     const int feat = w.lt * BM + row;
     const bool fv = feat < a.seg_rows[w.seg];
@@ -91,59 +104,92 @@ __device__ __forceinline__ void epi_qkv(const TcArgs& a, const Unit& w, int row,
     int off;
     const int reg = qkv_region(e, col, off);
     const bool even = (lane & 1) == 0;
-    const int nt = min(16, a.M - tok0);
-    // independent loads first: positions, then the (cos, sin) of each position
-    int p[16];
-    float2 cs[16];
     const int half = e.head_dim >> 1, pair = (off % e.head_dim) >> 1;
+    const bool rot = reg < 2;
+    const int nch = (ntok + 15) / 16;
+    float2 cs[16], csn[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) p[j] = j < nt ? epi_pos(e, tok0 + j) : 0;
+    for (int j = 0; j < 16; ++j)
+        cs[j] = (rot && j < ntok) ? e.rope[(size_t)wpos[j] * half + pair] : make_float2(1.f, 0.f);
+    for (int c = 0; c < nch; ++c) {
+        float v[16];
+        ptx::tmem_ld16(tbase + c * 16, v);
+        const int base = c * 16;
+        if (c + 1 < nch) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) cs[j] = (reg < 2 && j < nt) ? e.rope[(size_t)p[j] * half + pair] : make_float2(1.f, 0.f);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        if (j >= nt) break;                         // uniform across the warp
-        const int tok = tok0 + j;
-        const float x = v[j];
-        const float y = __shfl_xor_sync(0xffffffffu, x, 1);
-        if (even && fv) {
-            float x0 = x, x1 = y;
-            if (reg < 2) {
-                x0 = x * cs[j].x - y * cs[j].y;
-                x1 = x * cs[j].y + y * cs[j].x;
-            }
-            if (reg == 0) {
-                bf16 h0, l0, h1, l1;
-                split_bf16(x0, h0, l0);
-                split_bf16(x1, h1, l1);
-                *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<bf16*>(e.q_out) + (size_t)tok * e.nq + off) =
-                    __halves2bfloat162(h0, h1);
-                if (e.q_out_lo)
-                    *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<bf16*>(e.q_out_lo) + (size_t)tok * e.nq + off) =
-                        __halves2bfloat162(l0, l1);
-            } else {
-                void* dst = reg == 1 ? e.k_dst : e.v_dst;
-                if (e.kv_fresh)
-                    *reinterpret_cast<float2*>(reinterpret_cast<float*>(dst) + (size_t)tok * e.nkv + off) =
-                        make_float2(x0, x1);
-                else
-                    store_pair<bf16>(reinterpret_cast<bf16*>(dst) + (size_t)p[j] * e.nkv + off, x0, x1);
+            for (int j = 0; j < 16; ++j) {
+                const int t = base + 16 + j;
+                csn[j] = (rot && t < ntok) ? e.rope[(size_t)wpos[t] * half + pair] : make_float2(1.f, 0.f);
             }
         }
+        const int nt = min(16, ntok - base);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (j >= nt) break;                     // uniform across the warp
+            const int tok = tok0 + base + j;
+            const float x = v[j];
+            const float y = __shfl_xor_sync(0xffffffffu, x, 1);
+            if (even && fv) {
+                float x0 = x, x1 = y;
+                if (rot) {
+                    x0 = x * cs[j].x - y * cs[j].y;
+                    x1 = x * cs[j].y + y * cs[j].x;
+                }
+                if (reg == 0) {
+                    bf16 h0, l0, h1, l1;
+                    split_bf16(x0, h0, l0);
+                    split_bf16(x1, h1, l1);
+                    *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<bf16*>(e.q_out) + (size_t)tok * e.nq + off) =
+                        __halves2bfloat162(h0, h1);
+                    if (e.q_out_lo)
+                        *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<bf16*>(e.q_out_lo) + (size_t)tok * e.nq +
+                                                           off) = __halves2bfloat162(l0, l1);
+                } else {
+                    void* dst = reg == 1 ? e.k_dst : e.v_dst;
+                    if (e.kv_fresh)
+                        *reinterpret_cast<float2*>(reinterpret_cast<float*>(dst) + (size_t)tok * e.nkv + off) =
+                            make_float2(x0, x1);
+                    else
+                        store_pair<bf16>(reinterpret_cast<bf16*>(dst) + (size_t)wpos[base + j] * e.nkv + off, x0, x1);
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) cs[j] = csn[j];
     }
 }
 
-__device__ __forceinline__ void epi_resid(const TcArgs& a, const Unit& w, int row, int tok0, const float* v) {
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// Residual epilogue: h[token][feature] += y.  The warp's 32 features x 16 tokens are transposed
+// through shared memory so each lane adds four consecutive features of a token with one 16-byte
+// vector reduction (the K range may be split across CTAs, hence the atomic adds).
+__device__ __forceinline__ void epi_resid(const TcArgs& a, const Unit& w, int row, int lane, int tok0, const float* v,
+                                          float* wst) {
     const EpiParams& e = a.e;
-    const int feat = w.lt * BM + row;
-    if (feat >= a.seg_rows[w.seg]) return;
-    const int col = a.seg_base[w.seg] + feat;
+    const int feat0 = w.lt * BM + (row - lane);               // first feature of this warp
+    const int col0 = a.seg_base[w.seg] + feat0;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < 16; ++j) wst[lane * 17 + j] = v[j];   // [feature][token]
+    __syncwarp();
+    const int nf = a.seg_rows[w.seg] - feat0;                 // valid features in this warp (may be < 32)
+    const int fq = (lane & 7) * 4;                            // 4 features
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int j = (lane >> 3) + 4 * i;                    // token within the chunk
         const int tok = tok0 + j;
-        if (tok >= a.M) break;
-        atomicAdd(e.h + (size_t)tok * e.ldh + col, v[j]);
+        if (tok < a.M && fq < nf) {
+            float* hp = e.h + (size_t)tok * e.ldh + col0 + fq;
+            if (fq + 3 < nf)
+                red_add_v4(hp, wst[fq * 17 + j], wst[(fq + 1) * 17 + j], wst[(fq + 2) * 17 + j], wst[(fq + 3) * 17 + j]);
+            else
+                for (int t = 0; fq + t < nf; ++t) atomicAdd(hp + t, wst[(fq + t) * 17 + j]);
+        }
     }
+    __syncwarp();
 }
 
 __device__ __forceinline__ void epi_swiglu(const TcArgs& a, const Unit& w, int row, int tok0, const float* g,
@@ -183,6 +229,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    float* sepi = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);  // [4 warps][32 x 17]
+    int* spos = reinterpret_cast<int*>(sepi);                                        // [4 warps][256] (QKV)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -220,6 +268,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t issued = 0;                   // bit i: stage i has a load in flight or landed
             uint32_t issued_parity = 0;            // bit i: parity of that load's phase
             bool ok = true;
+            // L2 prefetch cursor: walks the same (unit, k-block) sequence PREFETCH_KB steps ahead
+            int pu = blockIdx.x, pkb = 0;
+            Unit pw;
+            bool pvalid = pu < a.units;
+            if (pvalid) { pw = decode_unit(a, pu); pkb = pw.kb0; }
+            auto prefetch_step = [&]() {
+                if (!pvalid) return;
+                const int kc = pkb * BK;
+                if (SWIGLU) {
+                    ptx::tma_prefetch_2d(&mw0, kc, pw.lt * BM);
+                    ptx::tma_prefetch_2d(&mw1, kc, pw.lt * BM);
+                } else {
+                    ptx::tma_prefetch_2d(pw.seg == 0 ? &mw0 : (pw.seg == 1 ? &mw1 : &mw2), kc, pw.lt * BM);
+                }
+                if (++pkb >= pw.kb1) {
+                    pu += gridDim.x;
+                    pvalid = pu < a.units;
+                    if (pvalid) { pw = decode_unit(a, pu); pkb = pw.kb0; }
+                }
+            };
+            if (a.prefetch == 0) pvalid = false;
+            for (int i = 0; i < a.prefetch; ++i) prefetch_step();
             for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
                 const Unit w = decode_unit(a, u);
                 const CUtensorMap* wm = w.seg == 0 ? &mw0 : (w.seg == 1 ? &mw1 : &mw2);
@@ -237,13 +307,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     const uint32_t sb = sa + A_STAGE;
                     const int r0 = a.x_row0 + w.t * a.BN;
-                    for (int i = 0; i < a.BN / B_BOX_ROWS; ++i) {
-                        ptx::tma_load_2d(sb + i * (B_BOX_ROWS * 128), &mx, kc, r0 + i * B_BOX_ROWS, fb);
-                        if (SPLIT)
-                            ptx::tma_load_2d(sb + b_bytes + i * (B_BOX_ROWS * 128), &mxl, kc, r0 + i * B_BOX_ROWS, fb);
-                    }
+                    ptx::tma_load_2d(sb, &mx, kc, r0, fb);                 // the whole token tile, one box
+                    if (SPLIT) ptx::tma_load_2d(sb + b_bytes, &mxl, kc, r0, fb);
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    prefetch_step();
                     if (++stage == a.stages) { stage = 0; phase ^= 1u; }
                 }
             }
@@ -304,13 +372,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int tok0 = w.t * a.BN;
             const int ntok = min(a.BN, a.M - tok0);
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256;
-            for (int c = 0; c * 16 < ntok; ++c) {
+            if (EPI == EPI_QKV) {
+                int* wpos = spos + (warp - 2) * (32 * 17);
+                for (int i = lane; i < ntok; i += 32) wpos[i] = epi_pos(a.e, tok0 + i);
+                __syncwarp();
+                qkv_tile(a, w, row, lane, tok0, ntok, tbase, wpos);
+                __syncwarp();
+            }
+            for (int c = 0; EPI != EPI_QKV && c * 16 < ntok; ++c) {
                 float v[16];
                 ptx::tmem_ld16(tbase + c * 16, v);
-                if (EPI == EPI_QKV) {
-                    epi_qkv(a, w, row, lane, tok0 + c * 16, v);
-                } else if (EPI == EPI_RESID) {
-                    epi_resid(a, w, row, tok0 + c * 16, v);
+                if (EPI == EPI_RESID) {
+                    epi_resid(a, w, row, lane, tok0 + c * 16, v, sepi + (warp - 2) * (32 * 17));
                 } else {
                     float up[16];
                     ptx::tmem_ld16(tbase + 128 + c * 16, up);
@@ -401,15 +474,11 @@ bool tc_init(Model& m, std::string& err) {
              make_map(&t->wg[l], m.w_gate[l], F, d, BM, err) && make_map(&t->wu[l], m.w_up[l], F, d, BM, err) &&
              make_map(&t->wd[l], m.w_down[l], d, F, BM, err);
     }
-    ok = ok && make_map(&t->xb[XBUF_X], m.x, T, d, B_BOX_ROWS, err) &&
-         make_map(&t->xb[XBUF_XA], m.xA, T, d, B_BOX_ROWS, err) &&
-         make_map(&t->xb[XBUF_ATTN], m.attn, T, nq, B_BOX_ROWS, err) &&
-         make_map(&t->xb[XBUF_ACT], m.act, T, F, B_BOX_ROWS, err);
-    if (m.split)
-        ok = ok && make_map(&t->xb_lo[XBUF_X], m.x_lo, T, d, B_BOX_ROWS, err) &&
-             make_map(&t->xb_lo[XBUF_XA], m.xA_lo, T, d, B_BOX_ROWS, err) &&
-             make_map(&t->xb_lo[XBUF_ATTN], m.attn_lo, T, nq, B_BOX_ROWS, err) &&
-             make_map(&t->xb_lo[XBUF_ACT], m.act_lo, T, F, B_BOX_ROWS, err);
+    t->xptr[XBUF_X] = m.x; t->xptr[XBUF_XA] = m.xA; t->xptr[XBUF_ATTN] = m.attn; t->xptr[XBUF_ACT] = m.act;
+    t->xptr_lo[XBUF_X] = m.x_lo; t->xptr_lo[XBUF_XA] = m.xA_lo; t->xptr_lo[XBUF_ATTN] = m.attn_lo;
+    t->xptr_lo[XBUF_ACT] = m.act_lo;
+    t->xcols[XBUF_X] = (int)d; t->xcols[XBUF_XA] = (int)d; t->xcols[XBUF_ATTN] = (int)nq; t->xcols[XBUF_ACT] = (int)F;
+    t->rows = (int)T;
     if (!ok) {
         delete t;
         return false;
@@ -456,7 +525,8 @@ cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, c
         mtiles += a.seg_tiles[i];
     }
     // token tiles: the fewest-padding split into tiles of at most 256 (128 for SwiGLU) rows
-    const int bn_max = swiglu ? 128 : 256;
+    int bn_max = swiglu ? 128 : 256;
+    if (const char* t = getenv("CB_TUNE_BN")) bn_max = std::min(bn_max, std::max(16, atoi(t)));
     int best_T = 0, best_BN = 0;
     for (int T0 = (M + bn_max - 1) / bn_max, T = T0; T <= T0 + 2; ++T) {
         int bn = ((M + T - 1) / T + 15) / 16 * 16;
@@ -471,7 +541,9 @@ cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, c
     a.splits = 1;
     if (e.kind == EPI_RESID) {
         double best = 1e30;
-        for (int S = 1; S <= 8; ++S) {
+        int smax = 8;
+        if (const char* t = getenv("CB_TUNE_SPLITK")) smax = std::max(1, atoi(t));
+        for (int S = 1; S <= smax; ++S) {
             if (a.kb_total / S < 4) break;
             const long long units = (long long)mtiles * a.ttiles * S;
             const long long waves = (units + m.num_sms - 1) / m.num_sms;
@@ -482,16 +554,33 @@ cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, c
     a.units = mtiles * a.ttiles * a.splits;
     const bool split = m.split;
     const int stage_bytes = (swiglu ? 2 * A_BYTES : A_BYTES) + (split ? 2 : 1) * a.BN * 128;
-    const int budget = 227 * 1024 - 1024 - 256;
+    const int budget = 227 * 1024 - 1024 - 256 - EPI_SMEM;
     a.stages = budget / stage_bytes;
     if (a.stages > MAX_STAGES) a.stages = MAX_STAGES;
+    if (const char* t = getenv("CB_TUNE_STAGES")) a.stages = std::min(a.stages, std::max(2, atoi(t)));
+    a.prefetch = 0;
+    if (const char* t = getenv("CB_TUNE_PF")) a.prefetch = std::max(0, atoi(t));
     if (a.stages < 2) return cudaErrorInvalidConfiguration;
     a.idesc = ptx::idesc_bf16(BM, a.BN);
-    const size_t smem = 1024 + (size_t)a.stages * stage_bytes + 256;
+    const size_t smem = 1024 + (size_t)a.stages * stage_bytes + 256 + EPI_SMEM;
     const int grid = a.units < m.num_sms ? a.units : m.num_sms;
     if (launches) *launches = 1;
-    const CUtensorMap& mx = t.xb[xbuf];
-    const CUtensorMap& mxl = split ? t.xb_lo[xbuf] : t.xb[xbuf];
+    auto tile_map = [&](std::map<int, CUtensorMap>& cache, const void* base, CUtensorMap** out) -> bool {
+        auto it = cache.find(a.BN);
+        if (it == cache.end()) {
+            CUtensorMap mp;
+            std::string err;
+            if (!make_map(&mp, base, (uint64_t)t.rows, (uint64_t)t.xcols[xbuf], (uint32_t)a.BN, err)) return false;
+            it = cache.emplace(a.BN, mp).first;
+        }
+        *out = &it->second;
+        return true;
+    };
+    CUtensorMap *pmx = nullptr, *pmxl = nullptr;
+    if (!tile_map(t.xb[xbuf], t.xptr[xbuf], &pmx)) return cudaErrorInvalidValue;
+    if (split && !tile_map(t.xb_lo[xbuf], t.xptr_lo[xbuf], &pmxl)) return cudaErrorInvalidValue;
+    const CUtensorMap& mx = *pmx;
+    const CUtensorMap& mxl = split ? *pmxl : *pmx;
     if (split) {
         switch (e.kind) {
             case EPI_QKV: return launch_kernel<EPI_QKV, true>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s);
