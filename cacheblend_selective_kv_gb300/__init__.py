@@ -23,7 +23,7 @@ CB_F32, CB_BF16 = 0, 1
 CB_PREC_SPLIT, CB_PREC_BF16 = 0, 1
 CB_MAX_CHUNKS = 1024
 EXPORTED = ("cb_model_create", "cb_model_destroy", "cb_rerope", "cb_blend", "cb_selected_count", "cb_last_error",
-            "cb_profile_enable", "cb_profile_read", "cb_model_status", "cb_rerope_static")
+            "cb_profile_enable", "cb_profile_read", "cb_model_status", "cb_rerope_static", "cb_model_diag")
 CB_STATIC_MAX_CHUNKS = 256
 CB_STATUS_BAD_TOKEN, CB_STATUS_WAIT_TIMEOUT, CB_STATUS_BAD_ROW = 1, 2, 4
 
@@ -100,6 +100,8 @@ def lib() -> ctypes.CDLL:
         L.cb_profile_read.argtypes = [vp, ctypes.POINTER(CbKernelProfile), i32]
         L.cb_rerope_static.restype = ctypes.c_int
         L.cb_rerope_static.argtypes = [vp, i64, i32, i32, i32, ctypes.c_double, i32, ctypes.POINTER(CbChunk), i32, vp]
+        L.cb_model_diag.restype = ctypes.c_int
+        L.cb_model_diag.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         L.cb_model_status.restype = ctypes.c_int
         L.cb_model_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), i32]
         L.cb_last_error.restype = ctypes.c_char_p
@@ -194,6 +196,13 @@ def cb_model_status(handle: int, clear: bool = False) -> int:
     v = ctypes.c_uint32()
     _check(lib().cb_model_status(handle, ctypes.byref(v), 1 if clear else 0))
     return v.value
+
+
+def cb_model_diag(handle: int) -> list:
+    """16 diagnostic words (status bits, then the first bounded wait that gave up); synchronises."""
+    w = (ctypes.c_uint32 * 16)()
+    _check(lib().cb_model_diag(handle, w))
+    return list(w)
 
 
 def cb_profile_enable(handle: int, enable: bool = True, max_launches: int = 65536) -> None:

@@ -40,7 +40,7 @@ size_t act_size(const Model& m) { return m.bf16 ? 2 : 4; }
 void free_ws(Model& m) {
     void* ptrs[] = {m.h, m.hA, m.x, m.xA, m.q, m.attn, m.act, m.kf, m.vf, m.dev, m.rows, m.iota,
                     m.rope, m.inv_freq, m.delta_cs, m.chunk_dst, m.chunk_delta, m.xfinal, m.status,
-                    m.x_lo, m.xA_lo, m.attn_lo, m.act_lo, m.q_lo};
+                    m.x_lo, m.xA_lo, m.attn_lo, m.act_lo, m.q_lo, m.part_o, m.part_ml};
     for (void* p : ptrs)
         if (p) cudaFree(p);
 }
@@ -101,8 +101,10 @@ cb_status cb_model_create(const cb_config* cfg, const cb_weights* w, cb_model** 
     m->bf16 = c.dtype == CB_BF16;
     m->split = m->bf16 && c.precision == CB_PREC_SPLIT;
     m->x_lo = m->xA_lo = m->attn_lo = m->act_lo = m->q_lo = nullptr;
+    m->part_o = m->part_ml = nullptr;
     if (cudaGetDevice(&m->device) != cudaSuccess) { delete m; return fail(CB_ERR_CUDA, "no CUDA device"); }
     cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device);
+    m->part_items = m->bf16 ? 8 * m->num_sms : 0;
     m->embed = w->embed;
     m->final_norm = w->final_norm;
     m->lm_head = w->lm_head;
@@ -131,10 +133,12 @@ cb_status cb_model_create(const cb_config* cfg, const cb_weights* w, cb_model** 
         {(void**)&m->iota, T * 4}, {(void**)&m->rope, T * half * sizeof(float2)},
         {(void**)&m->inv_freq, half * sizeof(double)}, {(void**)&m->delta_cs, mc * half * sizeof(float2)},
         {(void**)&m->chunk_dst, mc * 4}, {(void**)&m->chunk_delta, mc * 4}, {(void**)&m->xfinal, d * 4},
-        {(void**)&m->status, 16},
+        {(void**)&m->status, 64},
         {&m->x_lo, m->split ? T * d * as : 0}, {&m->xA_lo, m->split ? T * d * as : 0},
         {&m->attn_lo, m->split ? T * nq * as : 0}, {&m->act_lo, m->split ? T * F * as : 0},
-        {&m->q_lo, m->split ? T * nq * as : 0}};
+        {&m->q_lo, m->split ? T * nq * as : 0},
+        {(void**)&m->part_o, (size_t)m->part_items * 128 * c.head_dim * 4},
+        {(void**)&m->part_ml, (size_t)m->part_items * 128 * 2 * 4}};
     size_t total = 0;
     for (auto& a : allocs) {
         if (a.bytes == 0) continue;
@@ -395,10 +399,13 @@ cb_status cb_blend(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const 
     alignas(64) unsigned char kvmap[128];
     const bool attn_tc = m.attn_tc && attn_make_kvmap(m, out_kv, N, kvmap);
     auto attend = [&](int l, const int* qpos, int rowsq, double keys) {
+        int n = 1;
         S.k(K_ATTENTION, attn_flops(keys), 2.0 * N * row, [&] {
-            return attn_tc ? launch_attention_tc(m, m.qmap, m.qmap_lo, kvmap, l, qpos, rowsq, N, m.attn, m.attn_lo, s)
+            return attn_tc ? launch_attention_tc(m, m.qmap, m.qmap_lo, kvmap, l, qpos, rowsq, N, m.attn, m.attn_lo, s, &n)
                            : launch_attention(m, m.q, m.q_lo, qpos, rowsq, layer_kv(l), N, N, m.attn, m.attn_lo, s);
         });
+        S.launches += n - 1;
+        if (m.prof.on) m.prof.launches[K_ATTENTION] += n - 1;
     };
     auto norm = [&](const float* h, const void* g, void* out, int n) {
         void* lo = !m.split ? nullptr : (out == m.x ? m.x_lo : m.xA_lo);
@@ -509,7 +516,15 @@ cb_status cb_model_status(cb_model* m, uint32_t* bits, int32_t clear) {
     unsigned v = 0;
     CB_CUDA(cudaMemcpy(&v, m->status, sizeof v, cudaMemcpyDeviceToHost));
     *bits = v;
-    if (clear) CB_CUDA(cudaMemset(m->status, 0, sizeof v));
+    if (clear) CB_CUDA(cudaMemset(m->status, 0, 64));
+    return CB_OK;
+}
+
+cb_status cb_model_diag(cb_model* m, uint32_t* words) {
+    g_err[0] = 0;
+    if (!m || !words) return fail(CB_ERR_INVALID_ARG, "cb_model_diag: null argument");
+    if (cudaDeviceSynchronize() != cudaSuccess) return fail(CB_ERR_CUDA, "cb_model_diag: device error");
+    CB_CUDA(cudaMemcpy(words, m->status, 16 * sizeof(uint32_t), cudaMemcpyDeviceToHost));
     return CB_OK;
 }
 

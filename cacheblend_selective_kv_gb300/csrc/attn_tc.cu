@@ -4,15 +4,16 @@
 // Work unit = (tile of 128/G consecutive recomputed queries, KV head g): its 128 TMEM lanes hold the
 // G query heads that share KV head g for each of those queries (row r = query * G + head), so each
 // K/V block is read once for the whole GQA group.  Queries are sorted by position; a unit streams
-// key blocks 0 .. pos(last query) and masks keys past each row's own position (causal by global
+// 64-key blocks 0 .. pos(last query) and masks keys past each row's own position (causal by global
 // position).
-//   warp 0      TMA producer: the Q tile (4-D box), then 64-key K and V blocks of KV head g
-//   warp 1      MMA issuer: S = Q K^T (TMEM), then O_b = P_b V_b (TMEM)
-//   warps 2..5  softmax: one thread per row; online max/sum in fp32 (exp2), P written as bf16 into
-//               128-byte-swizzled shared memory (the A operand of the second MMA), and the per-block
-//               O_b accumulated in registers with the running rescale; final O / l stored as bf16.
-// S and O_b are double buffered in TMEM (4 x 128 columns) so the tensor cores run one block ahead
-// of the softmax.  V is consumed as an MN-major operand straight from its [key][dim] layout.
+//   warp 0      TMA producer: the Q tile (4-D box), then K and V blocks of KV head g
+//   warp 1      MMA issuer: S = Q K^T into TMEM; O_h += P_h V_h for each half h of the block's keys
+//   warps 2..9  softmax, two warps per TMEM lane quarter: the warps of half h own keys 32h..32h+31 of
+//               every block, keep their own running max and sum, write P_h (bf16) into 128-byte-swizzled
+//               shared memory and accumulate O_h in TMEM.  O_h is rescaled in TMEM only when that
+//               half's running max grows by more than 2^8 (exp2 domain), so P stays below 256.
+// At the end of a unit the half-1 warps combine both halves: O = (O_0 2^(m_0-M) + O_1 2^(m_1-M)) / l.
+// S is double buffered in TMEM; V is consumed as an MN-major operand from its [key][dim] layout.
 #include <cudaTypedefs.h>
 
 #include "cb_ptx.cuh"
@@ -22,8 +23,10 @@ namespace cb {
 namespace {
 
 constexpr int BKV = 64;                  // keys per block
+constexpr int HK = 32;                   // keys per softmax half
 constexpr int ROWS = 128;                // TMEM lanes per unit
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 320;         // producer, MMA, 8 softmax warps
+constexpr float RESCALE_LOG2 = 8.0f;     // lazy-rescale threshold (P <= 2^8)
 
 struct AttnArgs {
     int M;              // recomputed query rows
@@ -37,10 +40,21 @@ struct AttnArgs {
     const int* pos;     // [M] positions (NULL: identity)
     bf16* out;          // [M][Hq * hd]
     bf16* out_lo;       // low parts (split precision) or NULL
+    int parts;          // key-range parts per (query tile, KV head); 1 = write the normalised output
+    int part_blocks;    // key blocks per part
+    float* part_o;      // parts > 1: [unit * parts + part][128][hd] unnormalised O
+    float* part_ml;     // parts > 1: [unit * parts + part][128][2] (max in exp2 domain, sum)
     float scale_log2;   // log2(e) / sqrt(hd)
     uint32_t idesc_qk, idesc_pv;
     unsigned* status;
 };
+
+// 2^x on the special-function unit (about 2 ulp; the result feeds a bf16 hi+lo pair)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -79,14 +93,44 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, unsign
     return true;
 }
 
-__device__ __forceinline__ void unit_of(const AttnArgs& a, int u, int& qt, int& g) {
-    qt = a.n_qt - 1 - u / a.Hkv;     // latest (longest) query tiles first
-    g = u % a.Hkv;
+// A wait that, when it gives up, records where (once per launch) in the diagnostic words after the
+// status bits: {magic, barrier code, parity, counter, block, warp, unit}.
+__device__ __forceinline__ bool await(uint32_t bar, uint32_t parity, volatile int* abort, unsigned* status, int code,
+                                      uint32_t cnt, int unit) {
+    if (ptx::mbar_wait(bar, parity, abort, status)) return true;
+    if (atomicCAS(status + 1, 0u, 0xA77Eu) == 0u) {
+        status[2] = (unsigned)code;
+        status[3] = parity;
+        status[4] = cnt;
+        status[5] = blockIdx.x;
+        status[6] = threadIdx.x >> 5;
+        status[7] = (unsigned)unit;
+    }
+    return false;
+}
+
+// work item u -> query tile (latest, i.e. longest, first), KV head and key-range part
+__device__ __forceinline__ void unit_of(const AttnArgs& a, int u, int& qt, int& g, int& part) {
+    part = u % a.parts;
+    const int rest = u / a.parts;
+    qt = a.n_qt - 1 - rest / a.Hkv;
+    g = rest % a.Hkv;
 }
 __device__ __forceinline__ int tile_blocks(const AttnArgs& a, int qt) {
     const int last = min((qt + 1) * a.QT, a.M) - 1;
-    const int pmax = a.pos ? a.pos[last] : last;
+    int pmax = a.pos ? a.pos[last] : last;
+    if (pmax < 0 || pmax >= a.n_keys) {             // a position outside the cache: record, clamp
+        atomicOr(a.status, ST_BAD_ROW);
+        pmax = pmax < 0 ? 0 : a.n_keys - 1;
+    }
     return pmax / BKV + 1;
+}
+
+// key blocks [b0, b1) of an item (empty when the part starts past the tile's last position)
+__device__ __forceinline__ void item_blocks(const AttnArgs& a, int qt, int part, int& b0, int& b1) {
+    const int nb = tile_blocks(a, qt);
+    b0 = part * a.part_blocks;
+    b1 = min(b0 + a.part_blocks, nb);
 }
 
 template <int HD, bool SPLIT>
@@ -100,24 +144,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr int Q_BYTES = ROWS * HD * 2;            // one Q tile (hi or lo)
     constexpr int KB_BYTES = BKV * HD * 2;            // one K (or V) block
     constexpr int P_BYTES = ROWS * BKV * 2;           // one P tile (hi or lo)
+    constexpr uint32_t S_COL = 0, O_COL = 128;        // TMEM: S buffers at 0 / 64, O_h at 128 + 128 h
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;                               // [NP] Q tiles
     uint8_t* sK = sQ + NP * Q_BYTES;                  // [KV_STAGES] K blocks
     uint8_t* sV = sK + KV_STAGES * KB_BYTES;          // [KV_STAGES] V blocks
     uint8_t* sP = sV + KV_STAGES * KB_BYTES;          // [2 buffers][NP] P tiles
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * NP * P_BYTES);
+    float* cmb = reinterpret_cast<float*>(sP + 2 * NP * P_BYTES);   // [128][2] half-0 (max, sum)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(cmb + 2 * ROWS);
     uint64_t* q_full = bars;
     uint64_t* q_empty = bars + 1;
     uint64_t* kv_full = bars + 2;
     uint64_t* kv_empty = kv_full + KV_STAGES;
     uint64_t* s_full = kv_empty + KV_STAGES;
     uint64_t* s_empty = s_full + 2;
-    uint64_t* p_full = s_empty + 2;
-    uint64_t* p_empty = p_full + 2;
-    uint64_t* o_full = p_empty + 2;
-    uint64_t* o_empty = o_full + 2;
-    uint64_t* drain = o_empty + 2;
+    uint64_t* p_full = s_empty + 2;                   // [buffer][half]
+    uint64_t* o_full = p_full + 4;                    // [half][block parity]
+    uint64_t* o_free = o_full + 4;
+    uint64_t* cmb_bar = o_free + 1;
+    uint64_t* drain = cmb_bar + 1;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -131,12 +177,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(ptx::smem_u32(s_full + i), 1);
-            ptx::mbar_init(ptx::smem_u32(s_empty + i), 4);
-            ptx::mbar_init(ptx::smem_u32(p_full + i), 4);
-            ptx::mbar_init(ptx::smem_u32(p_empty + i), 1);
-            ptx::mbar_init(ptx::smem_u32(o_full + i), 1);
-            ptx::mbar_init(ptx::smem_u32(o_empty + i), 4);
+            ptx::mbar_init(ptx::smem_u32(s_empty + i), 8);
         }
+        for (int i = 0; i < 4; ++i) ptx::mbar_init(ptx::smem_u32(o_full + i), 1);
+        for (int i = 0; i < 4; ++i) ptx::mbar_init(ptx::smem_u32(p_full + i), 4);
+        ptx::mbar_init(ptx::smem_u32(o_free), 4);
+        ptx::mbar_init(ptx::smem_u32(cmb_bar), 4);
         ptx::mbar_init(ptx::smem_u32(drain), 1);
         *abort = 0;
         ptx::fence_barrier_init();
@@ -151,7 +197,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    const uint32_t tmem = *tmem_holder;       // S buffers at columns 0, 128; O buffers at 256, 384
+    const uint32_t tmem = *tmem_holder;
 
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
@@ -162,10 +208,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t q_par = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-                int qt, g;
-                unit_of(a, u, qt, g);
-                const int nb = tile_blocks(a, qt);
-                if (!ptx::mbar_wait(ptx::smem_u32(q_empty), (q_cnt & 1u) ^ 1u, abort, a.status)) break;
+                int qt, g, part, b0, b1;
+                unit_of(a, u, qt, g, part);
+                item_blocks(a, qt, part, b0, b1);
+                if (b0 >= b1) continue;
+                if (!await(ptx::smem_u32(q_empty), (q_cnt & 1u) ^ 1u, abort, a.status, 1, q_cnt, u)) break;
                 const uint32_t qb = ptx::smem_u32(q_full);
                 ptx::mbar_arrive_expect_tx(qb, NP * Q_BYTES);
                 for (int h = 0; h < HALVES; ++h) {
@@ -176,10 +223,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 q_issued = true;
                 q_par = q_cnt & 1u;
                 ++q_cnt;
-                for (int b = 0; b < nb; ++b) {
+                for (int b = b0; b < b1; ++b) {
                     const int st = kv_cnt % KV_STAGES;
                     const uint32_t par = (kv_cnt / KV_STAGES) & 1u;
-                    if (!ptx::mbar_wait(ptx::smem_u32(kv_empty + st), par ^ 1u, abort, a.status)) { ok = false; break; }
+                    if (!await(ptx::smem_u32(kv_empty + st), par ^ 1u, abort, a.status, 2, kv_cnt, u)) { ok = false; break; }
                     const uint32_t fb = ptx::smem_u32(kv_full + st);
                     ptx::mbar_arrive_expect_tx(fb, 2 * KB_BYTES);
                     for (int h = 0; h < HALVES; ++h) {
@@ -200,190 +247,255 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            uint32_t q_cnt = 0, kv_cnt = 0, s_cnt = 0, o_cnt = 0;
+            uint32_t q_cnt = 0, kv_cnt = 0, s_cnt = 0, unit_cnt = 0;
             bool ok = true;
-            auto pv = [&](uint32_t blk_cnt, uint32_t st) -> bool {
-                // O_b = P_b V_b for the block whose S was buffer (blk_cnt & 1)
-                const int buf = blk_cnt & 1;
-                const uint32_t par = (blk_cnt >> 1) & 1u;
-                if (!ptx::mbar_wait(ptx::smem_u32(p_full + buf), par, abort, a.status)) return false;
-                if (!ptx::mbar_wait(ptx::smem_u32(o_empty + buf), par ^ 1u, abort, a.status)) return false;
-                ptx::tc_fence_after();
+            // O_h += P_h V_h for the block whose S had counter `sc`, whose K/V sit in stage `st`
+            auto pv = [&](uint32_t sc, uint32_t st, bool first) -> bool {
+                const int buf = sc & 1;
+                const uint32_t par = (sc >> 1) & 1u;
+                if (first && !await(ptx::smem_u32(o_free), (unit_cnt & 1u) ^ 1u, abort, a.status, 3, unit_cnt, -1)) return false;
                 const uint32_t pa = ptx::smem_u32(sP + buf * NP * P_BYTES);
                 const uint32_t va = ptx::smem_u32(sV + st * KB_BYTES);
+                for (int h = 0; h < 2; ++h) {
+                    if (!await(ptx::smem_u32(p_full + buf * 2 + h), par, abort, a.status, 10 + h, sc, -1)) return false;
+                    ptx::tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < BKV / 16; ++kk) {
-                    const uint64_t vd = sdesc_mn_sw128(va + kk * 16 * 128, BKV * 128);
-                    ptx::mma_bf16(tmem + 256 + buf * 128, ptx::sdesc_sw128(pa + kk * 32), vd, a.idesc_pv,
-                                  kk > 0 ? 1u : 0u);
-                    if (SPLIT)
-                        ptx::mma_bf16(tmem + 256 + buf * 128, ptx::sdesc_sw128(pa + P_BYTES + kk * 32), vd, a.idesc_pv,
-                                      1u);
+                    for (int kk = 0; kk < HK / 16; ++kk) {
+                        const int key = h * HK + kk * 16;
+                        const uint64_t vd = sdesc_mn_sw128(va + key * 128, BKV * 128);
+                        const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
+                        ptx::mma_bf16(tmem + O_COL + h * 128, ptx::sdesc_sw128(pa + key * 2), vd, a.idesc_pv, acc0);
+                        if (SPLIT)
+                            ptx::mma_bf16(tmem + O_COL + h * 128, ptx::sdesc_sw128(pa + P_BYTES + key * 2), vd,
+                                          a.idesc_pv, 1u);
+                    }
+                    ptx::mma_commit(ptx::smem_u32(o_full + h * 2 + buf));
                 }
-                ptx::mma_commit(ptx::smem_u32(p_empty + buf));
-                ptx::mma_commit(ptx::smem_u32(o_full + buf));
                 ptx::mma_commit(ptx::smem_u32(kv_empty + st));
-                ++o_cnt;
                 return true;
             };
             for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-                int qt, g;
-                unit_of(a, u, qt, g);
-                const int nb = tile_blocks(a, qt);
-                if (!ptx::mbar_wait(ptx::smem_u32(q_full), q_cnt & 1u, abort, a.status)) break;
+                int qt, g, part, b0, b1;
+                unit_of(a, u, qt, g, part);
+                item_blocks(a, qt, part, b0, b1);
+                if (b0 >= b1) continue;
+                const int nb = b1 - b0;
+                if (!await(ptx::smem_u32(q_full), q_cnt & 1u, abort, a.status, 4, q_cnt, u)) break;
                 ++q_cnt;
-                uint32_t prev_st = 0;
+                uint32_t prev_st = 0, prev_sc = 0;
                 for (int b = 0; b < nb; ++b) {
                     const uint32_t st = kv_cnt % KV_STAGES;
                     const uint32_t kpar = (kv_cnt / KV_STAGES) & 1u;
                     ++kv_cnt;
                     const int buf = s_cnt & 1;
                     const uint32_t spar = (s_cnt >> 1) & 1u;
-                    if (!ptx::mbar_wait(ptx::smem_u32(kv_full + st), kpar, abort, a.status) ||
-                        !ptx::mbar_wait(ptx::smem_u32(s_empty + buf), spar ^ 1u, abort, a.status)) { ok = false; break; }
+                    if (!await(ptx::smem_u32(kv_full + st), kpar, abort, a.status, 5, kv_cnt, u) ||
+                        !await(ptx::smem_u32(s_empty + buf), spar ^ 1u, abort, a.status, 6, s_cnt, u)) { ok = false; break; }
                     ptx::tc_fence_after();
                     const uint32_t qa = ptx::smem_u32(sQ), ka = ptx::smem_u32(sK + st * KB_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < HD / 16; ++kk) {
                         const uint32_t off = (kk & 3) * 32;
                         const uint64_t kd = ptx::sdesc_sw128(ka + (kk >> 2) * (BKV * 128) + off);
-                        ptx::mma_bf16(tmem + buf * 128, ptx::sdesc_sw128(qa + (kk >> 2) * (ROWS * 128) + off), kd,
-                                      a.idesc_qk, kk > 0 ? 1u : 0u);
+                        ptx::mma_bf16(tmem + S_COL + buf * 64, ptx::sdesc_sw128(qa + (kk >> 2) * (ROWS * 128) + off),
+                                      kd, a.idesc_qk, kk > 0 ? 1u : 0u);
                         if (SPLIT)
-                            ptx::mma_bf16(tmem + buf * 128,
+                            ptx::mma_bf16(tmem + S_COL + buf * 64,
                                           ptx::sdesc_sw128(qa + Q_BYTES + (kk >> 2) * (ROWS * 128) + off), kd,
                                           a.idesc_qk, 1u);
                     }
                     ptx::mma_commit(ptx::smem_u32(s_full + buf));
-                    ++s_cnt;
-                    if (b > 0 && !pv(s_cnt - 2, prev_st)) { ok = false; break; }
+                    if (b > 0 && !pv(prev_sc, prev_st, b == 1)) { ok = false; break; }
                     prev_st = st;
+                    prev_sc = s_cnt;
+                    ++s_cnt;
                 }
                 if (!ok) break;
-                if (!pv(s_cnt - 1, prev_st)) break;
+                if (!pv(prev_sc, prev_st, nb == 1)) break;
                 ptx::mma_commit(ptx::smem_u32(q_empty));
+                ++unit_cnt;
             }
             ptx::mma_commit(ptx::smem_u32(drain));
             drain_wait(ptx::smem_u32(drain), 0, a.status);
-            (void)o_cnt;
         }
     } else {
-        // ---------------------------------------------------------------- softmax (4 warps)
-        const int q4 = warp & 3;
+        // ---------------------------------------------------------------- softmax (8 warps)
+        const int q4 = warp & 3;                      // TMEM lane quarter
+        const int hf = (warp - 2) >> 2;               // key half of every block
         const int row = q4 * 32 + lane;
         const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-        uint32_t s_cnt = 0;
+        const uint32_t o_tm = tmem + lane_base + O_COL + hf * 128;
+        uint32_t sc = 0, unit_cnt = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-            int qt, g;
-            unit_of(a, u, qt, g);
-            const int nb = tile_blocks(a, qt);
+            int qt, g, part, b0, b1;
+            unit_of(a, u, qt, g, part);
+            item_blocks(a, qt, part, b0, b1);
+            if (b0 >= b1) continue;
+            const int nb = b1 - b0;
             const int qi = qt * a.QT + row / a.G;
             const bool valid = qi < a.M;
             const int prow = valid ? (a.pos ? a.pos[qi] : qi) : 0;
-            float m = -INFINITY, l = 0.f, alpha_pend = 0.f;
-            float o[HD];
+            const int prow_min = __reduce_min_sync(0xffffffffu, prow);
+            float m_run = -INFINITY, m_used = -INFINITY, l = 0.f;
+            for (int b = 0; b < nb; ++b) {
+                const int buf = sc & 1;
+                const uint32_t par = (sc >> 1) & 1u;
+                if (!await(ptx::smem_u32(s_full + buf), par, abort, a.status, 20 + hf, sc, u)) { ok = false; break; }
+                ptx::tc_fence_after();
+                float s[HK];
+                ptx::tmem_ld16(tmem + lane_base + S_COL + buf * 64 + hf * HK, s);
+                ptx::tmem_ld16(tmem + lane_base + S_COL + buf * 64 + hf * HK + 16, s + 16);
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(s_empty + buf));
+                const int j0 = (b0 + b) * BKV + hf * HK;
+                // causal mask only where this block crosses some row's position (warp-uniform test)
+                if (j0 + HK - 1 > prow_min) {
 #pragma unroll
-            for (int d = 0; d < HD; ++d) o[d] = 0.f;
-            for (int b = 0; b <= nb && ok; ++b) {
-                if (b < nb) {
-                    const int buf = s_cnt & 1;
-                    const uint32_t par = (s_cnt >> 1) & 1u;
-                    if (!ptx::mbar_wait(ptx::smem_u32(s_full + buf), par, abort, a.status)) { ok = false; break; }
-                    ptx::tc_fence_after();
-                    float s[BKV];
+                    for (int i = 0; i < HK; ++i) s[i] = (j0 + i <= prow) ? s[i] : -INFINITY;
+                }
+                float mx = s[0];
 #pragma unroll
-                    for (int c = 0; c < BKV / 16; ++c) ptx::tmem_ld16(tmem + lane_base + buf * 128 + c * 16, s + c * 16);
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(s_empty + buf));
-                    const int j0 = b * BKV;
-                    float mx = m;
-#pragma unroll
-                    for (int i = 0; i < BKV; ++i) {
-                        s[i] = (j0 + i <= prow) ? s[i] * a.scale_log2 : -INFINITY;
-                        mx = fmaxf(mx, s[i]);
-                    }
-                    const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - mx);
-                    float sum = 0.f;
-#pragma unroll
-                    for (int i = 0; i < BKV; ++i) {
-                        s[i] = exp2f(s[i] - mx);
-                        sum += s[i];
-                    }
-                    l = l * alpha + sum;
-                    m = mx;
-                    // P row (bf16) into the swizzled A-operand buffer
-                    if (!ptx::mbar_wait(ptx::smem_u32(p_empty + buf), par ^ 1u, abort, a.status)) { ok = false; break; }
-                    uint8_t* prow_ptr = sP + buf * NP * P_BYTES + row * 128;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint4 w, wl;
-                        bf16* hi = reinterpret_cast<bf16*>(&w);
-                        bf16* lo = reinterpret_cast<bf16*>(&wl);
-#pragma unroll
-                        for (int t = 0; t < 8; ++t) split_bf16(s[c * 8 + t], hi[t], lo[t]);
-                        *reinterpret_cast<uint4*>(prow_ptr + ((c ^ (row & 7)) << 4)) = w;
-                        if (SPLIT) *reinterpret_cast<uint4*>(prow_ptr + P_BYTES + ((c ^ (row & 7)) << 4)) = wl;
-                    }
-                    fence_proxy_async();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(p_full + buf));
-                    // accumulate the previous block's O_b with its own rescale
-                    if (b > 0) {
-                        const uint32_t ocnt = s_cnt - 1;
-                        const int ob = ocnt & 1;
-                        const uint32_t opar = (ocnt >> 1) & 1u;
-                        if (!ptx::mbar_wait(ptx::smem_u32(o_full + ob), opar, abort, a.status)) { ok = false; break; }
-                        ptx::tc_fence_after();
-#pragma unroll
-                        for (int c = 0; c < HD / 16; ++c) {
-                            float t[16];
-                            ptx::tmem_ld16(tmem + lane_base + 256 + ob * 128 + c * 16, t);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) o[c * 16 + i] = o[c * 16 + i] * alpha_pend + t[i];
+                for (int i = 1; i < HK; ++i) mx = fmaxf(mx, s[i]);
+                m_run = fmaxf(m_run, mx * a.scale_log2);      // exp2 domain
+                // O_h += P_h V for block sc-2 (same P buffer) must be complete before P buffer sc&1 is
+                // rewritten; block sc-1's update only before O_h is rescaled.  o_full[hf][x] completes
+                // once per block of parity x, and block sc's update cannot complete before its P is
+                // written, so neither wait lags its barrier by two phases.
+                if (sc >= 2 &&
+                    !await(ptx::smem_u32(o_full + hf * 2 + buf), ((sc >> 1) & 1u) ^ 1u, abort, a.status, 30 + hf, sc, u)) {
+                    ok = false;
+                    break;
+                }
+                // rescale O_h when the running max outgrew the scale in use by more than 2^8.  The TMEM
+                // accesses are warp-collective (.sync.aligned), so when any lane needs it the whole warp
+                // rescales, each row by its own factor (rescaling to the current max is always valid).
+                const bool need = m_used != -INFINITY && m_run > m_used + RESCALE_LOG2;
+                if (__any_sync(0xffffffffu, need)) {
+                    if (b > 0) {   // block sc-1 (this unit) has added into O_h
+                        const uint32_t pb = sc - 1;
+                        if (!await(ptx::smem_u32(o_full + hf * 2 + (pb & 1)), (pb >> 1) & 1u, abort, a.status, 35 + hf,
+                                   pb, u)) {
+                            ok = false;
+                            break;
                         }
-                        ptx::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(o_empty + ob));
                     }
-                    alpha_pend = alpha;
-                    ++s_cnt;
-                } else {
-                    // last block's O_b
-                    const uint32_t ocnt = s_cnt - 1;
-                    const int ob = ocnt & 1;
-                    const uint32_t opar = (ocnt >> 1) & 1u;
-                    if (!ptx::mbar_wait(ptx::smem_u32(o_full + ob), opar, abort, a.status)) { ok = false; break; }
                     ptx::tc_fence_after();
+                    const float f = (m_used == -INFINITY) ? 1.f : exp2f(m_used - m_run);
 #pragma unroll
                     for (int c = 0; c < HD / 16; ++c) {
                         float t[16];
-                        ptx::tmem_ld16(tmem + lane_base + 256 + ob * 128 + c * 16, t);
+                        ptx::tmem_ld16(o_tm + c * 16, t);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) o[c * 16 + i] = o[c * 16 + i] * alpha_pend + t[i];
+                        for (int i = 0; i < 16; ++i) t[i] *= f;
+                        ptx::tmem_st16(o_tm + c * 16, t);
                     }
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(o_empty + ob));
+                    ptx::tmem_wait_st();
+                    l *= f;
+                    m_used = m_run;
                 }
+                if (m_used == -INFINITY) m_used = m_run;    // nothing accumulated yet (O_h holds zeros)
+                // P = 2^(s * scale - m_used) (zero when nothing is visible yet), summed, and written as a
+                // bf16 hi + lo pair into the swizzled A-operand buffer (16-byte chunks hf*4 .. hf*4+3)
+                const float neg_m = (m_used == -INFINITY) ? -INFINITY : -m_used;
+                float sum = 0.f;
+#pragma unroll
+                for (int i = 0; i < HK; ++i) {
+                    s[i] = ex2_approx(fmaf(s[i], a.scale_log2, neg_m));
+                    sum += s[i];
+                }
+                l += sum;
+                uint8_t* prow_ptr = sP + buf * NP * P_BYTES + row * 128;
+#pragma unroll
+                for (int c = 0; c < HK / 8; ++c) {
+                    uint4 w, wl;
+                    __nv_bfloat162* hi = reinterpret_cast<__nv_bfloat162*>(&w);
+                    __nv_bfloat162* lo = reinterpret_cast<__nv_bfloat162*>(&wl);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const float p0 = s[c * 8 + 2 * t], p1 = s[c * 8 + 2 * t + 1];
+                        hi[t] = __floats2bfloat162_rn(p0, p1);
+                        if (SPLIT) {
+                            const float2 back = __bfloat1622float2(hi[t]);
+                            lo[t] = __floats2bfloat162_rn(p0 - back.x, p1 - back.y);
+                        }
+                    }
+                    const int chunk = (hf * 4 + c) ^ (row & 7);
+                    *reinterpret_cast<uint4*>(prow_ptr + (chunk << 4)) = w;
+                    if (SPLIT) *reinterpret_cast<uint4*>(prow_ptr + P_BYTES + (chunk << 4)) = wl;
+                }
+                fence_proxy_async();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(p_full + buf * 2 + hf));
+                ++sc;
             }
             if (!ok) break;
-            if (valid) {
-                const float inv = 1.0f / l;
-                const int head = g * a.G + row % a.G;
-                const size_t at = (size_t)qi * a.Hq * HD + (size_t)head * HD;
-#pragma unroll
-                for (int c = 0; c < HD / 8; ++c) {
-                    uint4 w, wl;
-                    bf16* h = reinterpret_cast<bf16*>(&w);
-                    bf16* lo = reinterpret_cast<bf16*>(&wl);
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) split_bf16(o[c * 8 + t] * inv, h[t], lo[t]);
-                    *reinterpret_cast<uint4*>(a.out + at + c * 8) = w;
-                    if (a.out_lo) *reinterpret_cast<uint4*>(a.out_lo + at + c * 8) = wl;
-                }
+            // the last block's O_h update
+            {
+                const uint32_t pb = sc - 1;
+                if (!await(ptx::smem_u32(o_full + hf * 2 + (pb & 1)), (pb >> 1) & 1u, abort, a.status, 40 + hf, pb, u))
+                    break;
             }
+            ptx::tc_fence_after();
+            if (hf == 0) {
+                cmb[row * 2] = m_used;
+                cmb[row * 2 + 1] = l;
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(cmb_bar));
+            } else {
+                if (!await(ptx::smem_u32(cmb_bar), unit_cnt & 1u, abort, a.status, 50, unit_cnt, u)) break;
+                const float m0 = cmb[row * 2], l0 = cmb[row * 2 + 1];
+                const float M = fmaxf(m0, m_used);
+                const float f0 = (m0 == -INFINITY) ? 0.f : exp2f(m0 - M);
+                const float f1 = (m_used == -INFINITY) ? 0.f : exp2f(m_used - M);
+                const float L = l0 * f0 + l * f1;
+                const uint32_t o0 = tmem + lane_base + O_COL, o1 = o0 + 128;
+                if (a.parts == 1) {
+                    const float inv = 1.0f / L;
+                    const int head = g * a.G + row % a.G;
+                    const size_t at = (size_t)qi * a.Hq * HD + (size_t)head * HD;
+#pragma unroll
+                    for (int c = 0; c < HD / 16; ++c) {
+                        float x0[16], x1[16];
+                        ptx::tmem_ld16(o0 + c * 16, x0);
+                        ptx::tmem_ld16(o1 + c * 16, x1);
+                        if (valid) {
+                            uint4 w[2], wl[2];
+                            bf16* h = reinterpret_cast<bf16*>(w);
+                            bf16* lo = reinterpret_cast<bf16*>(wl);
+#pragma unroll
+                            for (int t = 0; t < 16; ++t) split_bf16((x0[t] * f0 + x1[t] * f1) * inv, h[t], lo[t]);
+                            *reinterpret_cast<uint4*>(a.out + at + c * 16) = w[0];
+                            *reinterpret_cast<uint4*>(a.out + at + c * 16 + 8) = w[1];
+                            if (a.out_lo) {
+                                *reinterpret_cast<uint4*>(a.out_lo + at + c * 16) = wl[0];
+                                *reinterpret_cast<uint4*>(a.out_lo + at + c * 16 + 8) = wl[1];
+                            }
+                        }
+                    }
+                } else {
+                    // partial result of this key range: O (scaled to max M), M and the sum L
+                    float* po = a.part_o + ((size_t)u * ROWS + row) * HD;
+#pragma unroll
+                    for (int c = 0; c < HD / 16; ++c) {
+                        float x0[16], x1[16];
+                        ptx::tmem_ld16(o0 + c * 16, x0);
+                        ptx::tmem_ld16(o1 + c * 16, x1);
+#pragma unroll
+                        for (int t = 0; t < 16; t += 4)
+                            *reinterpret_cast<float4*>(po + c * 16 + t) =
+                                make_float4(x0[t] * f0 + x1[t] * f1, x0[t + 1] * f0 + x1[t + 1] * f1,
+                                            x0[t + 2] * f0 + x1[t + 2] * f1, x0[t + 3] * f0 + x1[t + 3] * f1);
+                    }
+                    *reinterpret_cast<float2*>(a.part_ml + ((size_t)u * ROWS + row) * 2) = make_float2(M, L);
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(o_free));
+            }
+            ++unit_cnt;
         }
     }
     ptx::tc_fence_before();
@@ -391,6 +503,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+// Merge the key-range parts of each (query, head): O = sum_p O_p 2^(M_p - M) / sum_p L_p 2^(M_p - M).
+// One warp per (query, head); each lane owns hd/32 consecutive dims.
+template <int HD>
+__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
+    const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (wid >= a.M * a.Hq) return;
+    const int qi = wid / a.Hq, head = wid % a.Hq;
+    const int qt = qi / a.QT, g = head / a.G;
+    const int r = (qi % a.QT) * a.G + head % a.G;
+    const int nb = tile_blocks(a, qt);
+    const int base = ((a.n_qt - 1 - qt) * a.Hkv + g) * a.parts;
+    float M = -INFINITY;
+    for (int p = 0; p < a.parts && p * a.part_blocks < nb; ++p)
+        M = fmaxf(M, a.part_ml[((size_t)(base + p) * ROWS + r) * 2]);
+    constexpr int PER = HD / 32;
+    float acc[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+    float L = 0.f;
+    for (int p = 0; p < a.parts && p * a.part_blocks < nb; ++p) {
+        const size_t it = (size_t)(base + p) * ROWS + r;
+        const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + it * 2);
+        const float f = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+        L += ml.y * f;
+        const float* po = a.part_o + it * HD + lane * PER;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) acc[i] += po[i] * f;
+    }
+    const float inv = 1.0f / L;
+    const size_t at = (size_t)qi * a.Hq * HD + (size_t)head * HD + lane * PER;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        bf16 h, lo;
+        split_bf16(acc[i] * inv, h, lo);
+        a.out[at + i] = h;
+        if (a.out_lo) a.out_lo[at + i] = lo;
     }
 }
 
@@ -410,7 +561,8 @@ bool get_encode() {
 template <int HD, bool SPLIT>
 size_t attn_smem() {
     const size_t np = SPLIT ? 2 : 1, stages = SPLIT ? 2 : 3;
-    return 1024 + np * ROWS * HD * 2 + 2 * stages * (size_t)BKV * HD * 2 + 2 * np * (size_t)ROWS * BKV * 2 + 256;
+    return 1024 + np * ROWS * HD * 2 + 2 * stages * (size_t)BKV * HD * 2 + 2 * np * (size_t)ROWS * BKV * 2 +
+           2 * ROWS * sizeof(float) + 256;
 }
 
 template <int HD, bool SPLIT>
@@ -466,7 +618,8 @@ bool attn_make_kvmap(const Model& m, const void* kv, int64_t rows, void* map_out
 }
 
 cudaError_t launch_attention_tc(const Model& m, const void* qmap, const void* qmap_lo, const void* kvmap, int layer,
-                                const int* qpos, int M, int n_keys, void* out, void* out_lo, cudaStream_t s) {
+                                const int* qpos, int M, int n_keys, void* out, void* out_lo, cudaStream_t s,
+                                int* launches) {
     const cb_config& c = m.cfg;
     AttnArgs a;
     memset(&a, 0, sizeof a);
@@ -479,6 +632,23 @@ cudaError_t launch_attention_tc(const Model& m, const void* qmap, const void* qm
     a.n_keys = n_keys;
     a.kv_z = 2 * layer;
     a.units = a.n_qt * a.Hkv;
+    // too few (query tile, KV head) units to fill the GPU: cut each key range into parts, merged by
+    // attn_combine_kernel, so the longest chain of key blocks shrinks
+    a.parts = 1;
+    const int nb_max = (n_keys + BKV - 1) / BKV;
+    a.part_blocks = nb_max;
+    if (m.part_o && a.units < 2 * m.num_sms && nb_max > 4) {
+        int parts = (4 * m.num_sms + a.units - 1) / a.units;
+        while (parts > 1 && (size_t)a.units * parts > (size_t)m.part_items) --parts;
+        if (parts > nb_max) parts = nb_max;
+        if (parts > 1) {
+            a.part_blocks = (nb_max + parts - 1) / parts;
+            a.parts = (nb_max + a.part_blocks - 1) / a.part_blocks;
+            a.part_o = m.part_o;
+            a.part_ml = m.part_ml;
+        }
+    }
+    a.units *= a.parts;
     a.pos = qpos;
     a.out = reinterpret_cast<bf16*>(out);
     a.out_lo = reinterpret_cast<bf16*>(out_lo);
@@ -490,9 +660,21 @@ cudaError_t launch_attention_tc(const Model& m, const void* qmap, const void* qm
     const CUtensorMap& mq = *reinterpret_cast<const CUtensorMap*>(qmap);
     const CUtensorMap& mql = *reinterpret_cast<const CUtensorMap*>(m.split ? qmap_lo : qmap);
     const CUtensorMap& mkv = *reinterpret_cast<const CUtensorMap*>(kvmap);
+    cudaError_t e;
     if (c.head_dim == 128)
-        return m.split ? launch_hd<128, true>(mq, mql, mkv, a, grid, s) : launch_hd<128, false>(mq, mql, mkv, a, grid, s);
-    return m.split ? launch_hd<64, true>(mq, mql, mkv, a, grid, s) : launch_hd<64, false>(mq, mql, mkv, a, grid, s);
+        e = m.split ? launch_hd<128, true>(mq, mql, mkv, a, grid, s) : launch_hd<128, false>(mq, mql, mkv, a, grid, s);
+    else
+        e = m.split ? launch_hd<64, true>(mq, mql, mkv, a, grid, s) : launch_hd<64, false>(mq, mql, mkv, a, grid, s);
+    if (launches) *launches = 1;
+    if (e != cudaSuccess || a.parts == 1) return e;
+    const int warps = M * c.n_heads;
+    const int blocks = (warps + 7) / 8;
+    if (c.head_dim == 128)
+        attn_combine_kernel<128><<<blocks, 256, 0, s>>>(a);
+    else
+        attn_combine_kernel<64><<<blocks, 256, 0, s>>>(a);
+    if (launches) *launches = 2;
+    return cudaGetLastError();
 }
 
 }  // namespace cb

@@ -135,6 +135,9 @@ struct Model {
     void* attn_lo;
     void* act_lo;
     void* q_lo;           // low part of q (split precision only)
+    float* part_o;        // attention key-range partials: [part_items][128][head_dim]
+    float* part_ml;       // [part_items][128][2]
+    int part_items;
     float* kf;            // [max_tokens][nkv] fresh K at the check layer (fp32)
     float* vf;            // [max_tokens][nkv] fresh V at the check layer (fp32)
     float* dev;           // [max_tokens] deviations
@@ -199,6 +202,7 @@ bool attn_tc_supported(const Model& m);
 bool attn_make_qmap(const Model& m, const void* q, void* map_out);
 bool attn_make_kvmap(const Model& m, const void* kv, int64_t rows, void* map_out);
 cudaError_t launch_attention_tc(const Model& m, const void* qmap, const void* qmap_lo, const void* kvmap, int layer,
-                                const int* qpos, int M, int n_keys, void* out, void* out_lo, cudaStream_t s);
+                                const int* qpos, int M, int n_keys, void* out, void* out_lo, cudaStream_t s,
+                                int* launches);
 
 }  // namespace cb

@@ -170,6 +170,11 @@ cb_status cb_blend(cb_model* model, const int32_t* tokens, int32_t n_tokens, con
  * Errors: CB_ERR_INVALID_ARG, CB_ERR_CUDA. */
 cb_status cb_model_status(cb_model* model, uint32_t* bits, int32_t clear);
 
+/* Synchronises and copies 16 diagnostic words: words[0] = the status bits; when a bounded wait gave
+ * up, words[1] = 0xA77E and words[2..7] = {barrier code, parity, counter, block, warp, work unit} of
+ * the first one (cleared with the status by cb_model_status(..., clear = 1)). */
+cb_status cb_model_diag(cb_model* model, uint32_t* words);
+
 /* Per-kernel-class timing of later cb_blend / cb_rerope calls on this model.  While enabled, each
  * launch is bracketed by CUDA events recorded on the call's stream (this serialises nothing that was
  * not already serial on that stream, but adds event records between kernels).  Classes: "rerope",

@@ -229,3 +229,24 @@ def test_tensor_core_attention_matches_cuda_core_attention(cb, monkeypatch):
     kv_a, kv_b = parity.bf16_to_f64(a["out_kv"]), parity.bf16_to_f64(b["out_kv"])
     assert np.max(np.abs(kv_a[1] - kv_b[1])) < 2e-2        # the check layer: one attention apart
     assert np.max(np.abs(kv_a - kv_b)) < 5e-2
+
+
+def test_attention_rescale_path_head_dim_128(cb):
+    """Large-magnitude keys make the running softmax max jump between key blocks, which exercises the
+    tensor-core attention's in-TMEM rescale (warp-collective); head_dim 128 with 8 KV heads."""
+    shape = workload.ModelShape(n_layers=2, d_model=256, n_heads=32, n_kv_heads=8, head_dim=128, ffn_hidden=512,
+                                vocab=1024, rope_theta=5e5, dtype="bf16")
+    w = workload.make_weights(shape, 3)
+    chunks = [(0, i * 500, 500) for i in range(4)]
+    toks = workload.tokens(3, 7, 2064, 1024)
+    caches = workload.synthetic_cache(shape, 3, 2000, 4.0)
+    model = cb.BlendModel(shape.as_dict(), w, max_tokens=2064, max_chunks=4)
+    out = model.blend(torch.from_numpy(toks).cuda(), cb.to_device(caches), chunks, 0.5, want_dev=True)
+    torch.cuda.synchronize()
+    assert model.status() == 0
+    ref = oracle.blend(shape.as_dict(), w, toks, caches, chunks, 0.5, "bf16", keep_exact=True)
+    diff = parity.assert_selection(out["selected"].cpu().numpy(), ref["selected"], ref["dev"], ref["k"])
+    assert not diff
+    parity.assert_kv(parity.bf16_to_f64(out["out_kv"]), ref["out_kv_exact"], "bf16")
+    parity.assert_logits(parity.bf16_to_f64(out["logits"]), ref["logits"], "bf16")
+    model.close()
