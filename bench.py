@@ -177,6 +177,13 @@ def max_over_ranks(ws, v):
     return float(t.item())
 
 
+def replica_throughput(ws: int, units_per_rank: float, steps: int, local_ms: float):
+    """Whole-job throughput of `ws` independent replicas: every rank processed `units_per_rank`
+    units per step; the job took as long as its slowest rank.  Returns (units/s, ms per step)."""
+    total_ms = max_over_ranks(ws, float(local_ms))
+    return ws * units_per_rank * steps / (total_ms / 1e3), total_ms / steps
+
+
 def run_reference(args, spec, ws, rank):
     """The reference arm: the CPU oracle, as it stands, on host cores (rank 0 only)."""
     if rank != 0:
@@ -297,9 +304,7 @@ def main():
         wall = time.perf_counter() - w0
     barrier(ws)
     step_ms = [a.elapsed_time(b) for a, b in evs]
-    total_ms = max_over_ranks(ws, float(np.sum(step_ms)))
-    ms_per_step = total_ms / args.steps
-    value = ws * spec.n_ctx * args.steps / (total_ms / 1e3)
+    value, ms_per_step = replica_throughput(ws, spec.n_ctx, args.steps, float(np.sum(step_ms)))
 
     # ---- per-kernel-class device time (CUDA events around each launch, a separate pass) -------
     kernels, roofline = {}, None
@@ -369,11 +374,11 @@ def main():
             e2e_step()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
-        e_ms = max_over_ranks(ws, float(np.sum([a.elapsed_time(b) for a, b in ev])))
+        e_val, e_ms = replica_throughput(ws, spec.n_ctx, args.steps, float(np.sum([a.elapsed_time(b) for a, b in ev])))
         bi = h_tokens.numel() * 4 + h_cached.numel() * h_cached.element_size()
         bo = h_out.numel() * h_out.element_size() + h_logits.numel() * 4
-        e2e = {"value": ws * spec.n_ctx * args.steps / (e_ms / 1e3), "unit": "tokens/s",
-               "latency_ms": e_ms / args.steps, "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo)}
+        e2e = {"value": e_val, "unit": "tokens/s", "latency_ms": e_ms, "h2d_bytes_per_step": int(bi),
+               "d2h_bytes_per_step": int(bo)}
 
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----------------------------------------------
     cpu = None

@@ -141,17 +141,21 @@ def attention(q, k, v, q_pos, k_pos, n_kv_heads: int) -> np.ndarray:
     k_pos = np.asarray(k_pos)
     out = np.empty((M, Hq, hd), np.float64)
     scale = 1.0 / math.sqrt(hd)
+    sorted_keys = bool(np.all(k_pos[1:] >= k_pos[:-1]))
     for b0 in range(0, M, _Q_BLOCK):
         qp = q_pos[b0:b0 + _Q_BLOCK]
-        visible = k_pos[None, :] <= qp[:, None]                     # [b][Nk]
+        # keys past the block's last position are invisible to all of its queries: with positions
+        # sorted they are simply not scored (their softmax weight would be exactly zero)
+        nk = int(np.searchsorted(k_pos, qp.max(), side="right")) if sorted_keys else k_pos.size
+        visible = k_pos[None, :nk] <= qp[:, None]                   # [b][nk]
         for h in range(Hq):
             g = h // group
-            s = (q[b0:b0 + _Q_BLOCK, h, :] @ k[:, g, :].T) * scale  # [b][Nk]
+            s = (q[b0:b0 + _Q_BLOCK, h, :] @ k[:nk, g, :].T) * scale  # [b][nk]
             s = np.where(visible, s, -np.inf)
             s = s - s.max(axis=1, keepdims=True)
             p = np.exp(s)
             p /= p.sum(axis=1, keepdims=True)
-            out[b0:b0 + _Q_BLOCK, h, :] = p @ v[:, g, :]
+            out[b0:b0 + _Q_BLOCK, h, :] = p @ v[:nk, g, :]
     return out
 
 
@@ -342,6 +346,28 @@ def blend(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratio: float, sto
 
     logits = m.logits(hA[-1])
     return dict(out_kv=out_kv, out_kv_exact=exact, logits=logits, selected=sel, dev=dev, k=kk, rows=A)
+
+
+def deviation_rows(cfg: dict, weights: dict, tokens, cached_kv, chunks, rows, store: str) -> np.ndarray:
+    """The check-layer deviation Δkv of the given context rows only.
+
+    Layer 0 of a context row depends only on its own token and the reused (re-RoPE'd) layer-0 K/V of
+    the context rows at or before it, so the blend's steps 1-4 can be followed for a subset of rows:
+    re-RoPE the caches of layers 0 and 1, layer 0 for those rows, their fresh layer-1 K/V, and the
+    deviation against the stored layer-1 cache.  Equal to blend()['dev'][rows]."""
+    m = Model(cfg, weights)
+    tokens = np.asarray(tokens, np.int64)
+    n_ctx = validate_chunks(chunks, tokens.shape[0])
+    rows = np.asarray(rows, np.int64)
+    assert rows.size and rows.max() < n_ctx
+    kv01 = rerope(np.asarray(cached_kv)[:2], chunks, m.theta, store)        # layers 0 and 1
+    h = m.embed_rows(tokens[rows])
+    W = m.layer(0)
+    q = m.q_only(W, h, rows)
+    o = attention(q, kv01[0, 0], kv01[0, 1], rows, np.arange(n_ctx), m.Hkv)
+    h = m.finish(W, h, o)
+    _, k_new, v_new = m.qkv(m.layer(1), h, rows)
+    return deviation(k_new, v_new, kv01[1, 0, rows], kv01[1, 1, rows])
 
 
 def prefill(cfg: dict, weights: dict, tokens, store: str) -> dict:

@@ -233,3 +233,15 @@ ALL_CHECKS = [check_rope_matrix, check_rope_composition, check_rmsnorm_silu, che
               check_prefill_vs_sequential, check_relative_position, check_r1_full_prefill,
               check_r0_full_reuse, check_causal_prefix, check_deviation_definition, check_topk_vs_sort,
               check_selected_count, check_round_bf16]
+
+
+def check_deviation_rows(ob):
+    """The row-restricted deviation equals the full blend's deviation on those rows."""
+    _, chunks, _, toks = micro_request()
+    full = ob.blend(MICRO_CFG, micro_weights(), toks, brute_caches(), chunks, 0.3, "f64")
+    rows = [0, 3, 8, 13, 20]
+    got = ob.deviation_rows(MICRO_CFG, micro_weights(), toks, brute_caches(), chunks, rows, "f64")
+    _close(got, full["dev"][rows], 1e-10 * max(1.0, full["dev"].max()), "deviation_rows vs blend")
+
+
+ALL_CHECKS.append(check_deviation_rows)

@@ -55,3 +55,105 @@ def test_llama8b_3k_full_blend(cb):
     print(f"logits max abs {np.abs(g_lg - ref['logits']).max():.4f}")
     parity.assert_kv(g_kv, ref["out_kv_exact"], "bf16")
     parity.assert_logits(g_lg, ref["logits"], "bf16")
+
+
+def _gpu_blend(cb, spec, seed, ratio, caches, want_dev=True):
+    shape = spec.shape
+    w = workload.make_weights(shape, seed)
+    req = workload.make_request(spec, seed, ratio)
+    model = cb.BlendModel(shape.as_dict(), w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks)
+    cached = torch.from_numpy(caches.view(np.int16)).cuda().view(torch.bfloat16)
+    out = model.blend(torch.from_numpy(req.tokens).cuda(), cached, req.chunks, ratio, want_dev=want_dev)
+    torch.cuda.synchronize()
+    assert model.status() == 0
+    res = dict(selected=out["selected"].cpu().numpy(), logits=parity.bf16_to_f64(out["logits"]), k=out["k"])
+    if want_dev:
+        res["dev"] = out["dev"].cpu().numpy().astype(np.float64)
+    res["kv"] = out["out_kv"]          # stays on the device; sampled below
+    del cached
+    return w, req, res, model
+
+
+def _kv_rows(res, layer, kv, rows):
+    t = res["kv"][layer, kv, torch.as_tensor(rows, device=res["kv"].device)]
+    return parity.bf16_to_f64(t)
+
+
+def _sampled_checks(spec, w, req, res, caches, ratio, rng, n_sample=48):
+    """Checks that need no full oracle blend: the selection is exactly the top-k of the GPU's own
+    deviations; the deviations of sampled context rows match the oracle's row-restricted deviation;
+    unselected context rows hold the re-RoPE'd cache at every layer."""
+    shape = spec.shape
+    k = res["k"]
+    assert list(res["selected"]) == list(oracle.select_hkvd(res["dev"], k))
+    rows = np.sort(rng.choice(spec.n_ctx, n_sample, replace=False))
+    ref_dev = oracle.deviation_rows(shape.as_dict(), w, req.tokens, caches, req.chunks, rows, "bf16")
+    rel = np.abs(res["dev"][rows] - ref_dev) / ref_dev
+    assert rel.max() < 2e-3, rel.max()
+    sel = set(res["selected"].tolist())
+    unsel = np.array([r for r in rows if r not in sel])
+    layers = [0, 1, shape.n_layers // 2, shape.n_layers - 1]
+    placed = oracle.rerope(caches[layers], req.chunks, shape.rope_theta, "bf16")
+    for li, layer in enumerate(layers):
+        for kv in (0, 1):
+            got = _kv_rows(res, layer, kv, unsel)
+            ref = placed[li, kv, unsel]
+            ulp = np.ldexp(1.0, np.frexp(np.abs(ref))[1] - 8)
+            assert np.all(np.abs(got - ref) <= ulp), (layer, kv)
+    return rel.max()
+
+
+def test_llama8b_8k_r005_full_blend_seed3(cb):
+    """8K context, 16 shuffled chunks, r = 0.05: the whole blend against the oracle."""
+    spec = workload.WORKLOADS["llama8b-8k"]
+    seed, ratio = 3, 0.05
+    caches = workload.synthetic_cache(spec.shape, seed, spec.n_ctx, workload.kv_std(spec.shape))
+    w, req, res, model = _gpu_blend(cb, spec, seed, ratio, caches)
+    assert [c[1] for c in req.chunks] == [512 * i for i in range(16)]
+    g_kv = parity.bf16_to_f64(res["kv"])
+    model.close()
+    ref = oracle.blend(spec.shape.as_dict(), w, req.tokens, caches, req.chunks, ratio, "bf16", keep_exact=True)
+    diff = parity.assert_selection(res["selected"], ref["selected"], ref["dev"], ref["k"])
+    if diff:
+        ref = oracle.blend(spec.shape.as_dict(), w, req.tokens, caches, req.chunks, ratio, "bf16",
+                           selected=res["selected"], keep_exact=True)
+    print(f"8K r=0.05: {len(diff)} rows in the tie band; kv max {parity.kv_error(g_kv, ref['out_kv_exact'], 'bf16')[0]:.4f}")
+    parity.assert_kv(g_kv, ref["out_kv_exact"], "bf16")
+    parity.assert_logits(res["logits"], ref["logits"], "bf16")
+
+
+@pytest.mark.parametrize("seed,ratio", [(4, 0.15), (5, 0.30)])
+def test_llama8b_8k_sampled(cb, seed, ratio):
+    """8K context at r = 0.15 (seed 4) and r = 0.30 (seed 5), shuffled chunk order: sampled checks."""
+    spec = workload.WORKLOADS["llama8b-8k"]
+    caches = workload.synthetic_cache(spec.shape, seed, spec.n_ctx, workload.kv_std(spec.shape))
+    w, req, res, model = _gpu_blend(cb, spec, seed, ratio, caches)
+    rel = _sampled_checks(spec, w, req, res, caches, ratio, np.random.default_rng(seed))
+    print(f"8K seed {seed} r={ratio}: sampled deviation rel err {rel:.2e}")
+    model.close()
+
+
+def test_llama8b_32k_sampled(cb):
+    """32K context (64 chunks + 128 query tokens), r = 0.15: sampled checks at full size."""
+    spec = workload.WORKLOADS["llama8b-32k"]
+    seed, ratio = spec.seeds[0], spec.ratios[0]
+    caches = workload.synthetic_cache(spec.shape, seed, spec.n_ctx, workload.kv_std(spec.shape))
+    w, req, res, model = _gpu_blend(cb, spec, seed, ratio, caches)
+    rel = _sampled_checks(spec, w, req, res, caches, ratio, np.random.default_rng(seed), n_sample=32)
+    print(f"32K r=0.15: sampled deviation rel err {rel:.2e}")
+    model.close()
+
+
+def test_llama8b_32k_full_reuse(cb):
+    """32K context at r = 0 (full KV reuse): the query rows' K/V at every layer and the logits
+    against the oracle; every context row is the re-RoPE'd cache."""
+    spec = workload.WORKLOADS["llama8b-32k"]
+    seed = spec.seeds[0]
+    caches = workload.synthetic_cache(spec.shape, seed, spec.n_ctx, workload.kv_std(spec.shape))
+    w, req, res, model = _gpu_blend(cb, spec, seed, 0.0, caches, want_dev=False)
+    q_rows = np.arange(spec.n_ctx, spec.n_tokens)
+    g_q = np.stack([np.stack([_kv_rows(res, l, kv, q_rows) for kv in (0, 1)]) for l in range(spec.shape.n_layers)])
+    model.close()
+    ref = oracle.blend(spec.shape.as_dict(), w, req.tokens, caches, req.chunks, 0.0, "bf16", keep_exact=True)
+    parity.assert_kv(g_q, ref["out_kv_exact"][:, :, spec.n_ctx:], "bf16", "query-row K/V")
+    parity.assert_logits(res["logits"], ref["logits"], "bf16")

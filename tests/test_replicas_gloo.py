@@ -1,0 +1,55 @@
+"""The multi-GPU path of bench.py is replicas only: every rank runs its own blend and the job's
+throughput is (ranks x units) / slowest rank.  Checked here with two gloo ranks on the CPU."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, ws, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(ws),
+                      LOCAL_RANK=str(rank))
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    ws_, rank_, local_ = bench.dist_setup(None)
+    assert (ws_, rank_, local_) == (ws, rank, rank)
+    bench.barrier(ws)
+    local_ms = [1000.0, 1500.0][rank]          # rank 1 is the slower replica
+    value, ms_per_step = bench.replica_throughput(ws, 3072, 10, local_ms)
+    out[rank] = (value, ms_per_step)
+    import torch.distributed as dist
+    dist.destroy_process_group()
+
+
+def test_replica_throughput_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    # both ranks agree: 2 replicas x 3072 tokens x 10 steps over the slower rank's 1.5 s
+    for r in range(2):
+        value, ms = out[r]
+        assert abs(value - 2 * 3072 * 10 / 1.5) < 1e-6
+        assert abs(ms - 150.0) < 1e-9
+
+
+def test_single_rank_needs_no_process_group():
+    import bench
+    value, ms = bench.replica_throughput(1, 100, 4, 200.0)
+    assert value == pytest.approx(100 * 4 / 0.2) and ms == pytest.approx(50.0)
