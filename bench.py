@@ -221,6 +221,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-profile", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time direct cb_blend calls instead of a graph replay")
     # profiling-capture helpers: a smaller case with the same per-layer kernel shapes
     ap.add_argument("--layers", type=int, default=None, help="truncate the model to its first N layers")
     ap.add_argument("--vocab", type=int, default=None, help="override the vocabulary size")
@@ -257,7 +258,6 @@ def main():
     weights = workload.make_weights(shape, seed)
     model = cb.BlendModel(shape.as_dict(), weights, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks, device=dev)
     del weights
-    stream = torch.cuda.current_stream(dev)
     if args.synthetic_cache:
         raw = workload.synthetic_cache(shape, seed, spec.n_ctx, workload.kv_std(shape))
         cached = cb.to_device(raw, dev)
@@ -277,43 +277,65 @@ def main():
     torch.cuda.synchronize()
     setup_s = time.perf_counter() - t_setup
 
+    stream = torch.cuda.Stream(dev)
+
     def step():
         return cb.cb_blend(model.handle, tokens, n, cached, req.chunks, ratio, out_kv, logits, sel, None, stream,
                            stats=True)
 
     st = None
-    for _ in range(args.warmup):
-        st = step()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            st = step()
     torch.cuda.synchronize()
 
+    def timed(fn, label):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        barrier(ws)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            torch.cuda.nvtx.range_push(label)
+            for i in range(args.steps):
+                flush.zero_()
+                evs[i][0].record(stream)
+                fn()
+                evs[i][1].record(stream)
+            torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        barrier(ws)
+        return float(np.sum([a.elapsed_time(b) for a, b in evs]))
+
+    # the blend is captured once in a CUDA graph (launch-latency free replays of the same kernels)
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+
     # ---- timed region --------------------------------------------------------------------------
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    barrier(ws)
-    torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         time.sleep(0.25)
         w0 = time.perf_counter()
-        torch.cuda.nvtx.range_push("timed_steps")
-        for i in range(args.steps):
-            flush.zero_()
-            evs[i][0].record(stream)
-            step()
-            evs[i][1].record(stream)
-        torch.cuda.nvtx.range_pop()
-        torch.cuda.synchronize()
+        local_ms = timed(graph.replay if graph is not None else step, "timed_steps")
         wall = time.perf_counter() - w0
-    barrier(ws)
-    step_ms = [a.elapsed_time(b) for a, b in evs]
-    value, ms_per_step = replica_throughput(ws, spec.n_ctx, args.steps, float(np.sum(step_ms)))
+    value, ms_per_step = replica_throughput(ws, spec.n_ctx, args.steps, local_ms)
+    direct_ms = None
+    if graph is not None:
+        direct_ms = replica_throughput(ws, spec.n_ctx, args.steps, timed(step, "direct_steps"))[1]
 
     # ---- per-kernel-class device time (CUDA events around each launch, a separate pass) -------
     kernels, roofline = {}, None
     peaks, peak_src = load_peaks()
     if not args.no_profile:
         cb.cb_profile_enable(model.handle, True, 8192)
-        for _ in range(args.steps):
-            flush.zero_()
-            step()
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                flush.zero_()
+                step()
         prof = cb.cb_profile_read(model.handle)
         cb.cb_profile_enable(model.handle, False)
         tensor_peak = peaks["bf16_tflops_sustained"] if shape.dtype == "bf16" else None
@@ -364,15 +386,16 @@ def main():
             h_out.copy_(out_kv, non_blocking=True)
             h_logits.copy_(logits, non_blocking=True)
 
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        for i in range(args.steps):
-            flush.zero_()
-            ev[i][0].record(stream)
-            e2e_step()
-            ev[i][1].record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                e2e_step()
+            torch.cuda.synchronize()
+            for i in range(args.steps):
+                flush.zero_()
+                ev[i][0].record(stream)
+                e2e_step()
+                ev[i][1].record(stream)
         torch.cuda.synchronize()
         e_val, e_ms = replica_throughput(ws, spec.n_ctx, args.steps, float(np.sum([a.elapsed_time(b) for a, b in ev])))
         bi = h_tokens.numel() * 4 + h_cached.numel() * h_cached.element_size()
@@ -400,7 +423,10 @@ def main():
                            "seed": seed, "parallelism": "replicas" if ws > 1 else "single",
                            "l2": "inputs exceed L2 (16 GB weights, 384 MiB caches) and a 256 MiB buffer is "
                                  "rewritten between steps outside the timed events",
-                           "timing": "CUDA events around each step on the launching stream, summed over the steps",
+                           "timing": ("CUDA events around each step on the launching stream, summed over the steps; "
+                                      + ("each step replays one cb_blend captured in a CUDA graph"
+                                         if graph is not None else "each step is a direct cb_blend call")),
+                           "direct_call_ms_per_step": direct_ms,
                            "setup_s": round(setup_s, 1), "wall_s_timed": round(wall, 4)},
                 "gpu_launches": int(st["kernel_launches"]) * args.steps if st else None,
                 "clocks": clocks, "roofline": roofline, "kernels": kernels, "e2e": e2e, "cpu_baseline": cpu}

@@ -148,7 +148,8 @@ def attention(q, k, v, q_pos, k_pos, n_kv_heads: int) -> np.ndarray:
         # sorted they are simply not scored (their softmax weight would be exactly zero)
         nk = int(np.searchsorted(k_pos, qp.max(), side="right")) if sorted_keys else k_pos.size
         visible = k_pos[None, :nk] <= qp[:, None]                   # [b][nk]
-        for h in range(Hq):
+
+        def head(h):
             g = h // group
             s = (q[b0:b0 + _Q_BLOCK, h, :] @ k[:nk, g, :].T) * scale  # [b][nk]
             s = np.where(visible, s, -np.inf)
@@ -156,6 +157,8 @@ def attention(q, k, v, q_pos, k_pos, n_kv_heads: int) -> np.ndarray:
             p = np.exp(s)
             p /= p.sum(axis=1, keepdims=True)
             out[b0:b0 + _Q_BLOCK, h, :] = p @ v[:nk, g, :]
+
+        list(_pool().map(head, range(Hq)))           # heads are independent
     return out
 
 
