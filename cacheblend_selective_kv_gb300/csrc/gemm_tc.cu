@@ -27,11 +27,14 @@ namespace cb {
 
 struct TcMaps {
     std::vector<CUtensorMap> wq, wk, wv, wo, wg, wu, wd;   // per layer, box {64, 128}
+    std::vector<CUtensorMap> wg64, wu64;                    // per layer, box {64, 64} (paired SwiGLU)
+    bool pair = true;                                       // CTA-pair kernel usable
+    int pair_clusters[2][3] = {};                           // co-resident clusters per (SPLIT, EPI), 0 = unknown
     const void* xptr[4];                                    // activation buffers (hi) and their row widths
     const void* xptr_lo[4];                                 // low parts (split precision) or NULL
     int xcols[4];
     int rows;
-    // token-tile maps, one box of {64, BN} rows per (buffer, BN), made on first use
+    // token-tile maps, one box of {64, rows} per (buffer, box rows), made on first use
     mutable std::map<int, CUtensorMap> xb[4], xb_lo[4];
 };
 
@@ -404,6 +407,230 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
+
+// =================================================================================================
+// CTA-pair kernel (cluster of 2, tcgen05 cta_group::2).
+//
+// One MMA covers M = 256 weight rows: each CTA of the pair stages 128 of them and half of the
+// token tile, and its TMEM receives the accumulator of its own 128 rows for all BN tokens.  Per
+// MMA cycle a CTA thus writes and reads about two thirds of the shared-memory bytes of the
+// single-CTA kernel above, whose split-precision main loop is bound by shared-memory bandwidth.
+//   rank 0, warp 0 / rank 1, warp 0   TMA of the own A rows and B half; completion on rank 0's
+//                                      full barrier (rank 0 expects both CTAs' bytes)
+//   rank 0, warp 1                     MMA issuer; commits release both CTAs' stages and signal
+//                                      both CTAs' accumulators
+//   both, warps 2..5                   epilogue of the own 128 rows; rank 0's tempty barrier
+//                                      counts all 8 epilogue warps
+// SwiGLU pairs gate and up rows of the same features in one CTA: rows 0-63 gate and 64-127 up of
+// 64 features (the pair covers 128), so each feature's gate and up meet in one CTA's TMEM and the
+// epilogue exchanges them between lane quarters q and q ^ 2 through shared memory.
+// =================================================================================================
+constexpr int EPI_SMEM_PAIR = 4 * 2 * 32 * 17 * 4;   // [quarter][slot][32 x 17] floats
+
+__device__ __forceinline__ void epi_swiglu_pair(const TcArgs& a, int feat, bool fv, int q, int lane, int tok0,
+                                                int ntok_c, int slot, const float* v, float* xs) {
+    const EpiParams& e = a.e;
+    float* mine = xs + ((q * 2 + slot) * 32) * 17;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) mine[lane * 17 + j] = v[j];
+    ptx::named_bar_sync(1 + (q & 1), 64);
+    const float* gs = xs + (((q & 1) * 2 + slot) * 32) * 17;         // gate quarter (q & 1)
+    const float* us = xs + ((((q & 1) + 2) * 2 + slot) * 32) * 17;   // up quarter (q & 1) + 2
+    const int j0 = q < 2 ? 0 : 8;                                     // gate warp: tokens 0-7, up warp: 8-15
+    if (fv) {
+        bf16* act = reinterpret_cast<bf16*>(e.act);
+        bf16* act_lo = reinterpret_cast<bf16*>(e.act_lo);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int j = j0 + i;
+            if (j >= ntok_c) break;
+            bf16 hi, lo;
+            split_bf16(silu_mul(gs[lane * 17 + j], us[lane * 17 + j]), hi, lo);
+            act[(size_t)(tok0 + j) * e.ld_act + feat] = hi;
+            if (act_lo) act_lo[(size_t)(tok0 + j) * e.ld_act + feat] = lo;
+        }
+    }
+    __syncwarp();
+}
+
+template <int EPI, bool SPLIT>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mxl,
+                     const __grid_constant__ CUtensorMap mw0, const __grid_constant__ CUtensorMap mw1,
+                     const __grid_constant__ CUtensorMap mw2, const TcArgs a) {
+    constexpr bool SWIGLU = EPI == EPI_SWIGLU;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int bh_bytes = (a.BN / 2) * 128;               // this CTA's half of a token tile (hi or lo)
+    const int stage_bytes = A_BYTES + (SPLIT ? 2 : 1) * bh_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.stages * stage_bytes);
+    uint64_t* full = bars;                               // used in rank 0 only
+    uint64_t* empty = bars + MAX_STAGES;
+    uint64_t* tfull = bars + 2 * MAX_STAGES;
+    uint64_t* tempty = tfull + 2;                        // used in rank 0 only
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    float* sepi = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);
+    int* spos = reinterpret_cast<int*>(sepi);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_rank();
+    const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < a.stages; ++i) {
+            ptx::mbar_init(ptx::smem_u32(full + i), 1);
+            ptx::mbar_init(ptx::smem_u32(empty + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(ptx::smem_u32(tfull + i), 1);
+            ptx::mbar_init(ptx::smem_u32(tempty + i), 8);
+        }
+        ptx::mbar_init(ptx::smem_u32(drain), 1);
+        *abort = 0;
+        ptx::fence_barrier_init();
+        ptx::prefetch_tmap(&mx);
+        if (SPLIT) ptx::prefetch_tmap(&mxl);
+        ptx::prefetch_tmap(&mw0);
+        if (a.nseg > 1 || SWIGLU) ptx::prefetch_tmap(&mw1);
+        if (a.nseg > 2) ptx::prefetch_tmap(&mw2);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(ptx::smem_u32(tmem_holder), TMEM_COLS);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    ptx::cluster_sync();                                 // barriers of both CTAs initialised
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            const uint32_t full0 = ptx::map_to_rank(ptx::smem_u32(full), 0);
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_parity = 0;
+            bool ok = true;
+            for (int u = cluster; u < a.units && ok; u += nclusters) {
+                const Unit w = decode_unit(a, u);
+                const CUtensorMap* wm = w.seg == 0 ? &mw0 : (w.seg == 1 ? &mw1 : &mw2);
+                const int arow = SWIGLU ? w.lt * 128 + (int)rank * 64 : (2 * w.lt + (int)rank) * BM;
+                const int r0 = a.x_row0 + w.t * a.BN + (int)rank * (a.BN / 2);
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!ptx::mbar_wait(ptx::smem_u32(empty + stage), phase ^ 1u, abort, a.status)) { ok = false; break; }
+                    const uint32_t sa = ptx::smem_u32(smem + stage * stage_bytes);
+                    const uint32_t fb = full0 + stage * 8;
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(ptx::smem_u32(full + stage), 2 * stage_bytes);
+                    const int kc = kb * BK;
+                    if (SWIGLU) {
+                        ptx::tma_load_2d_pair(sa, &mw0, kc, arow, fb);
+                        ptx::tma_load_2d_pair(sa + A_BYTES / 2, &mw1, kc, arow, fb);
+                    } else {
+                        ptx::tma_load_2d_pair(sa, wm, kc, arow, fb);
+                    }
+                    ptx::tma_load_2d_pair(sa + A_BYTES, &mx, kc, r0, fb);
+                    if (SPLIT) ptx::tma_load_2d_pair(sa + A_BYTES + bh_bytes, &mxl, kc, r0, fb);
+                    issued |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == a.stages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // Before the CTA may exit, every load it issued has landed and every release the MMA
+            // issuer multicast to this CTA has arrived: wait for the last release of each stage.
+            if (!*abort) {
+                for (int i = 0; i < a.stages; ++i)
+                    if (issued & (1u << i)) drain_wait(ptx::smem_u32(empty + i), (issued_parity >> i) & 1u, a.status);
+            } else {
+                const uint64_t t0 = ptx::global_ns();   // error path: give loads in flight time to land
+                while (ptx::global_ns() - t0 < 200000ull) {}
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer (rank 0)
+        if (lane == 0 && rank == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int u = cluster; u < a.units && ok; u += nclusters) {
+                const Unit w = decode_unit(a, u);
+                if (!ptx::mbar_wait(ptx::smem_u32(tempty + acc), acc_phase ^ 1u, abort, a.status)) break;
+                ptx::tc_fence_after();
+                const uint32_t d = tmem_base + acc * 256;
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!ptx::mbar_wait(ptx::smem_u32(full + stage), phase, abort, a.status)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    const uint32_t sa = ptx::smem_u32(smem + stage * stage_bytes);
+                    const uint64_t ad = ptx::sdesc_sw128(sa);
+                    const uint64_t bd = ptx::sdesc_sw128(sa + A_BYTES);
+                    const uint64_t bl = ptx::sdesc_sw128(sa + A_BYTES + bh_bytes);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint32_t accum = (kb > w.kb0 || kk > 0) ? 1u : 0u;
+                        ptx::mma_bf16_pair(d, ad + 2 * kk, bd + 2 * kk, a.idesc, accum);
+                        if (SPLIT) ptx::mma_bf16_pair(d, ad + 2 * kk, bl + 2 * kk, a.idesc, 1u);
+                    }
+                    ptx::mma_commit_pair(ptx::smem_u32(empty + stage), 0x3);
+                    if (++stage == a.stages) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                ptx::mma_commit_pair(ptx::smem_u32(tfull + acc), 0x3);
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+            ptx::mma_commit_pair(ptx::smem_u32(drain), 0x1);
+            drain_wait(ptx::smem_u32(drain), 0, a.status);
+        }
+    } else {
+        // ------------------------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const uint32_t tempty0 = ptx::map_to_rank(ptx::smem_u32(tempty), 0);
+        int acc = 0, gc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = cluster; u < a.units; u += nclusters) {
+            Unit w = decode_unit(a, u);
+            if (!SWIGLU) w.lt = 2 * w.lt + (int)rank;
+            if (!ptx::mbar_wait(ptx::smem_u32(tfull + acc), acc_phase, abort, a.status)) break;
+            ptx::tc_fence_after();
+            const int tok0 = w.t * a.BN;
+            const int ntok = min(a.BN, a.M - tok0);
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256;
+            if (EPI == EPI_QKV) {
+                int* wpos = spos + (warp - 2) * (32 * 17);
+                for (int i = lane; i < ntok; i += 32) wpos[i] = epi_pos(a.e, tok0 + i);
+                __syncwarp();
+                qkv_tile(a, w, row, lane, tok0, ntok, tbase, wpos);
+                __syncwarp();
+            } else if (EPI == EPI_RESID) {
+                for (int c = 0; c * 16 < ntok; ++c) {
+                    float v[16];
+                    ptx::tmem_ld16(tbase + c * 16, v);
+                    epi_resid(a, w, row, lane, tok0 + c * 16, v, sepi + (warp - 2) * (32 * 17));
+                }
+            } else {
+                const int feat = w.lt * 128 + (int)rank * 64 + (q & 1) * 32 + lane;
+                const bool fv = feat < a.seg_rows[0];
+                for (int c = 0; c * 16 < ntok; ++c, ++gc) {
+                    float v[16];
+                    __syncwarp();
+                    ptx::tmem_ld16(tbase + c * 16, v);
+                    epi_swiglu_pair(a, feat, fv, q, lane, tok0 + c * 16, min(16, ntok - c * 16), gc & 1, v, sepi);
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster(tempty0 + acc * 8);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+    __syncwarp();
+    ptx::tc_fence_before();
+    ptx::cluster_sync();                                 // no operation of either CTA still targets the other
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows, std::string& err) {
@@ -433,6 +660,44 @@ cudaError_t launch_kernel(const CUtensorMap& mx, const CUtensorMap& mxl, const C
     }
     gemm_tc_kernel<EPI, SPLIT><<<grid, NUM_THREADS, smem, s>>>(mx, mxl, *w0, w1 ? *w1 : *w0, w2 ? *w2 : *w0, a);
     return cudaGetLastError();
+}
+
+template <int EPI, bool SPLIT>
+cudaError_t launch_pair(const CUtensorMap& mx, const CUtensorMap& mxl, const CUtensorMap* w0, const CUtensorMap* w1,
+                        const CUtensorMap* w2, const TcArgs& a, int grid, size_t smem, cudaStream_t s) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e =
+            cudaFuncSetAttribute(gemm_pair_kernel<EPI, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    gemm_pair_kernel<EPI, SPLIT><<<grid, NUM_THREADS, smem, s>>>(mx, mxl, *w0, w1 ? *w1 : *w0, w2 ? *w2 : *w0, a);
+    return cudaGetLastError();
+}
+
+// clusters of the pair kernel that fit on the device at once (one CTA per SM)
+template <int EPI, bool SPLIT>
+int pair_capacity(size_t smem) {
+    cudaFuncSetAttribute(gemm_pair_kernel<EPI, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<EPI, SPLIT>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 }  // namespace
@@ -467,13 +732,18 @@ bool tc_init(Model& m, std::string& err) {
     const int L = c.n_layers;
     t->wq.resize(L); t->wk.resize(L); t->wv.resize(L); t->wo.resize(L); t->wg.resize(L); t->wu.resize(L);
     t->wd.resize(L);
+    t->wg64.resize(L); t->wu64.resize(L);
     bool ok = true;
     for (int l = 0; l < L && ok; ++l) {
         ok = make_map(&t->wq[l], m.wq[l], nq, d, BM, err) && make_map(&t->wk[l], m.wk[l], nkv, d, BM, err) &&
              make_map(&t->wv[l], m.wv[l], nkv, d, BM, err) && make_map(&t->wo[l], m.wo[l], d, nq, BM, err) &&
              make_map(&t->wg[l], m.w_gate[l], F, d, BM, err) && make_map(&t->wu[l], m.w_up[l], F, d, BM, err) &&
-             make_map(&t->wd[l], m.w_down[l], d, F, BM, err);
+             make_map(&t->wd[l], m.w_down[l], d, F, BM, err) && make_map(&t->wg64[l], m.w_gate[l], F, d, 64, err) &&
+             make_map(&t->wu64[l], m.w_up[l], F, d, 64, err);
     }
+    // CTA pairs need at least one co-resident cluster; CB_GEMM_PAIR=0 keeps the single-CTA kernel
+    const char* pe = getenv("CB_GEMM_PAIR");
+    t->pair = m.num_sms >= 2 && !(pe && pe[0] == '0');
     t->xptr[XBUF_X] = m.x; t->xptr[XBUF_XA] = m.xA; t->xptr[XBUF_ATTN] = m.attn; t->xptr[XBUF_ACT] = m.act;
     t->xptr_lo[XBUF_X] = m.x_lo; t->xptr_lo[XBUF_XA] = m.xA_lo; t->xptr_lo[XBUF_ATTN] = m.attn_lo;
     t->xptr_lo[XBUF_ACT] = m.act_lo;
@@ -495,9 +765,11 @@ void tc_destroy(Model& m) {
 cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, const GemmW& w, int N,
                            const EpiParams& e, cudaStream_t s, int* launches) {
     (void)N;
-    const TcMaps& t = *m.tc;
+    TcMaps& t = *m.tc;
     const int l = w.layer;
     const bool swiglu = e.kind == EPI_SWIGLU;
+    const bool split = m.split;
+    const bool pair = t.pair;
     TcArgs a;
     memset(&a, 0, sizeof a);
     a.M = M;
@@ -512,21 +784,27 @@ cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, c
         case WSEL_Q: wm[0] = &t.wq[l]; break;
         case WSEL_KV: wm[0] = &t.wk[l]; wm[1] = &t.wv[l]; break;
         case WSEL_O: wm[0] = &t.wo[l]; break;
-        case WSEL_GATEUP: wm[0] = &t.wg[l]; wm[1] = &t.wu[l]; break;
+        case WSEL_GATEUP:
+            wm[0] = pair ? &t.wg64[l] : &t.wg[l];
+            wm[1] = pair ? &t.wu64[l] : &t.wu[l];
+            break;
         default: wm[0] = &t.wd[l]; break;
     }
+    // weight tiles: 128 rows per CTA; a pair covers 256 rows (SwiGLU: 128 features, gate + up)
+    const int rows_per_tile = pair ? (swiglu ? 128 : 256) : BM;
     a.nseg = swiglu ? 1 : w.nseg;
     int mtiles = 0, base = 0;
     for (int i = 0; i < a.nseg; ++i) {
         a.seg_rows[i] = w.rows[i];
-        a.seg_tiles[i] = (w.rows[i] + BM - 1) / BM;
+        a.seg_tiles[i] = (w.rows[i] + rows_per_tile - 1) / rows_per_tile;
         a.seg_base[i] = base;
         base += w.rows[i];
         mtiles += a.seg_tiles[i];
     }
-    // token tiles: the fewest-padding split into tiles of at most 256 (128 for SwiGLU) rows
-    int bn_max = swiglu ? 128 : 256;
-    if (const char* t = getenv("CB_TUNE_BN")) bn_max = std::min(bn_max, std::max(16, atoi(t)));
+    // token tiles: the fewest-padding split into tiles of at most 256 rows (single-CTA SwiGLU,
+    // whose gate and up accumulators share one TMEM buffer: 128), multiples of 16
+    int bn_max = (swiglu && !pair) ? 128 : 256;
+    if (const char* v = getenv("CB_TUNE_BN")) bn_max = std::min(bn_max, std::max(16, atoi(v)));
     int best_T = 0, best_BN = 0;
     for (int T0 = (M + bn_max - 1) / bn_max, T = T0; T <= T0 + 2; ++T) {
         int bn = ((M + T - 1) / T + 15) / 16 * 16;
@@ -536,42 +814,62 @@ cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, c
     }
     a.ttiles = best_T;
     a.BN = best_BN;
+    const int epi_smem = pair ? EPI_SMEM_PAIR : EPI_SMEM;
+    const int b_rows = pair ? a.BN / 2 : a.BN;                 // token rows one CTA stages
+    const int stage_bytes = (swiglu && !pair ? 2 * A_BYTES : A_BYTES) + (split ? 2 : 1) * b_rows * 128;
+    const int budget = 227 * 1024 - 1024 - 256 - epi_smem;
+    a.stages = budget / stage_bytes;
+    if (a.stages > MAX_STAGES) a.stages = MAX_STAGES;
+    if (const char* v = getenv("CB_TUNE_STAGES")) a.stages = std::min(a.stages, std::max(2, atoi(v)));
+    if (a.stages < 2) return cudaErrorInvalidConfiguration;
+    // one CTA per SM (each holds all 512 TMEM columns)
+    const size_t smem = std::max<size_t>(1024 + (size_t)a.stages * stage_bytes + 256 + epi_smem, 120 * 1024);
+    // co-resident workers: SMs, or clusters of two
+    int workers = m.num_sms;
+    if (pair) {
+        int& cap = t.pair_clusters[split ? 1 : 0][e.kind];
+        if (cap == 0) {
+            switch (e.kind) {
+                case EPI_QKV: cap = split ? pair_capacity<EPI_QKV, true>(smem) : pair_capacity<EPI_QKV, false>(smem); break;
+                case EPI_RESID:
+                    cap = split ? pair_capacity<EPI_RESID, true>(smem) : pair_capacity<EPI_RESID, false>(smem);
+                    break;
+                default: cap = split ? pair_capacity<EPI_SWIGLU, true>(smem) : pair_capacity<EPI_SWIGLU, false>(smem);
+            }
+            if (cap <= 0) cap = -1;
+        }
+        if (cap < 0) return cudaErrorInvalidConfiguration;
+        workers = cap;
+    }
     // split K only where the epilogue accumulates (residual adds): pick the split that minimises
     // waves x (k-blocks per unit + 2 blocks of per-unit latency)
     a.splits = 1;
     if (e.kind == EPI_RESID) {
         double best = 1e30;
         int smax = 8;
-        if (const char* t = getenv("CB_TUNE_SPLITK")) smax = std::max(1, atoi(t));
+        if (const char* v = getenv("CB_TUNE_SPLITK")) smax = std::max(1, atoi(v));
         for (int S = 1; S <= smax; ++S) {
             if (a.kb_total / S < 4) break;
             const long long units = (long long)mtiles * a.ttiles * S;
-            const long long waves = (units + m.num_sms - 1) / m.num_sms;
+            const long long waves = (units + workers - 1) / workers;
             const double cost = waves * ((double)a.kb_total / S + 2.0);
             if (cost < best - 1e-9) { best = cost; a.splits = S; }
         }
     }
     a.units = mtiles * a.ttiles * a.splits;
-    const bool split = m.split;
-    const int stage_bytes = (swiglu ? 2 * A_BYTES : A_BYTES) + (split ? 2 : 1) * a.BN * 128;
-    const int budget = 227 * 1024 - 1024 - 256 - EPI_SMEM;
-    a.stages = budget / stage_bytes;
-    if (a.stages > MAX_STAGES) a.stages = MAX_STAGES;
-    if (const char* t = getenv("CB_TUNE_STAGES")) a.stages = std::min(a.stages, std::max(2, atoi(t)));
     a.prefetch = 0;
-    if (const char* t = getenv("CB_TUNE_PF")) a.prefetch = std::max(0, atoi(t));
-    if (a.stages < 2) return cudaErrorInvalidConfiguration;
-    a.idesc = ptx::idesc_bf16(BM, a.BN);
-    const size_t smem = 1024 + (size_t)a.stages * stage_bytes + 256 + EPI_SMEM;
-    const int grid = a.units < m.num_sms ? a.units : m.num_sms;
+    if (!pair)
+        if (const char* v = getenv("CB_TUNE_PF")) a.prefetch = std::max(0, atoi(v));
+    a.idesc = ptx::idesc_bf16(pair ? 256 : BM, a.BN);
+    const int grid = pair ? 2 * std::min(a.units, workers) : std::min(a.units, workers);
     if (launches) *launches = 1;
-    auto tile_map = [&](std::map<int, CUtensorMap>& cache, const void* base, CUtensorMap** out) -> bool {
-        auto it = cache.find(a.BN);
+    auto tile_map = [&](std::map<int, CUtensorMap>& cache, const void* ptr, CUtensorMap** out) -> bool {
+        auto it = cache.find(b_rows);
         if (it == cache.end()) {
             CUtensorMap mp;
             std::string err;
-            if (!make_map(&mp, base, (uint64_t)t.rows, (uint64_t)t.xcols[xbuf], (uint32_t)a.BN, err)) return false;
-            it = cache.emplace(a.BN, mp).first;
+            if (!make_map(&mp, ptr, (uint64_t)t.rows, (uint64_t)t.xcols[xbuf], (uint32_t)b_rows, err)) return false;
+            it = cache.emplace(b_rows, mp).first;
         }
         *out = &it->second;
         return true;
@@ -581,18 +879,24 @@ cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, c
     if (split && !tile_map(t.xb_lo[xbuf], t.xptr_lo[xbuf], &pmxl)) return cudaErrorInvalidValue;
     const CUtensorMap& mx = *pmx;
     const CUtensorMap& mxl = split ? *pmxl : *pmx;
-    if (split) {
-        switch (e.kind) {
-            case EPI_QKV: return launch_kernel<EPI_QKV, true>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s);
-            case EPI_RESID: return launch_kernel<EPI_RESID, true>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s);
-            default: return launch_kernel<EPI_SWIGLU, true>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s);
-        }
-    }
-    switch (e.kind) {
-        case EPI_QKV: return launch_kernel<EPI_QKV, false>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s);
-        case EPI_RESID: return launch_kernel<EPI_RESID, false>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s);
-        default: return launch_kernel<EPI_SWIGLU, false>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s);
-    }
+#define CB_GEMM_DISPATCH(LAUNCH)                                                                     \
+    do {                                                                                             \
+        if (split) {                                                                                 \
+            switch (e.kind) {                                                                        \
+                case EPI_QKV: return LAUNCH<EPI_QKV, true>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s);     \
+                case EPI_RESID: return LAUNCH<EPI_RESID, true>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s); \
+                default: return LAUNCH<EPI_SWIGLU, true>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s);       \
+            }                                                                                        \
+        }                                                                                            \
+        switch (e.kind) {                                                                            \
+            case EPI_QKV: return LAUNCH<EPI_QKV, false>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s);        \
+            case EPI_RESID: return LAUNCH<EPI_RESID, false>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s);    \
+            default: return LAUNCH<EPI_SWIGLU, false>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s);          \
+        }                                                                                            \
+    } while (0)
+    if (pair) CB_GEMM_DISPATCH(launch_pair);
+    CB_GEMM_DISPATCH(launch_kernel);
+#undef CB_GEMM_DISPATCH
 }
 
 }  // namespace cb

@@ -250,3 +250,50 @@ def test_attention_rescale_path_head_dim_128(cb):
     parity.assert_kv(parity.bf16_to_f64(out["out_kv"]), ref["out_kv_exact"], "bf16")
     parity.assert_logits(parity.bf16_to_f64(out["logits"]), ref["logits"], "bf16")
     model.close()
+
+
+def test_cta_pair_gemms_match_single_cta_gemms(cb, monkeypatch):
+    """The CTA-pair tcgen05 GEMMs (M = 256 over two SMs) and the single-CTA ones give the same blend up
+    to summation order (split-K partial sums may differ in order)."""
+    spec, w, req, caches, ratio = setup_case("small-bf16")
+    shape = spec.shape.as_dict()
+    tokens = torch.from_numpy(req.tokens).cuda()
+    outs = []
+    for pair in ("1", "0"):
+        monkeypatch.setenv("CB_GEMM_PAIR", pair)
+        model = cb.BlendModel(shape, w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks)
+        outs.append(model.blend(tokens, cached_tensor(caches, "bf16"), req.chunks, ratio, want_dev=True))
+        torch.cuda.synchronize()
+        assert model.status() == 0
+        model.close()
+    a, b = outs
+    dev_a, dev_b = a["dev"].cpu().numpy(), b["dev"].cpu().numpy()
+    assert np.max(np.abs(dev_a - dev_b) / (np.abs(dev_b) + 1e-3 * dev_b.max())) < 1e-3
+    kv_a, kv_b = parity.bf16_to_f64(a["out_kv"]), parity.bf16_to_f64(b["out_kv"])
+    assert np.max(np.abs(kv_a[0] - kv_b[0])) < 1e-2
+    assert np.max(np.abs(kv_a - kv_b)) < 3e-2
+
+
+def test_ragged_projection_shapes(cb):
+    """Output widths that are not multiples of a CTA pair's 256 weight rows (d_model 384, KV width 128,
+    SwiGLU hidden 704 = 5.5 x 128) and a token count that is not a multiple of 16: the tiles past the
+    end read zeros and store nothing."""
+    shape = workload.ModelShape(n_layers=3, d_model=384, n_heads=6, n_kv_heads=2, head_dim=64, ffn_hidden=704,
+                                vocab=1024, rope_theta=1e4, dtype="bf16")
+    w = workload.make_weights(shape, 5)
+    chunks = [(0, 0, 100), (0, 100, 77), (0, 177, 64)]
+    n_ctx, n_tok = 241, 241 + 19
+    toks = workload.tokens(5, 9, n_tok, 1024)
+    caches = workload.synthetic_cache(shape, 5, n_ctx, workload.kv_std(shape))
+    model = cb.BlendModel(shape.as_dict(), w, max_tokens=n_tok, max_chunks=3)
+    out = model.blend(torch.from_numpy(toks).cuda(), cb.to_device(caches), chunks, 0.3, want_dev=True)
+    torch.cuda.synchronize()
+    assert model.status() == 0
+    ref = oracle.blend(shape.as_dict(), w, toks, caches, chunks, 0.3, "bf16", keep_exact=True)
+    diff = parity.assert_selection(out["selected"].cpu().numpy(), ref["selected"], ref["dev"], ref["k"])
+    if diff:
+        ref = oracle.blend(shape.as_dict(), w, toks, caches, chunks, 0.3, "bf16",
+                           selected=out["selected"].cpu().numpy(), keep_exact=True)
+    parity.assert_kv(parity.bf16_to_f64(out["out_kv"]), ref["out_kv_exact"], "bf16")
+    parity.assert_logits(parity.bf16_to_f64(out["logits"]), ref["logits"], "bf16")
+    model.close()
