@@ -388,3 +388,122 @@ def chunk_caches(cfg: dict, weights: dict, chunk_tokens, chunks, store: str) -> 
             raise NotImplementedError("chunk caches are prefilled from position 0")
         parts.append(prefill(cfg, weights, toks, store)["out_kv"])
     return np.concatenate(parts, axis=2)
+
+
+# ----------------------------------------------------------------------------------------------
+# gradual filtering (Figure 9 of the page)
+# ----------------------------------------------------------------------------------------------
+def gradual_counts(n_ctx: int, ratios) -> list:
+    """Per-layer selected counts k_l = ceil(r_l * n_ctx) for layers 1..L-1 (reading R3 per layer).
+
+    Section "核心思想" (gradual filtering): r_1 > r_2 > ... so that S_{l+1} is a subset of S_l;
+    a schedule that grows is rejected."""
+    ks = [selected_count(n_ctx, r) for r in ratios]
+    if any(not (0.0 <= float(r) <= 1.0) for r in ratios):
+        raise ValueError("ratios must lie in [0, 1]")
+    if any(b > a for a, b in zip(ks, ks[1:])):
+        raise ValueError("the selected counts must not grow from layer to layer")
+    return ks
+
+
+def blend_gradual(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratios, store: str, selected=None,
+                  keep_exact: bool = False) -> dict:
+    """CacheBlend blend with gradual filtering: the recomputed set shrinks layer by layer.
+
+    Sections "核心思想" and "选 token" of the page (the funnel of Figure 9):
+      * layer 0 and the check layer 1 are as in blend(); layer 1 keeps k_1 = ceil(r_1 n_ctx) rows S_1;
+      * at a later layer l only the rows that carried an updated hidden state out of layer l-1
+        (S_{l-1}, plus the query) get fresh Q/K/V; where k_l < k_{l-1}, each candidate's deviation ||KV_new - KV_pre||^2 against the re-RoPE'd
+        cache of layer l (taken before the store) ranks the candidates again and S_l is the top k_l
+        of them (ties to the lower position), so S_l is a subset of S_{l-1};
+      * the fresh K/V of S_l and the query are stored (reading R10), then attention, O and MLP run
+        for S_l plus the query only: theirs are the hidden states passed on.
+    ``ratios`` has one entry per layer 1..L-1 and must give non-increasing counts.
+    Readings added to R1-R9:
+      R10 a layer that compares treats its candidates as the check layer treats every row: the
+          fresh K/V of the rows it keeps are stored, and a candidate that drops out keeps its cached
+          K/V from that layer on (its fresh K/V served only the comparison);
+      R11 a layer whose count equals the previous one keeps the set without comparing (the page's
+          check_flag off); the comparison would select every candidate anyway.
+    ``selected`` (optional) maps a layer to the k_l rows to use there instead of the top-k choice
+    (only to follow another implementation through a tie inside the comparison band).
+
+    Returns dict(out_kv, out_kv_exact, logits, sets {layer: S_l ascending}, devs {layer: dev of
+    that layer's candidates, in the candidates' order}, counts [k_1..k_{L-1}], rows: final A)."""
+    m = Model(cfg, weights)
+    tokens = np.asarray(tokens, np.int64)
+    N = tokens.shape[0]
+    n_ctx = validate_chunks(chunks, N)
+    L, Hkv, hd = m.L, m.Hkv, m.hd
+    if len(ratios) != L - 1:
+        raise ValueError("one ratio per layer 1..L-1")
+    counts = gradual_counts(n_ctx, ratios)
+    selected = selected or {}
+    pos = np.arange(N)
+    query = np.arange(n_ctx, N)
+
+    kv_dtype = np.float64 if store == "f64" else np.float32
+    out_kv = np.zeros((L, 2, N, Hkv, hd), kv_dtype)
+    if n_ctx:
+        out_kv[:, :, :n_ctx] = rerope(cached_kv, chunks, m.theta, store)
+    exact = np.zeros((L, 2, N, Hkv, hd), np.float64) if keep_exact else None
+    if keep_exact and n_ctx:
+        exact[:, :, :n_ctx] = rerope(cached_kv, chunks, m.theta, "f64")
+
+    def store_rows(layer, rows, k_new, v_new):
+        out_kv[layer, 0, rows] = round_store(k_new, store)
+        out_kv[layer, 1, rows] = round_store(v_new, store)
+        if keep_exact:
+            exact[layer, 0, rows], exact[layer, 1, rows] = k_new, v_new
+
+    h = m.embed_rows(tokens)
+    # layer 0: every row, context K/V reused
+    W = m.layer(0)
+    q = m.q_only(W, h, pos)
+    _, kq, vq = m.qkv(W, h[n_ctx:], pos[n_ctx:])
+    store_rows(0, query, kq, vq)
+    o = attention(q, out_kv[0, 0].astype(np.float64), out_kv[0, 1].astype(np.float64), pos, pos, Hkv)
+    h = m.finish(W, h, o)
+    del W
+
+    sets, devs = {}, {}
+    # check layer 1: every row compared, S_1 chosen among all context rows
+    W = m.layer(1)
+    q, k_new, v_new = m.qkv(W, h, pos)
+    devs[1] = deviation(k_new[:n_ctx], v_new[:n_ctx], out_kv[1, 0, :n_ctx].astype(np.float64),
+                        out_kv[1, 1, :n_ctx].astype(np.float64))
+    sets[1] = np.sort(np.asarray(selected[1], np.int64)) if 1 in selected else select_hkvd(devs[1], counts[0])
+    assert len(sets[1]) == counts[0]
+    A = np.concatenate([sets[1], query])
+    store_rows(1, A, k_new[A], v_new[A])
+    o = attention(q[A], out_kv[1, 0].astype(np.float64), out_kv[1, 1].astype(np.float64), A, pos, Hkv)
+    hA = m.finish(W, h[A], o)
+    del W, h, q, k_new, v_new
+
+    for layer in range(2, L):
+        W = m.layer(layer)
+        cand = sets[layer - 1]
+        q, k_a, v_a = m.qkv(W, hA, A)          # fresh Q/K/V of S_{l-1} and the query
+        k_prev, k_cur = counts[layer - 2], counts[layer - 1]
+        if k_cur < k_prev:
+            devs[layer] = deviation(k_a[:k_prev], v_a[:k_prev], out_kv[layer, 0, cand].astype(np.float64),
+                                    out_kv[layer, 1, cand].astype(np.float64))
+            if layer in selected:               # positions given: their indices among the candidates
+                keep = np.searchsorted(cand, np.sort(np.asarray(selected[layer], np.int64)))
+                assert len(keep) == k_cur and np.array_equal(cand[keep], np.sort(selected[layer]))
+            else:
+                keep = select_hkvd(devs[layer], k_cur)
+            sets[layer] = cand[keep]
+        else:
+            keep = np.arange(k_prev)
+            sets[layer] = cand
+        local = np.concatenate([keep, np.arange(k_prev, k_prev + (N - n_ctx))])
+        A = A[local]
+        store_rows(layer, A, k_a[local], v_a[local])     # R10: the kept rows' fresh K/V, before attention
+        o = attention(q[local], out_kv[layer, 0].astype(np.float64), out_kv[layer, 1].astype(np.float64), A,
+                      pos, Hkv)
+        hA = m.finish(W, hA[local], o)
+        del W
+
+    logits = m.logits(hA[-1])
+    return dict(out_kv=out_kv, out_kv_exact=exact, logits=logits, sets=sets, devs=devs, counts=counts, rows=A)

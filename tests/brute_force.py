@@ -142,3 +142,74 @@ def top_k_by_sorting(dev, k):
     """Largest k by a full sort on (-dev, index); returned ascending."""
     order = sorted(range(len(dev)), key=lambda j: (-float(dev[j]), j))
     return sorted(order[:k])
+
+
+def _layer_row(W, h, pos, R, Hq, Hkv, hd, eps):
+    """One row's q (list of Hq vectors), k, v ([Hkv][hd]) at position pos, explicit per head."""
+    x = _norm(h, W["attn_norm"], eps)
+    Rm = R(pos)
+    q = [Rm @ (W["wq"][i * hd:(i + 1) * hd] @ x) for i in range(Hq)]
+    k = np.stack([Rm @ (W["wk"][i * hd:(i + 1) * hd] @ x) for i in range(Hkv)])
+    v = np.stack([W["wv"][i * hd:(i + 1) * hd] @ x for i in range(Hkv)])
+    return q, k, v
+
+
+def _attend_row(q, kv_layer, pos, Hq, Hkv, hd):
+    """Softmax attention of one row's heads over every key row at position <= pos."""
+    group = Hq // Hkv
+    o = []
+    for i in range(Hq):
+        g = i // group
+        s = [float(np.dot(q[i], kv_layer[0][j][g])) / math.sqrt(hd) for j in range(pos + 1)]
+        mx = max(s)
+        e = [math.exp(sj - mx) for sj in s]
+        z = sum(e)
+        o.append(sum((e[j] / z) * kv_layer[1][j][g] for j in range(pos + 1)))
+    return np.concatenate(o)
+
+
+def selective_blend(cfg, weights, tokens, placed_kv, n_ctx, counts):
+    """Blend with a per-layer shrinking recomputed set, one row at a time (micro inputs only).
+
+    placed_kv: the chunk caches after placement, [L][2][n_ctx][Hkv][hd].  counts: k_l for layers
+    1..L-1, non-increasing.  Layer 0 updates every row's hidden state and stores fresh K/V for the
+    query rows only; at layer l >= 1 the rows holding an updated hidden state get fresh K/V, and when
+    k_l is below the number of such context rows, each one's ||K_new - K_pre||^2 + ||V_new - V_pre||^2
+    against the placed cache ranks them (ties to the lower row); the k_l largest and the query rows
+    have their fresh K/V stored, attend, and carry their hidden state on.
+    Returns (kv [L][2][N][Hkv][hd], logits of the last row, {layer: kept context rows})."""
+    dec = SequentialDecoder(cfg, weights)
+    L, Hq, Hkv, hd, eps = dec.L, dec.Hq, dec.Hkv, dec.hd, dec.eps
+    N = len(tokens)
+    kv = np.zeros((L, 2, N, Hkv, hd))
+    kv[:, :, :n_ctx] = placed_kv
+    h = {j: dec.E[int(tokens[j])].copy() for j in range(N)}
+    live = list(range(N))
+    kept = {}
+    for li, W in enumerate(dec.layers):
+        fresh = {j: _layer_row(W, h[j], j, dec.R, Hq, Hkv, hd, eps) for j in live}
+        ctx_live = [j for j in live if j < n_ctx]
+        if li == 0:
+            keep = ctx_live
+            store = [j for j in live if j >= n_ctx]
+        else:
+            k_l = counts[li - 1]
+            if k_l < len(ctx_live):
+                dev = {}
+                for j in ctx_live:
+                    dk = fresh[j][1] - kv[li, 0, j]
+                    dv = fresh[j][2] - kv[li, 1, j]
+                    dev[j] = float(np.sum(dk * dk) + np.sum(dv * dv))
+                keep = sorted(sorted(ctx_live, key=lambda j: (-dev[j], j))[:k_l])
+            else:
+                keep = ctx_live
+            kept[li] = list(keep)
+            store = keep + [j for j in live if j >= n_ctx]
+        for j in store:
+            kv[li, 0, j], kv[li, 1, j] = fresh[j][1], fresh[j][2]
+        live = keep + [j for j in live if j >= n_ctx]
+        for j in live:
+            hj = h[j] + W["wo"] @ _attend_row(fresh[j][0], kv[li], j, Hq, Hkv, hd)
+            x = _norm(hj, W["mlp_norm"], eps)
+            h[j] = hj + W["w_down"] @ (_sigmoid_gate(W["w_gate"] @ x) * (W["w_up"] @ x))
+    return kv, dec.logits(h[N - 1]), kept

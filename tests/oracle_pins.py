@@ -245,3 +245,83 @@ def check_deviation_rows(ob):
 
 
 ALL_CHECKS.append(check_deviation_rows)
+
+
+# ------------------------------------------------------------------------------------------------
+# gradual filtering (Figure 9): a 5-layer micro model so that the set can shrink more than once
+# ------------------------------------------------------------------------------------------------
+MICRO5 = workload.ModelShape(n_layers=5, d_model=64, n_heads=4, n_kv_heads=2, head_dim=16, ffn_hidden=96,
+                             vocab=101, rope_theta=1e4, dtype="f32")
+MICRO5_CFG = MICRO5.as_dict()
+# ratios of layers 1..4 over 21 context rows: k = 13, 10, 10, 5 (layer 3 keeps its set); the first
+# chunk's 8 rows are a true prefix (zero deviation), so k_1 = 13 takes exactly the other rows
+GRADUAL_RATIOS = (0.6, 0.45, 0.45, 0.2)
+
+
+def micro5_weights():
+    if "w5" not in _cache:
+        _cache["w5"] = workload.make_weights(MICRO5, seed=13, std=0.1)
+    return _cache["w5"]
+
+
+def micro5_caches():
+    if "caches5" not in _cache:
+        chunk_tokens, _, _, _ = micro_request()
+        parts = [bf.full_prefill(MICRO5_CFG, micro5_weights(), t)[0] for t in chunk_tokens]
+        _cache["caches5"] = np.concatenate(parts, axis=2)
+    return _cache["caches5"]
+
+
+def check_gradual_vs_brute_force(ob):
+    """The gradual-filtering blend against a row-by-row selective decoder written from the page's
+    description of the funnel: K/V of every layer, logits, and each layer's kept rows."""
+    _, chunks, _, toks = micro_request()
+    got = ob.blend_gradual(MICRO5_CFG, micro5_weights(), toks, micro5_caches(), chunks, GRADUAL_RATIOS, "f64")
+    placed = bf.place_chunk_caches(MICRO5_CFG, micro5_caches(), chunks)
+    n_ctx = placed.shape[2]
+    counts = [int(np.ceil(r * n_ctx - 1e-9)) for r in GRADUAL_RATIOS]
+    assert counts == [13, 10, 10, 5] and list(got["counts"]) == counts
+    kv, logits, kept = bf.selective_blend(MICRO5_CFG, micro5_weights(), toks, placed, n_ctx, counts)
+    for layer in range(1, MICRO5.n_layers):
+        assert list(got["sets"][layer]) == kept[layer], f"kept rows of layer {layer}"
+    _close(got["out_kv"], kv, 1e-10, "gradual K/V")
+    _close(got["logits"], logits, 1e-10, "gradual logits")
+
+
+def check_gradual_sets_nested(ob):
+    """S_{l+1} is a subset of S_l with k_l = ceil(r_l n_ctx) rows; only shrinking layers compare."""
+    _, chunks, _, toks = micro_request()
+    got = ob.blend_gradual(MICRO5_CFG, micro5_weights(), toks, micro5_caches(), chunks, GRADUAL_RATIOS, "f64")
+    sets = got["sets"]
+    for layer in range(1, MICRO5.n_layers):
+        assert len(sets[layer]) == got["counts"][layer - 1]
+        assert np.all(np.diff(sets[layer]) > 0)
+        if layer > 1:
+            assert set(sets[layer]) <= set(sets[layer - 1]), f"S_{layer} not within S_{layer - 1}"
+    assert sorted(got["devs"]) == [1, 2, 4], "deviation compared at the check layer and shrinking layers only"
+    # a shrinking layer ranks its candidates by their own deviation at that layer
+    for layer in (2, 4):
+        cand = sets[layer - 1]
+        order = bf.top_k_by_sorting(got["devs"][layer], len(sets[layer]))
+        assert list(cand[order]) == list(sets[layer])
+    # a schedule whose counts grow is rejected
+    try:
+        ob.blend_gradual(MICRO5_CFG, micro5_weights(), toks, micro5_caches(), chunks, (0.3, 0.5, 0.5, 0.5), "f64")
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("growing schedule accepted")
+
+
+def check_gradual_constant_is_blend(ob):
+    """A constant schedule never shrinks the set: the blend with one selection at the check layer."""
+    _, chunks, _, toks = micro_request()
+    for r in (0.0, 0.4, 1.0):
+        one = ob.blend(MICRO_CFG, micro_weights(), toks, brute_caches(), chunks, r, "f64")
+        grad = ob.blend_gradual(MICRO_CFG, micro_weights(), toks, brute_caches(), chunks, (r, r), "f64")
+        _close(grad["out_kv"], one["out_kv"], 1e-12, f"constant schedule K/V (r={r})")
+        _close(grad["logits"], one["logits"], 1e-12, f"constant schedule logits (r={r})")
+        assert list(grad["sets"][1]) == list(one["selected"]) == list(grad["sets"][2])
+
+
+ALL_CHECKS += [check_gradual_vs_brute_force, check_gradual_sets_nested, check_gradual_constant_is_blend]

@@ -11,6 +11,7 @@ import oracle_pins as pins
 _orig_rope, _orig_attention, _orig_rmsnorm = ob.rope, ob.attention, ob.rmsnorm
 _orig_dev, _orig_sel, _orig_freqs, _orig_silu = ob.deviation, ob.select_hkvd, ob.rope_freqs, ob.silu
 _orig_rerope, _orig_round = ob.rerope, ob.round_bf16
+_orig_counts = ob.gradual_counts
 
 
 def rope_sign_flipped(x, pos, theta):
@@ -86,6 +87,16 @@ def round_truncates(x):
     return np.ldexp(np.trunc(np.ldexp(m, 8)), e - 8)
 
 
+def gradual_counts_floor(n_ctx, ratios):
+    return [int(np.floor(float(r) * n_ctx)) for r in ratios]
+
+
+def gradual_counts_first_only(n_ctx, ratios):
+    """The set chosen at the check layer kept to the end (no shrinking)."""
+    ks = _orig_counts(n_ctx, ratios)
+    return [ks[0]] * len(ks)
+
+
 MUTATIONS = [
     ("rope", rope_sign_flipped), ("rope_freqs", rope_freq_halved), ("rope", rope_half_split),
     ("attention", attention_gqa_modulo), ("attention", attention_no_scale), ("attention", attention_strict_causal),
@@ -93,6 +104,7 @@ MUTATIONS = [
     ("deviation", deviation_k_only), ("deviation", deviation_unsquared),
     ("select_hkvd", select_ties_high), ("select_hkvd", select_smallest),
     ("rerope", rerope_wrong_direction), ("round_bf16", round_truncates),
+    ("gradual_counts", gradual_counts_floor), ("gradual_counts", gradual_counts_first_only),
 ]
 
 
