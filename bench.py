@@ -218,6 +218,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama8b-3k", choices=sorted(workload.WORKLOADS))
     ap.add_argument("--ratio", type=float, default=None)
+    ap.add_argument("--gradual", action="store_true",
+                    help="gradual filtering: 2r at the check layer, shrinking to r over the next 4 layers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-profile", action="store_true")
@@ -272,16 +274,26 @@ def main():
     out_kv = model.kv_buffer(n)
     logits = torch.empty(shape.vocab, dtype=torch.float32, device=dev)
     k = cb.cb_selected_count(spec.n_ctx, ratio)
-    sel = torch.empty(max(k, 1), dtype=torch.int32, device=dev)
+    schedule = workload.funnel_ratios(shape.n_layers, ratio) if args.gradual else None
+    n_sel = k
+    if schedule:
+        counts = [cb.cb_selected_count(spec.n_ctx, r) for r in schedule]
+        n_sel = counts[0] + sum(b for a, b in zip(counts, counts[1:]) if b < a)
+    sel = torch.empty(max(n_sel, 1), dtype=torch.int32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # > L2 (129 MB)
     torch.cuda.synchronize()
     setup_s = time.perf_counter() - t_setup
 
     stream = torch.cuda.Stream(dev)
 
+    def blend_call(tok, cache, st=False):
+        if schedule:
+            return cb.cb_blend_gradual(model.handle, tok, n, cache, req.chunks, schedule, out_kv, logits, sel, None,
+                                       stream, stats=st)
+        return cb.cb_blend(model.handle, tok, n, cache, req.chunks, ratio, out_kv, logits, sel, None, stream, stats=st)
+
     def step():
-        return cb.cb_blend(model.handle, tokens, n, cached, req.chunks, ratio, out_kv, logits, sel, None, stream,
-                           stats=True)
+        return blend_call(tokens, cached, True)
 
     st = None
     with torch.cuda.stream(stream):
@@ -382,7 +394,7 @@ def main():
         def e2e_step():
             d_tokens.copy_(h_tokens, non_blocking=True)
             d_cached.copy_(h_cached, non_blocking=True)
-            cb.cb_blend(model.handle, d_tokens, n, d_cached, req.chunks, ratio, out_kv, logits, sel, None, stream)
+            blend_call(d_tokens, d_cached)
             h_out.copy_(out_kv, non_blocking=True)
             h_logits.copy_(logits, non_blocking=True)
 
@@ -405,7 +417,7 @@ def main():
 
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----------------------------------------------
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not schedule:
         dt, scale, desc = oracle_sample(spec, seed, ratio)
         cpu = {"value": spec.n_ctx / (dt * scale), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                "sample": desc, "sample_seconds": dt}
@@ -421,6 +433,8 @@ def main():
                            "n_ctx": spec.n_ctx, "n_query": spec.n_query, "n_chunks": spec.n_chunks,
                            "chunk_len": spec.chunk_len, "ratio": ratio, "k": k, "recomputed_rows": k + spec.n_query,
                            "seed": seed, "parallelism": "replicas" if ws > 1 else "single",
+                           "schedule": ("gradual filtering, per-layer ratios " + ",".join(f"{r:.4g}" for r in schedule))
+                           if schedule else "one selection at the check layer",
                            "l2": "inputs exceed L2 (16 GB weights, 384 MiB caches) and a 256 MiB buffer is "
                                  "rewritten between steps outside the timed events",
                            "timing": ("CUDA events around each step on the launching stream, summed over the steps; "

@@ -5,8 +5,8 @@ declared in ``include/cacheblend.h``.  PyTorch is used for device memory and str
 no fallback: if ``libcacheblend.so`` is missing or cannot be loaded, every call raises.
 
 Entry points (same names as the C ABI): ``cb_model_create``, ``cb_model_destroy``,
-``cb_rerope``, ``cb_blend``, ``cb_selected_count``, ``cb_last_error``; ``BlendModel`` bundles a
-handle with the device tensors it borrows.
+``cb_rerope``, ``cb_blend``, ``cb_blend_gradual``, ``cb_selected_count``, ``cb_last_error``;
+``BlendModel`` bundles a handle with the device tensors it borrows.
 """
 from __future__ import annotations
 
@@ -22,8 +22,9 @@ CB_OK, CB_ERR_INVALID_ARG, CB_ERR_UNSUPPORTED, CB_ERR_OOM, CB_ERR_CUDA, CB_ERR_I
 CB_F32, CB_BF16 = 0, 1
 CB_PREC_SPLIT, CB_PREC_BF16 = 0, 1
 CB_MAX_CHUNKS = 1024
-EXPORTED = ("cb_model_create", "cb_model_destroy", "cb_rerope", "cb_blend", "cb_selected_count", "cb_last_error",
-            "cb_profile_enable", "cb_profile_read", "cb_model_status", "cb_rerope_static", "cb_model_diag")
+EXPORTED = ("cb_model_create", "cb_model_destroy", "cb_rerope", "cb_blend", "cb_blend_gradual", "cb_selected_count",
+            "cb_last_error", "cb_profile_enable", "cb_profile_read", "cb_model_status", "cb_rerope_static",
+            "cb_model_diag")
 CB_STATIC_MAX_CHUNKS = 256
 CB_STATUS_BAD_TOKEN, CB_STATUS_WAIT_TIMEOUT, CB_STATUS_BAD_ROW = 1, 2, 4
 
@@ -92,6 +93,9 @@ def lib() -> ctypes.CDLL:
         L.cb_blend.restype = ctypes.c_int
         L.cb_blend.argtypes = [vp, vp, i32, vp, ctypes.POINTER(CbChunk), i32, ctypes.c_double, vp, vp, vp, vp,
                                ctypes.POINTER(CbStats), vp]
+        L.cb_blend_gradual.restype = ctypes.c_int
+        L.cb_blend_gradual.argtypes = [vp, vp, i32, vp, ctypes.POINTER(CbChunk), i32, ctypes.POINTER(ctypes.c_double),
+                                       i32, vp, vp, vp, vp, ctypes.POINTER(CbStats), vp]
         L.cb_selected_count.restype = i32
         L.cb_selected_count.argtypes = [i32, ctypes.c_double]
         L.cb_profile_enable.restype = ctypes.c_int
@@ -191,6 +195,19 @@ def cb_blend(handle: int, tokens, n_tokens: int, cached_kv, chunks, ratio: float
     return None
 
 
+def cb_blend_gradual(handle: int, tokens, n_tokens: int, cached_kv, chunks, ratios, out_kv, out_logits,
+                     out_selected=None, out_dev=None, stream=None, stats: bool = False):
+    """Gradual filtering: ratios[l - 1] is the ratio of layer l (n_layers - 1 entries, non-increasing counts)."""
+    st = CbStats()
+    r = (ctypes.c_double * max(1, len(ratios)))(*[float(x) for x in ratios])
+    _check(lib().cb_blend_gradual(handle, _ptr(tokens), int(n_tokens), _ptr(cached_kv), _chunks(chunks), len(chunks),
+                                  r, len(ratios), _ptr(out_kv), _ptr(out_logits), _ptr(out_selected), _ptr(out_dev),
+                                  ctypes.byref(st) if stats else None, _stream(stream)))
+    if stats:
+        return {f: getattr(st, f) for f, _ in CbStats._fields_}
+    return None
+
+
 def cb_model_status(handle: int, clear: bool = False) -> int:
     """Device status bits (CB_STATUS_*) recorded by the kernels; synchronises."""
     v = ctypes.c_uint32()
@@ -281,6 +298,40 @@ class BlendModel:
         out = dict(out_kv=out_kv, logits=logits, selected=sel[:k], k=k)
         if want_dev:
             out["dev"] = dev[:n_ctx]
+        if stats:
+            out["stats"] = st
+        return out
+
+    def blend_gradual(self, tokens, cached_kv, chunks, ratios, out_kv=None, stream=None, want_dev=False,
+                      stats=False):
+        """Run cb_blend_gradual; returns dict(out_kv, logits, counts [k_1..k_{L-1}], sets {layer: positions} for
+        the check layer and every shrinking layer, devs {layer: deviations}?, stats?).  The sets and
+        deviations are device tensors (asynchronous on `stream`)."""
+        import torch
+        n = int(tokens.shape[0])
+        n_ctx = sum(c[2] for c in chunks)
+        counts = [cb_selected_count(n_ctx, r) for r in ratios]
+        check = [1] + [l for l in range(2, len(ratios) + 1) if counts[l - 1] < counts[l - 2]]
+        n_sel = sum(counts[l - 1] for l in check)
+        n_dev = n_ctx + sum(counts[l - 2] for l in check[1:])
+        if out_kv is None:
+            out_kv = self.kv_buffer(n)
+        logits = torch.empty(self.shape["vocab"], dtype=torch.float32, device=self.device)
+        sel = torch.empty(max(n_sel, 1), dtype=torch.int32, device=self.device)
+        dev = torch.empty(max(n_dev, 1), dtype=torch.float32, device=self.device) if want_dev else None
+        st = cb_blend_gradual(self.handle, tokens, n, cached_kv, chunks, ratios, out_kv, logits,
+                              sel if n_sel > 0 else None, dev, stream, stats)
+        sets, devs, at, dat = {}, {}, 0, 0
+        for i, l in enumerate(check):
+            sets[l] = sel[at:at + counts[l - 1]]
+            at += counts[l - 1]
+            if want_dev:
+                nd = n_ctx if i == 0 else counts[l - 2]
+                devs[l] = dev[dat:dat + nd]
+                dat += nd
+        out = dict(out_kv=out_kv, logits=logits, counts=counts, sets=sets)
+        if want_dev:
+            out["devs"] = devs
         if stats:
             out["stats"] = st
         return out

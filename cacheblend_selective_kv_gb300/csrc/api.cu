@@ -38,7 +38,7 @@ cb_status fail(cb_status code, const char* fmt, ...) {
 size_t act_size(const Model& m) { return m.bf16 ? 2 : 4; }
 
 void free_ws(Model& m) {
-    void* ptrs[] = {m.h, m.hA, m.x, m.xA, m.q, m.attn, m.act, m.kf, m.vf, m.dev, m.rows, m.iota,
+    void* ptrs[] = {m.h, m.hA, m.x, m.xA, m.q, m.attn, m.act, m.kf, m.vf, m.dev, m.rows, m.rows2, m.sel_local, m.iota,
                     m.rope, m.inv_freq, m.delta_cs, m.chunk_dst, m.chunk_delta, m.xfinal, m.status,
                     m.x_lo, m.xA_lo, m.attn_lo, m.act_lo, m.q_lo, m.part_o, m.part_ml};
     for (void* p : ptrs)
@@ -118,7 +118,8 @@ cb_status cb_model_create(const cb_config* cfg, const cb_weights* w, cb_model** 
     m->w_up.assign(w->w_up, w->w_up + c.n_layers);
     m->w_down.assign(w->w_down, w->w_down + c.n_layers);
     m->h = m->hA = nullptr; m->x = m->xA = m->q = m->attn = m->act = nullptr;
-    m->kf = m->vf = m->dev = nullptr; m->rows = m->iota = nullptr; m->rope = nullptr; m->inv_freq = nullptr;
+    m->kf = m->vf = m->dev = nullptr; m->rows = m->rows2 = m->sel_local = m->iota = nullptr; m->rope = nullptr;
+    m->inv_freq = nullptr;
     m->delta_cs = nullptr; m->chunk_dst = m->chunk_delta = nullptr; m->xfinal = nullptr; m->status = nullptr;
     m->tc = nullptr;
 
@@ -130,6 +131,7 @@ cb_status cb_model_create(const cb_config* cfg, const cb_weights* w, cb_model** 
         {(void**)&m->h, T * d * 4}, {(void**)&m->hA, T * d * 4}, {&m->x, T * d * as}, {&m->xA, T * d * as},
         {&m->q, T * nq * as}, {&m->attn, T * nq * as}, {&m->act, T * F * as}, {(void**)&m->kf, T * nkv * 4},
         {(void**)&m->vf, T * nkv * 4}, {(void**)&m->dev, T * 4}, {(void**)&m->rows, T * 4},
+        {(void**)&m->rows2, T * 4}, {(void**)&m->sel_local, T * 4},
         {(void**)&m->iota, T * 4}, {(void**)&m->rope, T * half * sizeof(float2)},
         {(void**)&m->inv_freq, half * sizeof(double)}, {(void**)&m->delta_cs, mc * half * sizeof(float2)},
         {(void**)&m->chunk_dst, mc * 4}, {(void**)&m->chunk_delta, mc * 4}, {(void**)&m->xfinal, d * 4},
@@ -229,7 +231,7 @@ cb_status check_chunks(const cb_chunk* chunks, int32_t n_chunks, int max_chunks,
 
 const char* const kClassName[K_NCLASS] = {"rerope", "embed", "rmsnorm", "gemm_q", "gemm_kv", "gemm_qkv", "gemm_o",
                                          "gemm_gateup", "gemm_down", "attention", "deviation", "topk",
-                                         "gather_scatter", "logits", "delta_table"};
+                                         "gather_scatter", "logits", "delta_table", "refilter"};
 
 // Enqueues launches on one stream; counts them and, when profiling is on, brackets each with events.
 struct Sched {
@@ -346,38 +348,24 @@ cb_status cb_rerope(cb_model* m, void* kv, int64_t n_rows, const cb_chunk* chunk
     return CB_OK;
 }
 
-cb_status cb_blend(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const void* cached_kv,
-                   const cb_chunk* chunks, int32_t n_chunks, double ratio, void* out_kv, float* out_logits,
-                   int32_t* out_selected, float* out_dev, cb_stats* stats, void* stream) {
-    g_err[0] = 0;
-    if (!mp) return fail(CB_ERR_INVALID_ARG, "cb_blend: null model");
-    Model& m = *mp;
+}  // extern "C"
+
+namespace {
+
+// One blend.  ks[l] (l = 1..L-1) is the number of context rows whose hidden state leaves layer l:
+// constant for the blend with one selection at the check layer, non-increasing for gradual filtering
+// (a layer with ks[l] < ks[l-1] compares its candidates again and keeps the top ks[l]).
+cb_status blend_impl(Model& m, const int32_t* tokens, int32_t n_tokens, const void* cached_kv, const ChunkTable& t,
+                     int n_chunks, int n_ctx, const std::vector<int>& ks, void* out_kv, float* out_logits,
+                     int32_t* out_selected, float* out_dev, cb_stats* stats, cudaStream_t s) {
     const cb_config& c = m.cfg;
-    if (!tokens || !out_kv || !out_logits) return fail(CB_ERR_INVALID_ARG, "cb_blend: null tokens, out_kv or out_logits");
-    if (n_tokens <= 0 || n_tokens > c.max_tokens)
-        return fail(CB_ERR_INVALID_ARG, "n_tokens %d outside (0, max_tokens=%d]", n_tokens, c.max_tokens);
-    if (!(ratio >= 0.0 && ratio <= 1.0)) return fail(CB_ERR_INVALID_ARG, "ratio must be in [0, 1]");
-    ChunkTable t;
-    int n_ctx = 0;
-    cb_status st = check_chunks(chunks, n_chunks, c.max_chunks, n_ctx, t);
-    if (st != CB_OK) return st;
-    if (n_ctx >= n_tokens) return fail(CB_ERR_INVALID_ARG, "need at least one query token after the %d context rows", n_ctx);
-    if (n_chunks > 0 && !cached_kv) return fail(CB_ERR_INVALID_ARG, "cached_kv is NULL but chunks were given");
     const size_t es = act_size(m);
     const int L = c.n_layers, d = c.d_model, nq = c.n_heads * c.head_dim, nkv = c.n_kv_heads * c.head_dim;
     const int F = c.ffn_hidden, N = n_tokens, Q = N - n_ctx;
     const bool inplace = n_chunks > 0 && cached_kv == out_kv;
-    if (n_chunks > 0 && !inplace) {
-        // the two buffers may not overlap unless identical
-        const char* a = (const char*)cached_kv;
-        const char* b = (const char*)out_kv;
-        const size_t abytes = (size_t)L * 2 * n_ctx * nkv * es, bbytes = (size_t)L * 2 * N * nkv * es;
-        if (a < b + bbytes && b < a + abytes) return fail(CB_ERR_INVALID_ARG, "cached_kv and out_kv overlap");
-    }
-    const int k = cb_selected_count(n_ctx, ratio);
+    const int k = ks[1];
     const int M = k + Q;
 
-    cudaStream_t s = (cudaStream_t)stream;
     Sched S{m, s};
     char* kvb = (char*)out_kv;
     auto layer_kv = [&](int l) { return (void*)(kvb + (size_t)l * 2 * N * nkv * es); };
@@ -387,7 +375,9 @@ cb_status cb_blend(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const 
     auto attn_flops = [&](double keys) { return 4.0 * hd * Hq * keys; };
     // causal key counts of the recomputed rows (selected rows at the mean context position)
     const double keys0 = (double)N * (N + 1) / 2.0;
-    const double keysA = (double)Q * (n_ctx + 1) + (double)Q * (Q - 1) / 2.0 + (double)k * (n_ctx + 1) / 2.0;
+    auto keys_of = [&](int kl) {
+        return (double)Q * (n_ctx + 1) + (double)Q * (Q - 1) / 2.0 + (double)kl * (n_ctx + 1) / 2.0;
+    };
 
     // re-RoPE placement of the chunk caches (section "位置恢复、KV 存储与加载流水线")
     if (n_chunks > 0) {
@@ -451,7 +441,7 @@ cb_status cb_blend(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const 
         S.gemm(K_GEMM_KV, XBUF_X, 0, N, d, wsel(m, 1, WSEL_KV), 2 * nkv, ekv);
         if (n_ctx > 0)
             S.k(K_DEVIATION, 0, (double)n_ctx * 2 * nkv * (4 + es),
-                [&] { return launch_deviation(m, m.kf, m.vf, layer_kv(1), N, n_ctx, devp, s); });
+                [&] { return launch_deviation(m, m.kf, m.vf, layer_kv(1), N, nullptr, n_ctx, devp, s); });
         S.k(K_TOPK, 0, (double)n_ctx * 4, [&] { return launch_topk(m, devp, n_ctx, k, Q, m.rows, out_selected, s); });
         S.k(K_GATHER, 0, (double)M * (8.0 * d + 2.0 * d * es + 2.0 * nkv * (4 + es)),
             [&] { return launch_gather_scatter(m, m.rows, M, m.h, m.hA, m.x, m.xA, m.x_lo, m.xA_lo, m.kf, m.vf,
@@ -464,34 +454,86 @@ cb_status cb_blend(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const 
     }
 
     // ---- layers >= 1: attention of the recomputed rows over the blended K/V, O, MLP ------------
+    // The recomputed rows' state lives in one of two buffer sets; a shrinking layer (gradual
+    // filtering) compacts the kept rows into the other set.
+    float* hc = m.hA;
+    int xc = XBUF_XA;
+    int* rows_c = m.rows;
+    int k_prev = k;
+    size_t dev_at = out_dev ? (size_t)n_ctx : 0;     // out_dev: later shrinking layers follow the check layer
+    size_t sel_at = (size_t)k;                       // out_selected: likewise
+    double attn_total = attn_flops(keys0);
     for (int l = 1; l < L; ++l) {
-        if (l >= 2) {
-            norm(m.hA, m.attn_norm[l], m.xA, M);
-            EpiParams e = epi_base(m, EPI_QKV, M);
+        const int kl = ks[l];
+        const int Mp = k_prev + Q, Ml = kl + Q;
+        void* xcp = xc == XBUF_X ? m.x : m.xA;
+        if (l >= 2 && kl < k_prev) {
+            // shrinking layer (Figure 9): fresh K/V of the candidates, their deviation against the
+            // re-RoPE'd cache of this layer, the top kl of them, compaction, then Q of the kept rows
+            norm(hc, m.attn_norm[l], xcp, Mp);
+            EpiParams ekv = epi_base(m, EPI_QKV, Mp);
+            ekv.qkv_base = nq;
+            ekv.kv_fresh = 1;
+            ekv.pos = rows_c;
+            ekv.k_dst = m.kf;
+            ekv.v_dst = m.vf;
+            S.gemm(K_GEMM_KV, xc, 0, Mp, d, wsel(m, l, WSEL_KV), 2 * nkv, ekv);
+            float* devl = (out_dev ? out_dev : m.dev) + dev_at;
+            S.k(K_DEVIATION, 0, (double)k_prev * 2 * nkv * (4 + es),
+                [&] { return launch_deviation(m, m.kf, m.vf, layer_kv(l), N, rows_c, k_prev, devl, s); });
+            S.k(K_TOPK, 0, (double)k_prev * 4,
+                [&] { return launch_topk(m, devl, k_prev, kl, Q, m.sel_local, nullptr, s); });
+            float* hn = hc == m.hA ? m.h : m.hA;
+            const int xn = xc == XBUF_XA ? XBUF_X : XBUF_XA;
+            void* xnp = xn == XBUF_X ? m.x : m.xA;
+            int* rows_n = rows_c == m.rows ? m.rows2 : m.rows;
+            int* sel_out = out_selected ? out_selected + sel_at : nullptr;
+            S.k(K_REFILTER, 0, (double)Ml * (8.0 * d + 2.0 * d * es * (m.split ? 2 : 1) + 2.0 * nkv * (4 + es)),
+                [&] { return launch_refilter(m, m.sel_local, rows_c, rows_n, Ml, kl, sel_out, hc, hn, xcp, xnp,
+                                             m.split ? (xc == XBUF_X ? m.x_lo : m.xA_lo) : nullptr,
+                                             m.split ? (xn == XBUF_X ? m.x_lo : m.xA_lo) : nullptr, m.kf, m.vf,
+                                             layer_kv(l), N, s); });
+            EpiParams e = epi_base(m, EPI_QKV, Ml);
             e.qkv_base = 0;
-            e.pos = m.rows;
+            e.pos = rows_n;
+            e.q_out = m.q;
+            S.gemm(K_GEMM_Q, xn, 0, Ml, d, wsel(m, l, WSEL_Q), nq, e);
+            if (out_dev) dev_at += (size_t)k_prev;
+            sel_at += (size_t)kl;
+            hc = hn;
+            xc = xn;
+            xcp = xnp;
+            rows_c = rows_n;
+        } else if (l >= 2) {
+            norm(hc, m.attn_norm[l], xcp, Ml);
+            EpiParams e = epi_base(m, EPI_QKV, Ml);
+            e.qkv_base = 0;
+            e.pos = rows_c;
             e.q_out = m.q;
             e.k_dst = layer_kv(l);
             e.v_dst = layer_v(l);
-            S.gemm(K_GEMM_QKV, XBUF_XA, 0, M, d, wsel(m, l, WSEL_QKV), nq + 2 * nkv, e);
+            S.gemm(K_GEMM_QKV, xc, 0, Ml, d, wsel(m, l, WSEL_QKV), nq + 2 * nkv, e);
         }
-        attend(l, m.rows, M, keysA);
-        EpiParams er = epi_base(m, EPI_RESID, M);
-        er.h = m.hA;
+        attend(l, rows_c, Ml, keys_of(kl));
+        attn_total += attn_flops(keys_of(kl));
+        EpiParams er = epi_base(m, EPI_RESID, Ml);
+        er.h = hc;
         er.ldh = d;
-        S.gemm(K_GEMM_O, XBUF_ATTN, 0, M, nq, wsel(m, l, WSEL_O), d, er);
-        norm(m.hA, m.mlp_norm[l], m.xA, M);
-        EpiParams eg = epi_base(m, EPI_SWIGLU, M);
+        S.gemm(K_GEMM_O, XBUF_ATTN, 0, Ml, nq, wsel(m, l, WSEL_O), d, er);
+        norm(hc, m.mlp_norm[l], xcp, Ml);
+        EpiParams eg = epi_base(m, EPI_SWIGLU, Ml);
         eg.act = m.act;
         eg.act_lo = m.act_lo;
         eg.ld_act = F;
-        S.gemm(K_GEMM_GATEUP, XBUF_XA, 0, M, d, wsel(m, l, WSEL_GATEUP), F, eg);
-        S.gemm(K_GEMM_DOWN, XBUF_ACT, 0, M, F, wsel(m, l, WSEL_DOWN), d, er);
+        S.gemm(K_GEMM_GATEUP, xc, 0, Ml, d, wsel(m, l, WSEL_GATEUP), F, eg);
+        S.gemm(K_GEMM_DOWN, XBUF_ACT, 0, Ml, F, wsel(m, l, WSEL_DOWN), d, er);
+        k_prev = kl;
     }
 
     // ---- logits of the last row --------------------------------------------------------------
+    const float* h_last = hc + (size_t)(k_prev + Q - 1) * d;
     S.k(K_LOGITS, 2.0 * d * c.vocab, (double)c.vocab * d * es,
-        [&] { return launch_logits(m, m.hA + (size_t)(M - 1) * d, out_logits, s); });
+        [&] { return launch_logits(m, h_last, out_logits, s); });
 
     if (S.err != cudaSuccess) return fail(CB_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(S.err));
     if (stats) {
@@ -502,11 +544,84 @@ cb_status cb_blend(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const 
         stats->kernel_launches = S.launches;
         stats->reserved = 0;
         stats->gemm_flops = S.gemm_flops + 2.0 * d * (double)c.vocab;
-        stats->attn_flops = attn_flops(keys0) + (L - 1) * attn_flops(keysA);
+        stats->attn_flops = attn_total;
+        double scat = 0;
+        for (int l = 1; l < L; ++l) scat += (double)(ks[l] + Q) * 2 * row;
         stats->kv_bytes_moved = (n_chunks ? (inplace ? 2.0 * L * n_ctx * row : 4.0 * L * n_ctx * row) : 0) +
-                                (double)n_ctx * 2 * nkv * (4 + es) + (double)(L - 1) * M * 2 * row;
+                                (double)n_ctx * 2 * nkv * (4 + es) + scat;
     }
     return CB_OK;
+}
+
+// validation shared by cb_blend and cb_blend_gradual; fills the chunk table and n_ctx
+cb_status check_blend(const Model& m, const int32_t* tokens, int32_t n_tokens, const void* cached_kv,
+                      const cb_chunk* chunks, int32_t n_chunks, void* out_kv, float* out_logits, ChunkTable& t,
+                      int& n_ctx) {
+    const cb_config& c = m.cfg;
+    if (!tokens || !out_kv || !out_logits) return fail(CB_ERR_INVALID_ARG, "cb_blend: null tokens, out_kv or out_logits");
+    if (n_tokens <= 0 || n_tokens > c.max_tokens)
+        return fail(CB_ERR_INVALID_ARG, "n_tokens %d outside (0, max_tokens=%d]", n_tokens, c.max_tokens);
+    cb_status st = check_chunks(chunks, n_chunks, c.max_chunks, n_ctx, t);
+    if (st != CB_OK) return st;
+    if (n_ctx >= n_tokens) return fail(CB_ERR_INVALID_ARG, "need at least one query token after the %d context rows", n_ctx);
+    if (n_chunks > 0 && !cached_kv) return fail(CB_ERR_INVALID_ARG, "cached_kv is NULL but chunks were given");
+    if (n_chunks > 0 && cached_kv != out_kv) {
+        // the two buffers may not overlap unless identical
+        const size_t es = act_size(m), nkv = (size_t)c.n_kv_heads * c.head_dim;
+        const char* a = (const char*)cached_kv;
+        const char* b = (const char*)out_kv;
+        const size_t abytes = (size_t)c.n_layers * 2 * n_ctx * nkv * es, bbytes = (size_t)c.n_layers * 2 * n_tokens * nkv * es;
+        if (a < b + bbytes && b < a + abytes) return fail(CB_ERR_INVALID_ARG, "cached_kv and out_kv overlap");
+    }
+    return CB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+cb_status cb_blend(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const void* cached_kv,
+                   const cb_chunk* chunks, int32_t n_chunks, double ratio, void* out_kv, float* out_logits,
+                   int32_t* out_selected, float* out_dev, cb_stats* stats, void* stream) {
+    g_err[0] = 0;
+    if (!mp) return fail(CB_ERR_INVALID_ARG, "cb_blend: null model");
+    Model& m = *mp;
+    if (!(ratio >= 0.0 && ratio <= 1.0)) return fail(CB_ERR_INVALID_ARG, "ratio must be in [0, 1]");
+    ChunkTable t;
+    int n_ctx = 0;
+    cb_status st = check_blend(m, tokens, n_tokens, cached_kv, chunks, n_chunks, out_kv, out_logits, t, n_ctx);
+    if (st != CB_OK) return st;
+    std::vector<int> ks(m.cfg.n_layers, cb_selected_count(n_ctx, ratio));
+    return blend_impl(m, tokens, n_tokens, cached_kv, t, n_chunks, n_ctx, ks, out_kv, out_logits, out_selected,
+                      out_dev, stats, (cudaStream_t)stream);
+}
+
+cb_status cb_blend_gradual(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const void* cached_kv,
+                           const cb_chunk* chunks, int32_t n_chunks, const double* ratios, int32_t n_ratios,
+                           void* out_kv, float* out_logits, int32_t* out_selected, float* out_dev, cb_stats* stats,
+                           void* stream) {
+    g_err[0] = 0;
+    if (!mp) return fail(CB_ERR_INVALID_ARG, "cb_blend_gradual: null model");
+    Model& m = *mp;
+    const int L = m.cfg.n_layers;
+    if (!ratios || n_ratios != L - 1)
+        return fail(CB_ERR_INVALID_ARG, "cb_blend_gradual: need n_layers - 1 = %d ratios (got %d)", L - 1, n_ratios);
+    for (int i = 0; i < n_ratios; ++i)
+        if (!(ratios[i] >= 0.0 && ratios[i] <= 1.0)) return fail(CB_ERR_INVALID_ARG, "ratio of layer %d outside [0, 1]", i + 1);
+    ChunkTable t;
+    int n_ctx = 0;
+    cb_status st = check_blend(m, tokens, n_tokens, cached_kv, chunks, n_chunks, out_kv, out_logits, t, n_ctx);
+    if (st != CB_OK) return st;
+    std::vector<int> ks(L, 0);
+    for (int l = 1; l < L; ++l) {
+        ks[l] = cb_selected_count(n_ctx, ratios[l - 1]);
+        if (l >= 2 && ks[l] > ks[l - 1])
+            return fail(CB_ERR_INVALID_ARG, "layer %d keeps %d rows, more than layer %d's %d: the sets must be nested",
+                        l, ks[l], l - 1, ks[l - 1]);
+    }
+    ks[0] = ks[1];
+    return blend_impl(m, tokens, n_tokens, cached_kv, t, n_chunks, n_ctx, ks, out_kv, out_logits, out_selected,
+                      out_dev, stats, (cudaStream_t)stream);
 }
 
 cb_status cb_model_status(cb_model* m, uint32_t* bits, int32_t clear) {

@@ -99,7 +99,7 @@ struct TcMaps;   // tensor maps of the tensor-core path (defined in gemm_tc.cu)
 
 // kernel classes for the opt-in per-class timing
 enum KClass { K_REROPE, K_EMBED, K_RMSNORM, K_GEMM_Q, K_GEMM_KV, K_GEMM_QKV, K_GEMM_O, K_GEMM_GATEUP, K_GEMM_DOWN,
-              K_ATTENTION, K_DEVIATION, K_TOPK, K_GATHER, K_LOGITS, K_DELTA, K_NCLASS };
+              K_ATTENTION, K_DEVIATION, K_TOPK, K_GATHER, K_LOGITS, K_DELTA, K_REFILTER, K_NCLASS };
 
 struct Profile {
     bool on = false;
@@ -142,6 +142,8 @@ struct Model {
     float* vf;            // [max_tokens][nkv] fresh V at the check layer (fp32)
     float* dev;           // [max_tokens] deviations
     int* rows;            // [max_tokens] recomputed-row positions (selected ascending, then query)
+    int* rows2;           // [max_tokens] the other rows buffer of gradual filtering (sets alternate)
+    int* sel_local;       // [max_tokens] kept rows of a shrinking layer, as indices into the previous set
     int* iota;            // [max_tokens] 0, 1, 2, ...
     float2* rope;         // [max_tokens][hd/2]
     double* inv_freq;     // [hd/2] theta^(-2i/hd)
@@ -175,7 +177,11 @@ cudaError_t launch_embed(const Model& m, const int* tokens, int n, float* h, cud
 cudaError_t launch_rmsnorm(const Model& m, const float* h, const void* g, void* out, void* out_lo, int n,
                            cudaStream_t s);
 cudaError_t launch_deviation(const Model& m, const float* kf, const float* vf, const void* kv_layer, int64_t kv_rows,
-                             int n_ctx, float* dev, cudaStream_t s);
+                             const int* crow, int n_ctx, float* dev, cudaStream_t s);
+cudaError_t launch_refilter(const Model& m, const int* local, const int* rows_old, int* rows_new, int M_new, int k_new,
+                            int* out_sel, const float* h_old, float* h_new, const void* x_old, void* x_new,
+                            const void* xlo_old, void* xlo_new, const float* kf, const float* vf, void* kv_layer,
+                            int64_t kv_rows, cudaStream_t s);
 cudaError_t launch_topk(const Model& m, const float* dev, int n_ctx, int k, int n_query, int* rows, int* out_sel,
                         cudaStream_t s);
 cudaError_t launch_gather_scatter(const Model& m, const int* rows, int M, const float* h, float* hA, const void* x,

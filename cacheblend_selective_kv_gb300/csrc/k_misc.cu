@@ -216,17 +216,21 @@ cudaError_t launch_rmsnorm(const Model& m, const float* h, const void* g, void* 
 }
 
 // ------------------------------------------------------------------------------------------------
-// KV deviation at the check layer (CacheBlend deep-dive page, section "核心思想", Δkv formula):
-// dev[j] = sum over KV heads and dims of (k_new - k_pre)^2 + (v_new - v_pre)^2,
-// with fresh fp32 K/V and the re-RoPE'd stored cache.  One warp per row.
+// KV deviation (CacheBlend deep-dive page, section "核心思想", Δkv formula):
+// dev[r] = sum over KV heads and dims of (k_new - k_pre)^2 + (v_new - v_pre)^2,
+// with fresh fp32 K/V (row r) and the re-RoPE'd stored cache (row crow[r], or r when crow is
+// NULL: the check layer compares every context row in place; a later shrinking layer compares
+// its candidates, whose cache rows are their positions).  One warp per row.
 // ------------------------------------------------------------------------------------------------
 template <typename T>
 __global__ void deviation_kernel(const float* __restrict__ kf, const float* __restrict__ vf,
-                                 const T* __restrict__ kv_layer, int64_t kv_rows, int n_ctx, int W, float* dev) {
+                                 const T* __restrict__ kv_layer, int64_t kv_rows, const int* __restrict__ crow,
+                                 int n_ctx, int W, float* dev) {
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (warp >= n_ctx) return;
-    const T* kc = kv_layer + (int64_t)warp * W;
-    const T* vc = kv_layer + (kv_rows + warp) * (int64_t)W;
+    const int64_t j = crow ? crow[warp] : warp;
+    const T* kc = kv_layer + j * W;
+    const T* vc = kv_layer + (kv_rows + j) * (int64_t)W;
     const float* kn = kf + (int64_t)warp * W;
     const float* vn = vf + (int64_t)warp * W;
     float acc = 0.f;
@@ -246,14 +250,14 @@ __global__ void deviation_kernel(const float* __restrict__ kf, const float* __re
 }
 
 cudaError_t launch_deviation(const Model& m, const float* kf, const float* vf, const void* kv_layer, int64_t kv_rows,
-                             int n_ctx, float* dev, cudaStream_t s) {
+                             const int* crow, int n_ctx, float* dev, cudaStream_t s) {
     if (n_ctx <= 0) return cudaSuccess;
     const int W = m.cfg.n_kv_heads * m.cfg.head_dim;
     const int grid = (n_ctx + 7) / 8;
     if (m.bf16)
-        deviation_kernel<bf16><<<grid, 256, 0, s>>>(kf, vf, (const bf16*)kv_layer, kv_rows, n_ctx, W, dev);
+        deviation_kernel<bf16><<<grid, 256, 0, s>>>(kf, vf, (const bf16*)kv_layer, kv_rows, crow, n_ctx, W, dev);
     else
-        deviation_kernel<float><<<grid, 256, 0, s>>>(kf, vf, (const float*)kv_layer, kv_rows, n_ctx, W, dev);
+        deviation_kernel<float><<<grid, 256, 0, s>>>(kf, vf, (const float*)kv_layer, kv_rows, crow, n_ctx, W, dev);
     return cudaGetLastError();
 }
 
@@ -298,6 +302,64 @@ cudaError_t launch_gather_scatter(const Model& m, const int* rows, int M, const 
     else
         gather_scatter_kernel<float><<<M, 256, 0, s>>>(rows, h, hA, (const float*)x, (float*)xA, nullptr, nullptr, kf,
                                                        vf, (float*)kv_layer, kv_rows, d, W);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------------
+// A shrinking layer of gradual filtering (Figure 9 funnel): the kept rows are local[i] (indices into
+// the previous layer's compact rows; the kept context rows ascending, then the query rows).  Row i of
+// the new compact set takes the hidden state and normalised input of row local[i] (into the other
+// buffer of each pair: compaction in place would race), its position, and its fresh K/V is stored
+// into the blended cache at that position before attention.  out_sel (optional) receives the kept
+// context rows' positions.
+// ------------------------------------------------------------------------------------------------
+template <typename T>
+__global__ void refilter_kernel(const int* __restrict__ local, const int* __restrict__ rows_old, int* __restrict__ rows_new,
+                                int k_new, int* __restrict__ out_sel, const float* __restrict__ h_old, float* __restrict__ h_new,
+                                const T* __restrict__ x_old, T* __restrict__ x_new, const T* __restrict__ xlo_old,
+                                T* __restrict__ xlo_new, const float* __restrict__ kf, const float* __restrict__ vf,
+                                T* kv_layer, int64_t kv_rows, int d, int W) {
+    const int i = blockIdx.x;
+    const int src = local[i];
+    const int r = rows_old[src];
+    if (threadIdx.x == 0) {
+        rows_new[i] = r;
+        if (out_sel && i < k_new) out_sel[i] = r;
+    }
+    for (int e = threadIdx.x * 4; e < d; e += blockDim.x * 4)
+        *reinterpret_cast<float4*>(h_new + (size_t)i * d + e) = *reinterpret_cast<const float4*>(h_old + (size_t)src * d + e);
+    for (int e = threadIdx.x * 8; e < d; e += blockDim.x * 8) {
+        float f[8];
+        Vec8<T>::load(x_old + (size_t)src * d + e, f);
+        Vec8<T>::store(x_new + (size_t)i * d + e, f);
+        if (xlo_old) {
+            Vec8<T>::load(xlo_old + (size_t)src * d + e, f);
+            Vec8<T>::store(xlo_new + (size_t)i * d + e, f);
+        }
+    }
+    for (int e = threadIdx.x * 8; e < W; e += blockDim.x * 8) {
+        float f[8];
+        Vec8<float>::load(kf + (size_t)src * W + e, f);
+        Vec8<T>::store(kv_layer + (int64_t)r * W + e, f);
+        Vec8<float>::load(vf + (size_t)src * W + e, f);
+        Vec8<T>::store(kv_layer + (kv_rows + r) * (int64_t)W + e, f);
+    }
+}
+
+cudaError_t launch_refilter(const Model& m, const int* local, const int* rows_old, int* rows_new, int M_new, int k_new,
+                            int* out_sel, const float* h_old, float* h_new, const void* x_old, void* x_new,
+                            const void* xlo_old, void* xlo_new, const float* kf, const float* vf, void* kv_layer,
+                            int64_t kv_rows, cudaStream_t s) {
+    if (M_new <= 0) return cudaSuccess;
+    const int d = m.cfg.d_model, W = m.cfg.n_kv_heads * m.cfg.head_dim;
+    if (m.bf16)
+        refilter_kernel<bf16><<<M_new, 256, 0, s>>>(local, rows_old, rows_new, k_new, out_sel, h_old, h_new,
+                                                    (const bf16*)x_old, (bf16*)x_new, (const bf16*)xlo_old,
+                                                    (bf16*)xlo_new, kf, vf, (bf16*)kv_layer, kv_rows, d, W);
+    else
+        refilter_kernel<float><<<M_new, 256, 0, s>>>(local, rows_old, rows_new, k_new, out_sel, h_old, h_new,
+                                                     (const float*)x_old, (float*)x_new, nullptr, nullptr, kf, vf,
+                                                     (float*)kv_layer, kv_rows, d, W);
     return cudaGetLastError();
 }
 

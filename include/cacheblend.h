@@ -160,6 +160,27 @@ cb_status cb_blend(cb_model* model, const int32_t* tokens, int32_t n_tokens, con
                    const cb_chunk* chunks, int32_t n_chunks, double ratio, void* out_kv, float* out_logits,
                    int32_t* out_selected, float* out_dev, cb_stats* stats, void* stream);
 
+/* One blend with gradual filtering (section "核心思想", the layer-by-layer funnel of Figure 9): the set
+ * of context rows recomputed shrinks from layer to layer, each set nested in the previous one.
+ *   ratios      host, n_ratios = n_layers - 1 entries: ratios[l - 1] is r_l of layer l, and
+ *               k_l = ceil(r_l * n_ctx - 1e-9) context rows carry an updated hidden state out of layer l.
+ *               The counts must not grow (k_l <= k_{l-1}); equal counts keep the set unchanged.
+ *   Layer 1 is the check layer of cb_blend (every row compared, the top k_1 kept).  A later layer l with
+ *   k_l < k_{l-1} computes fresh K/V for the k_{l-1} candidates (and the query), ranks the candidates by
+ *   their deviation against this layer's re-RoPE'd cache, keeps the top k_l (ties to the lower
+ *   position), stores the kept rows' and the query's fresh K/V, and runs attention, O and MLP for them
+ *   only.  A candidate that drops out keeps its cached K/V from that layer on.
+ *   out_selected device int32 or NULL: the check layer's set (k_1 rows, ascending), followed by the set
+ *                of every shrinking layer in layer order (k_l rows each, ascending).
+ *   out_dev      device float32 or NULL: the check layer's n_ctx deviations, followed by every
+ *                shrinking layer's k_{l-1} candidate deviations (candidates in ascending position).
+ *   All other arguments, the validation and the asynchrony are those of cb_blend; a constant schedule
+ *   gives exactly cb_blend's result.  A growing schedule or n_ratios != n_layers - 1 -> CB_ERR_INVALID_ARG. */
+cb_status cb_blend_gradual(cb_model* model, const int32_t* tokens, int32_t n_tokens, const void* cached_kv,
+                           const cb_chunk* chunks, int32_t n_chunks, const double* ratios, int32_t n_ratios,
+                           void* out_kv, float* out_logits, int32_t* out_selected, float* out_dev, cb_stats* stats,
+                           void* stream);
+
 /* Device status bits recorded by the kernels instead of trapping (cumulative since creation). */
 #define CB_STATUS_BAD_TOKEN    1u  /* a token id outside [0, vocab) was read; its embedding was zeroed */
 #define CB_STATUS_WAIT_TIMEOUT 2u  /* a bounded barrier wait in a tensor-core kernel gave up (~2 s); the
@@ -179,7 +200,7 @@ cb_status cb_model_diag(cb_model* model, uint32_t* words);
  * launch is bracketed by CUDA events recorded on the call's stream (this serialises nothing that was
  * not already serial on that stream, but adds event records between kernels).  Classes: "rerope",
  * "embed", "rmsnorm", "gemm_q", "gemm_kv", "gemm_qkv", "gemm_o", "gemm_gateup", "gemm_down",
- * "attention", "deviation", "topk", "gather_scatter", "logits", "delta_table". */
+ * "attention", "deviation", "topk", "gather_scatter", "logits", "delta_table", "refilter". */
 typedef struct {
     char name[24];
     int32_t launches;        /* launches recorded since the last read */

@@ -11,10 +11,11 @@ library routines for special cases, and the page's printed sizing numbers).
 The selected set at 0 < r < 1 has no printed worked example on the pages; it is
 pinned only through the page's Δkv definition against a brute-force full prefill.
 """
-from .cpu_blend import (attention, blend, chunk_caches, deviation, deviation_rows, prefill, rerope, rmsnorm, rope, rope_freqs,
-                    round_bf16, round_store, select_hkvd, selected_count, silu, to_f64, Model, validate_chunks)
+from .cpu_blend import (attention, blend, blend_gradual, chunk_caches, deviation, deviation_rows, gradual_counts, prefill,
+                        rerope, rmsnorm, rope, rope_freqs, round_bf16, round_store, select_hkvd, selected_count, silu,
+                        to_f64, Model, validate_chunks)
 from . import accounting
 
-__all__ = ["attention", "blend", "chunk_caches", "deviation", "deviation_rows", "prefill", "rerope", "rmsnorm", "rope",
+__all__ = ["attention", "blend", "blend_gradual", "gradual_counts", "chunk_caches", "deviation", "deviation_rows", "prefill", "rerope", "rmsnorm", "rope",
            "rope_freqs", "round_bf16", "round_store", "select_hkvd", "selected_count", "silu", "to_f64",
            "Model", "validate_chunks", "accounting"]

@@ -157,3 +157,18 @@ def test_llama8b_32k_full_reuse(cb):
     ref = oracle.blend(spec.shape.as_dict(), w, req.tokens, caches, req.chunks, 0.0, "bf16", keep_exact=True)
     parity.assert_kv(g_q, ref["out_kv_exact"][:, :, spec.n_ctx:], "bf16", "query-row K/V")
     parity.assert_logits(res["logits"], ref["logits"], "bf16")
+
+
+def test_llama8b_3k_gradual(cb):
+    """Gradual filtering at the 8B shape, 3K context: 0.30 at the check layer shrinking to 0.15 by
+    layer 5 (the funnel schedule bench.py --gradual times).  Every shrinking layer's set, all K/V and
+    the logits against the full oracle."""
+    import test_gpu_gradual as tg
+    spec = workload.WORKLOADS["llama8b-3k"]
+    shape, seed = spec.shape, spec.seeds[0]
+    ratios = workload.funnel_ratios(shape.n_layers, spec.ratios[0])
+    w = workload.make_weights(shape, seed)
+    req = workload.make_request(spec, seed, spec.ratios[0])
+    caches = workload.synthetic_cache(shape, seed, spec.n_ctx, workload.kv_std(shape))
+    r = tg.compare_gradual(cb, shape, w, req.tokens, caches, req.chunks, ratios, "bf16")
+    print(f"8B 3K gradual: {r}")

@@ -252,3 +252,16 @@ def synthetic_cache(s: ModelShape, seed: int, n_rows: int, std: float) -> np.nda
 def kv_std(s: ModelShape, std: float = 0.02) -> float:
     """Scale of K/V entries in a random-init model (unit-RMS input times N(0,std) weights)."""
     return std * float(np.sqrt(s.d_model))
+
+
+def funnel_ratios(n_layers: int, r: float, r_first: float = None, steps: int = 4) -> tuple:
+    """A gradual-filtering schedule for layers 1..n_layers-1: the check layer keeps r_first (2r by
+    default, capped at 1), and the ratio shrinks in equal steps to r over the next `steps` layers,
+    then stays at r (the funnel of Figure 9, settling near the target r).  Holds no method arithmetic:
+    it only chooses inputs."""
+    r1 = min(1.0, 2.0 * r) if r_first is None else r_first
+    out = []
+    for layer in range(1, n_layers):
+        t = min(layer - 1, steps) / steps
+        out.append(r1 + (r - r1) * t)
+    return tuple(out)
