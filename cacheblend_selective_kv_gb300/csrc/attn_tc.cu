@@ -4,16 +4,21 @@
 // Work unit = (tile of 128/G consecutive recomputed queries, KV head g): its 128 TMEM lanes hold the
 // G query heads that share KV head g for each of those queries (row r = query * G + head), so each
 // K/V block is read once for the whole GQA group.  Queries are sorted by position; a unit streams
-// 64-key blocks 0 .. pos(last query) and masks keys past each row's own position (causal by global
+// 128-key blocks 0 .. pos(last query) and masks keys past each row's own position (causal by global
 // position).
-//   warp 0      TMA producer: the Q tile (4-D box), then K and V blocks of KV head g
-//   warp 1      MMA issuer: S = Q K^T into TMEM; O_h += P_h V_h for each half h of the block's keys
-//   warps 2..9  softmax, two warps per TMEM lane quarter: the warps of half h own keys 32h..32h+31 of
-//               every block, keep their own running max and sum, write P_h (bf16) into 128-byte-swizzled
-//               shared memory and accumulate O_h in TMEM.  O_h is rescaled in TMEM only when that
-//               half's running max grows by more than 2^8 (exp2 domain), so P stays below 256.
+//   warp 0      TMA producer of the Q tile (4-D box) and the K blocks (3-stage ring)
+//   warp 10     TMA producer of the V blocks (2-stage ring)
+//   warp 1      MMA issuer: S = Q K^T into a TMEM buffer; O_h += P_h V_h with P read from TMEM
+//   warps 2..9  softmax, two warps per TMEM lane quarter: the warps of half h own keys 64h..64h+63
+//               of every block, keep their own running max and sum, and overwrite their S columns
+//               with P_h (bf16; in split precision a hi and a lo part), which the PV MMA reads as its
+//               A operand straight from tensor memory.  O_h lives in TMEM and is rescaled only when
+//               that half's running max grows by more than 2^8 (exp2 domain), so P stays below 256.
 // At the end of a unit the half-1 warps combine both halves: O = (O_0 2^(m_0-M) + O_1 2^(m_1-M)) / l.
-// S is double buffered in TMEM; V is consumed as an MN-major operand from its [key][dim] layout.
+// S/P is double buffered in TMEM; a buffer is reused for S once the PV MMAs that read its P are done.
+// K blocks are released as soon as their S MMAs complete and V blocks once their PV MMAs do, so the
+// K loads run up to three blocks ahead.  V is consumed as an MN-major operand from its [key][dim]
+// layout.
 #include <cudaTypedefs.h>
 
 #include "cb_ptx.cuh"
@@ -22,10 +27,11 @@ namespace cb {
 
 namespace {
 
-constexpr int BKV = 64;                  // keys per block
-constexpr int HK = 32;                   // keys per softmax half
+constexpr int BKV = 128;                 // keys per block
+constexpr int HK = 64;                   // keys per softmax half
 constexpr int ROWS = 128;                // TMEM lanes per unit
-constexpr int NUM_THREADS = 320;         // producer, MMA, 8 softmax warps
+constexpr int NUM_THREADS = 352;         // K producer, MMA, 8 softmax warps, V producer
+constexpr int K_STAGES = 3, V_STAGES = 2;
 constexpr float RESCALE_LOG2 = 8.0f;     // lazy-rescale threshold (P <= 2^8)
 
 struct AttnArgs {
@@ -56,8 +62,30 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-__device__ __forceinline__ void fence_proxy_async() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+// D[tmem] (+)= A[tmem] * B[smem]: A (M = 128 rows in the lanes, K = 16 bf16 packed two per 32-bit
+// column, 8 columns) read from tensor memory; one thread issues it
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 32 lanes x 32-bit, 16 consecutive columns per thread (raw words)
+__device__ __forceinline__ void tmem_st16_u(uint32_t taddr, const uint32_t* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+          "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo_k, float hi_k) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(lo_k, hi_k);      // .x (lower key) in the low 16 bits
+    return *reinterpret_cast<uint32_t*>(&t);
 }
 
 // MN-major operand descriptor, 128-byte swizzle: rows of 64 elements (128 B) along the MN
@@ -139,27 +167,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                    const __grid_constant__ CUtensorMap mkv, const AttnArgs a) {
     // split precision carries q and P as hi + lo bf16 pairs: two MMAs into the same accumulator
     constexpr int NP = SPLIT ? 2 : 1;
-    constexpr int KV_STAGES = SPLIT ? 2 : 3;
     constexpr int HALVES = HD / 64;
     constexpr int Q_BYTES = ROWS * HD * 2;            // one Q tile (hi or lo)
     constexpr int KB_BYTES = BKV * HD * 2;            // one K (or V) block
-    constexpr int P_BYTES = ROWS * BKV * 2;           // one P tile (hi or lo)
-    constexpr uint32_t S_COL = 0, O_COL = 128;        // TMEM: S buffers at 0 / 64, O_h at 128 + 128 h
+    constexpr uint32_t S_COL = 0, O_COL = 256;        // TMEM: S/P buffers at 0 / 128, O_h at 256 + HD h
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;                               // [NP] Q tiles
-    uint8_t* sK = sQ + NP * Q_BYTES;                  // [KV_STAGES] K blocks
-    uint8_t* sV = sK + KV_STAGES * KB_BYTES;          // [KV_STAGES] V blocks
-    uint8_t* sP = sV + KV_STAGES * KB_BYTES;          // [2 buffers][NP] P tiles
-    float* cmb = reinterpret_cast<float*>(sP + 2 * NP * P_BYTES);   // [128][2] half-0 (max, sum)
+    uint8_t* sK = sQ + NP * Q_BYTES;                  // [K_STAGES] K blocks
+    uint8_t* sV = sK + K_STAGES * KB_BYTES;           // [V_STAGES] V blocks
+    float* cmb = reinterpret_cast<float*>(sV + V_STAGES * KB_BYTES);   // [128][2] half-0 (max, sum)
     uint64_t* bars = reinterpret_cast<uint64_t*>(cmb + 2 * ROWS);
     uint64_t* q_full = bars;
     uint64_t* q_empty = bars + 1;
-    uint64_t* kv_full = bars + 2;
-    uint64_t* kv_empty = kv_full + KV_STAGES;
-    uint64_t* s_full = kv_empty + KV_STAGES;
-    uint64_t* s_empty = s_full + 2;
-    uint64_t* p_full = s_empty + 2;                   // [buffer][half]
+    uint64_t* k_full = bars + 2;
+    uint64_t* k_empty = k_full + K_STAGES;
+    uint64_t* v_full = k_empty + K_STAGES;
+    uint64_t* v_empty = v_full + V_STAGES;
+    uint64_t* s_full = v_empty + V_STAGES;            // [buffer]: S written
+    uint64_t* s_free = s_full + 2;                    // [buffer]: the PV MMAs reading its P are done
+    uint64_t* p_full = s_free + 2;                    // [buffer][half]
     uint64_t* o_full = p_full + 4;                    // [half][block parity]
     uint64_t* o_free = o_full + 4;
     uint64_t* cmb_bar = o_free + 1;
@@ -171,13 +198,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         ptx::mbar_init(ptx::smem_u32(q_full), 1);
         ptx::mbar_init(ptx::smem_u32(q_empty), 1);
-        for (int i = 0; i < KV_STAGES; ++i) {
-            ptx::mbar_init(ptx::smem_u32(kv_full + i), 1);
-            ptx::mbar_init(ptx::smem_u32(kv_empty + i), 1);
+        for (int i = 0; i < K_STAGES; ++i) {
+            ptx::mbar_init(ptx::smem_u32(k_full + i), 1);
+            ptx::mbar_init(ptx::smem_u32(k_empty + i), 1);
+        }
+        for (int i = 0; i < V_STAGES; ++i) {
+            ptx::mbar_init(ptx::smem_u32(v_full + i), 1);
+            ptx::mbar_init(ptx::smem_u32(v_empty + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(ptx::smem_u32(s_full + i), 1);
-            ptx::mbar_init(ptx::smem_u32(s_empty + i), 8);
+            ptx::mbar_init(ptx::smem_u32(s_free + i), 1);
         }
         for (int i = 0; i < 4; ++i) ptx::mbar_init(ptx::smem_u32(o_full + i), 1);
         for (int i = 0; i < 4; ++i) ptx::mbar_init(ptx::smem_u32(p_full + i), 4);
@@ -200,9 +231,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem = *tmem_holder;
 
     if (warp == 0) {
-        // ---------------------------------------------------------------- TMA producer
+        // ---------------------------------------------------------------- TMA producer: Q and K
         if (lane == 0) {
-            uint32_t q_cnt = 0, kv_cnt = 0;
+            uint32_t q_cnt = 0, k_cnt = 0;
             uint32_t issued = 0, issued_par = 0;
             bool q_issued = false;
             uint32_t q_par = 0;
@@ -224,38 +255,65 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 q_par = q_cnt & 1u;
                 ++q_cnt;
                 for (int b = b0; b < b1; ++b) {
-                    const int st = kv_cnt % KV_STAGES;
-                    const uint32_t par = (kv_cnt / KV_STAGES) & 1u;
-                    if (!await(ptx::smem_u32(kv_empty + st), par ^ 1u, abort, a.status, 2, kv_cnt, u)) { ok = false; break; }
-                    const uint32_t fb = ptx::smem_u32(kv_full + st);
-                    ptx::mbar_arrive_expect_tx(fb, 2 * KB_BYTES);
-                    for (int h = 0; h < HALVES; ++h) {
+                    const int st = k_cnt % K_STAGES;
+                    const uint32_t par = (k_cnt / K_STAGES) & 1u;
+                    if (!await(ptx::smem_u32(k_empty + st), par ^ 1u, abort, a.status, 2, k_cnt, u)) { ok = false; break; }
+                    const uint32_t fb = ptx::smem_u32(k_full + st);
+                    ptx::mbar_arrive_expect_tx(fb, KB_BYTES);
+                    for (int h = 0; h < HALVES; ++h)
                         tma_load_3d(ptx::smem_u32(sK + st * KB_BYTES + h * (BKV * 128)), &mkv, g * HD + h * 64,
                                     b * BKV, a.kv_z, fb);
-                        tma_load_3d(ptx::smem_u32(sV + st * KB_BYTES + h * (BKV * 128)), &mkv, g * HD + h * 64,
-                                    b * BKV, a.kv_z + 1, fb);
-                    }
                     issued |= 1u << st;
                     issued_par = (issued_par & ~(1u << st)) | (par << st);
-                    ++kv_cnt;
+                    ++k_cnt;
                 }
             }
+            // every load this thread issued has landed before the CTA may exit
             if (q_issued) drain_wait(ptx::smem_u32(q_full), q_par, a.status);
-            for (int i = 0; i < KV_STAGES; ++i)
-                if (issued & (1u << i)) drain_wait(ptx::smem_u32(kv_full + i), (issued_par >> i) & 1u, a.status);
+            for (int i = 0; i < K_STAGES; ++i)
+                if (issued & (1u << i)) drain_wait(ptx::smem_u32(k_full + i), (issued_par >> i) & 1u, a.status);
+        }
+    } else if (warp == NUM_THREADS / 32 - 1) {
+        // ---------------------------------------------------------------- TMA producer: V
+        if (lane == 0) {
+            uint32_t v_cnt = 0, issued = 0, issued_par = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+                int qt, g, part, b0, b1;
+                unit_of(a, u, qt, g, part);
+                item_blocks(a, qt, part, b0, b1);
+                for (int b = b0; b < b1; ++b) {
+                    const int st = v_cnt % V_STAGES;
+                    const uint32_t par = (v_cnt / V_STAGES) & 1u;
+                    if (!await(ptx::smem_u32(v_empty + st), par ^ 1u, abort, a.status, 7, v_cnt, u)) { ok = false; break; }
+                    const uint32_t fb = ptx::smem_u32(v_full + st);
+                    ptx::mbar_arrive_expect_tx(fb, KB_BYTES);
+                    for (int h = 0; h < HALVES; ++h)
+                        tma_load_3d(ptx::smem_u32(sV + st * KB_BYTES + h * (BKV * 128)), &mkv, g * HD + h * 64,
+                                    b * BKV, a.kv_z + 1, fb);
+                    issued |= 1u << st;
+                    issued_par = (issued_par & ~(1u << st)) | (par << st);
+                    ++v_cnt;
+                }
+            }
+            for (int i = 0; i < V_STAGES; ++i)
+                if (issued & (1u << i)) drain_wait(ptx::smem_u32(v_full + i), (issued_par >> i) & 1u, a.status);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            uint32_t q_cnt = 0, kv_cnt = 0, s_cnt = 0, unit_cnt = 0;
+            uint32_t q_cnt = 0, k_cnt = 0, v_cnt = 0, s_cnt = 0, unit_cnt = 0;
             bool ok = true;
-            // O_h += P_h V_h for the block whose S had counter `sc`, whose K/V sit in stage `st`
-            auto pv = [&](uint32_t sc, uint32_t st, bool first) -> bool {
+            // O_h += P_h V_h for the block whose S had counter `sc` (P in that S buffer)
+            auto pv = [&](uint32_t sc, bool first) -> bool {
                 const int buf = sc & 1;
                 const uint32_t par = (sc >> 1) & 1u;
+                const uint32_t st = v_cnt % V_STAGES, vpar = (v_cnt / V_STAGES) & 1u;
                 if (first && !await(ptx::smem_u32(o_free), (unit_cnt & 1u) ^ 1u, abort, a.status, 3, unit_cnt, -1)) return false;
-                const uint32_t pa = ptx::smem_u32(sP + buf * NP * P_BYTES);
+                if (!await(ptx::smem_u32(v_full + st), vpar, abort, a.status, 8, v_cnt, -1)) return false;
+                ++v_cnt;
                 const uint32_t va = ptx::smem_u32(sV + st * KB_BYTES);
+                const uint32_t pt = tmem + S_COL + buf * 128;
                 for (int h = 0; h < 2; ++h) {
                     if (!await(ptx::smem_u32(p_full + buf * 2 + h), par, abort, a.status, 10 + h, sc, -1)) return false;
                     ptx::tc_fence_after();
@@ -264,14 +322,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const int key = h * HK + kk * 16;
                         const uint64_t vd = sdesc_mn_sw128(va + key * 128, BKV * 128);
                         const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
-                        ptx::mma_bf16(tmem + O_COL + h * 128, ptx::sdesc_sw128(pa + key * 2), vd, a.idesc_pv, acc0);
-                        if (SPLIT)
-                            ptx::mma_bf16(tmem + O_COL + h * 128, ptx::sdesc_sw128(pa + P_BYTES + key * 2), vd,
-                                          a.idesc_pv, 1u);
+                        mma_bf16_tmem_a(tmem + O_COL + h * HD, pt + h * 64 + kk * 8, vd, a.idesc_pv, acc0);
+                        if (SPLIT) mma_bf16_tmem_a(tmem + O_COL + h * HD, pt + h * 64 + 32 + kk * 8, vd, a.idesc_pv, 1u);
                     }
                     ptx::mma_commit(ptx::smem_u32(o_full + h * 2 + buf));
                 }
-                ptx::mma_commit(ptx::smem_u32(kv_empty + st));
+                ptx::mma_commit(ptx::smem_u32(s_free + buf));
+                ptx::mma_commit(ptx::smem_u32(v_empty + st));
                 return true;
             };
             for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
@@ -282,37 +339,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int nb = b1 - b0;
                 if (!await(ptx::smem_u32(q_full), q_cnt & 1u, abort, a.status, 4, q_cnt, u)) break;
                 ++q_cnt;
-                uint32_t prev_st = 0, prev_sc = 0;
+                uint32_t prev_sc = 0;
                 for (int b = 0; b < nb; ++b) {
-                    const uint32_t st = kv_cnt % KV_STAGES;
-                    const uint32_t kpar = (kv_cnt / KV_STAGES) & 1u;
-                    ++kv_cnt;
+                    const uint32_t st = k_cnt % K_STAGES;
+                    const uint32_t kpar = (k_cnt / K_STAGES) & 1u;
+                    ++k_cnt;
                     const int buf = s_cnt & 1;
                     const uint32_t spar = (s_cnt >> 1) & 1u;
-                    if (!await(ptx::smem_u32(kv_full + st), kpar, abort, a.status, 5, kv_cnt, u) ||
-                        !await(ptx::smem_u32(s_empty + buf), spar ^ 1u, abort, a.status, 6, s_cnt, u)) { ok = false; break; }
+                    if (!await(ptx::smem_u32(k_full + st), kpar, abort, a.status, 5, k_cnt, u) ||
+                        !await(ptx::smem_u32(s_free + buf), spar ^ 1u, abort, a.status, 6, s_cnt, u)) { ok = false; break; }
                     ptx::tc_fence_after();
                     const uint32_t qa = ptx::smem_u32(sQ), ka = ptx::smem_u32(sK + st * KB_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < HD / 16; ++kk) {
                         const uint32_t off = (kk & 3) * 32;
                         const uint64_t kd = ptx::sdesc_sw128(ka + (kk >> 2) * (BKV * 128) + off);
-                        ptx::mma_bf16(tmem + S_COL + buf * 64, ptx::sdesc_sw128(qa + (kk >> 2) * (ROWS * 128) + off),
+                        ptx::mma_bf16(tmem + S_COL + buf * 128, ptx::sdesc_sw128(qa + (kk >> 2) * (ROWS * 128) + off),
                                       kd, a.idesc_qk, kk > 0 ? 1u : 0u);
                         if (SPLIT)
-                            ptx::mma_bf16(tmem + S_COL + buf * 64,
+                            ptx::mma_bf16(tmem + S_COL + buf * 128,
                                           ptx::sdesc_sw128(qa + Q_BYTES + (kk >> 2) * (ROWS * 128) + off), kd,
                                           a.idesc_qk, 1u);
                     }
                     ptx::mma_commit(ptx::smem_u32(s_full + buf));
-                    if (b > 0 && !pv(prev_sc, prev_st, b == 1)) { ok = false; break; }
-                    prev_st = st;
+                    ptx::mma_commit(ptx::smem_u32(k_empty + st));
+                    if (b == nb - 1) ptx::mma_commit(ptx::smem_u32(q_empty));
+                    if (b > 0 && !pv(prev_sc, b == 1)) { ok = false; break; }
                     prev_sc = s_cnt;
                     ++s_cnt;
                 }
                 if (!ok) break;
-                if (!pv(prev_sc, prev_st, nb == 1)) break;
-                ptx::mma_commit(ptx::smem_u32(q_empty));
+                if (!pv(prev_sc, nb == 1)) break;
                 ++unit_cnt;
             }
             ptx::mma_commit(ptx::smem_u32(drain));
@@ -324,7 +381,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int hf = (warp - 2) >> 2;               // key half of every block
         const int row = q4 * 32 + lane;
         const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-        const uint32_t o_tm = tmem + lane_base + O_COL + hf * 128;
+        const uint32_t o_tm = tmem + lane_base + O_COL + hf * HD;
         uint32_t sc = 0, unit_cnt = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
@@ -343,12 +400,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint32_t par = (sc >> 1) & 1u;
                 if (!await(ptx::smem_u32(s_full + buf), par, abort, a.status, 20 + hf, sc, u)) { ok = false; break; }
                 ptx::tc_fence_after();
+                const uint32_t s_tm = tmem + lane_base + S_COL + buf * 128 + hf * HK;
                 float s[HK];
-                ptx::tmem_ld16(tmem + lane_base + S_COL + buf * 64 + hf * HK, s);
-                ptx::tmem_ld16(tmem + lane_base + S_COL + buf * 64 + hf * HK + 16, s + 16);
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(s_empty + buf));
+#pragma unroll
+                for (int c = 0; c < HK / 16; ++c) ptx::tmem_ld16(s_tm + c * 16, s + c * 16);
                 const int j0 = (b0 + b) * BKV + hf * HK;
                 // causal mask only where this block crosses some row's position (warp-uniform test)
                 if (j0 + HK - 1 > prow_min) {
@@ -359,21 +414,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int i = 1; i < HK; ++i) mx = fmaxf(mx, s[i]);
                 m_run = fmaxf(m_run, mx * a.scale_log2);      // exp2 domain
-                // O_h += P_h V for block sc-2 (same P buffer) must be complete before P buffer sc&1 is
-                // rewritten; block sc-1's update only before O_h is rescaled.  o_full[hf][x] completes
-                // once per block of parity x, and block sc's update cannot complete before its P is
-                // written, so neither wait lags its barrier by two phases.
-                if (sc >= 2 &&
-                    !await(ptx::smem_u32(o_full + hf * 2 + buf), ((sc >> 1) & 1u) ^ 1u, abort, a.status, 30 + hf, sc, u)) {
-                    ok = false;
-                    break;
-                }
                 // rescale O_h when the running max outgrew the scale in use by more than 2^8.  The TMEM
                 // accesses are warp-collective (.sync.aligned), so when any lane needs it the whole warp
                 // rescales, each row by its own factor (rescaling to the current max is always valid).
+                // O_h must first hold block sc-1's update: o_full[hf][x] completes once per block of
+                // parity x, and block sc+1's update cannot complete before this warp writes its P.
                 const bool need = m_used != -INFINITY && m_run > m_used + RESCALE_LOG2;
                 if (__any_sync(0xffffffffu, need)) {
-                    if (b > 0) {   // block sc-1 (this unit) has added into O_h
+                    if (b > 0) {
                         const uint32_t pb = sc - 1;
                         if (!await(ptx::smem_u32(o_full + hf * 2 + (pb & 1)), (pb >> 1) & 1u, abort, a.status, 35 + hf,
                                    pb, u)) {
@@ -396,8 +444,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     m_used = m_run;
                 }
                 if (m_used == -INFINITY) m_used = m_run;    // nothing accumulated yet (O_h holds zeros)
-                // P = 2^(s * scale - m_used) (zero when nothing is visible yet), summed, and written as a
-                // bf16 hi + lo pair into the swizzled A-operand buffer (16-byte chunks hf*4 .. hf*4+3)
+                // P = 2^(s * scale - m_used) (zero when nothing is visible yet), summed, and written over
+                // this half's S columns as bf16: hi in columns 0..31, lo (split precision) in 32..63,
+                // two keys per 32-bit column, the lower key in the low half
                 const float neg_m = (m_used == -INFINITY) ? -INFINITY : -m_used;
                 float sum = 0.f;
 #pragma unroll
@@ -406,26 +455,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     sum += s[i];
                 }
                 l += sum;
-                uint8_t* prow_ptr = sP + buf * NP * P_BYTES + row * 128;
 #pragma unroll
-                for (int c = 0; c < HK / 8; ++c) {
-                    uint4 w, wl;
-                    __nv_bfloat162* hi = reinterpret_cast<__nv_bfloat162*>(&w);
-                    __nv_bfloat162* lo = reinterpret_cast<__nv_bfloat162*>(&wl);
+                for (int c = 0; c < HK / 32; ++c) {
+                    uint32_t w[16], wl[16];
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const float p0 = s[c * 8 + 2 * t], p1 = s[c * 8 + 2 * t + 1];
-                        hi[t] = __floats2bfloat162_rn(p0, p1);
+                    for (int t = 0; t < 16; ++t) {
+                        const float p0 = s[c * 32 + 2 * t], p1 = s[c * 32 + 2 * t + 1];
+                        w[t] = pack_bf16x2(p0, p1);
                         if (SPLIT) {
-                            const float2 back = __bfloat1622float2(hi[t]);
-                            lo[t] = __floats2bfloat162_rn(p0 - back.x, p1 - back.y);
+                            const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162*>(&w[t]);
+                            const float2 back = __bfloat1622float2(hb);
+                            wl[t] = pack_bf16x2(p0 - back.x, p1 - back.y);
                         }
                     }
-                    const int chunk = (hf * 4 + c) ^ (row & 7);
-                    *reinterpret_cast<uint4*>(prow_ptr + (chunk << 4)) = w;
-                    if (SPLIT) *reinterpret_cast<uint4*>(prow_ptr + P_BYTES + (chunk << 4)) = wl;
+                    tmem_st16_u(s_tm + c * 16, w);
+                    if (SPLIT) tmem_st16_u(s_tm + 32 + c * 16, wl);
                 }
-                fence_proxy_async();
+                ptx::tmem_wait_st();
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(p_full + buf * 2 + hf));
@@ -442,16 +488,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (hf == 0) {
                 cmb[row * 2] = m_used;
                 cmb[row * 2 + 1] = l;
+                ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(cmb_bar));
             } else {
                 if (!await(ptx::smem_u32(cmb_bar), unit_cnt & 1u, abort, a.status, 50, unit_cnt, u)) break;
+                ptx::tc_fence_after();
                 const float m0 = cmb[row * 2], l0 = cmb[row * 2 + 1];
                 const float M = fmaxf(m0, m_used);
                 const float f0 = (m0 == -INFINITY) ? 0.f : exp2f(m0 - M);
                 const float f1 = (m_used == -INFINITY) ? 0.f : exp2f(m_used - M);
                 const float L = l0 * f0 + l * f1;
-                const uint32_t o0 = tmem + lane_base + O_COL, o1 = o0 + 128;
+                const uint32_t o0 = tmem + lane_base + O_COL, o1 = o0 + HD;
                 if (a.parts == 1) {
                     const float inv = 1.0f / L;
                     const int head = g * a.G + row % a.G;
@@ -560,9 +608,8 @@ bool get_encode() {
 
 template <int HD, bool SPLIT>
 size_t attn_smem() {
-    const size_t np = SPLIT ? 2 : 1, stages = SPLIT ? 2 : 3;
-    return 1024 + np * ROWS * HD * 2 + 2 * stages * (size_t)BKV * HD * 2 + 2 * np * (size_t)ROWS * BKV * 2 +
-           2 * ROWS * sizeof(float) + 256;
+    const size_t np = SPLIT ? 2 : 1;
+    return 1024 + np * ROWS * HD * 2 + (size_t)(K_STAGES + V_STAGES) * BKV * HD * 2 + 2 * ROWS * sizeof(float) + 256;
 }
 
 template <int HD, bool SPLIT>
