@@ -21,6 +21,9 @@
 // layout.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <cstdlib>
+
 #include "cb_ptx.cuh"
 
 namespace cb {
@@ -684,8 +687,10 @@ cudaError_t launch_attention_tc(const Model& m, const void* qmap, const void* qm
     a.parts = 1;
     const int nb_max = (n_keys + BKV - 1) / BKV;
     a.part_blocks = nb_max;
+    int per_sm = 4;                              // work items aimed at per SM
+    if (const char* v = getenv("CB_TUNE_ATTN_ITEMS")) per_sm = std::max(1, atoi(v));
     if (m.part_o && a.units < 2 * m.num_sms && nb_max > 4) {
-        int parts = (4 * m.num_sms + a.units - 1) / a.units;
+        int parts = (per_sm * m.num_sms + a.units - 1) / a.units;
         while (parts > 1 && (size_t)a.units * parts > (size_t)m.part_items) --parts;
         if (parts > nb_max) parts = nb_max;
         if (parts > 1) {
