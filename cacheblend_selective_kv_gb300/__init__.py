@@ -22,9 +22,9 @@ CB_OK, CB_ERR_INVALID_ARG, CB_ERR_UNSUPPORTED, CB_ERR_OOM, CB_ERR_CUDA, CB_ERR_I
 CB_F32, CB_BF16 = 0, 1
 CB_PREC_SPLIT, CB_PREC_BF16 = 0, 1
 CB_MAX_CHUNKS = 1024
-EXPORTED = ("cb_model_create", "cb_model_destroy", "cb_rerope", "cb_blend", "cb_blend_gradual", "cb_selected_count",
-            "cb_last_error", "cb_profile_enable", "cb_profile_read", "cb_model_status", "cb_rerope_static",
-            "cb_model_diag")
+EXPORTED = ("cb_model_create", "cb_model_destroy", "cb_rerope", "cb_blend", "cb_blend_gradual", "cb_blend_streamed",
+            "cb_selected_count", "cb_last_error", "cb_profile_enable", "cb_profile_read", "cb_model_status",
+            "cb_rerope_static", "cb_model_diag", "cb_load_time", "cb_controller_ratio", "cb_pick_storage")
 CB_STATIC_MAX_CHUNKS = 256
 CB_STATUS_BAD_TOKEN, CB_STATUS_WAIT_TIMEOUT, CB_STATUS_BAD_ROW = 1, 2, 4
 
@@ -55,6 +55,11 @@ class CbStats(ctypes.Structure):
                 ("n_recompute", ctypes.c_int32), ("kernel_launches", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("gemm_flops", ctypes.c_double), ("attn_flops", ctypes.c_double),
                 ("kv_bytes_moved", ctypes.c_double)]
+
+
+class CbLayerIO(ctypes.Structure):
+    _fields_ = [("cached_kv_host", ctypes.c_void_p), ("out_kv_host", ctypes.c_void_p), ("copy_stream", ctypes.c_void_p),
+                ("copy_back_stream", ctypes.c_void_p)]
 
 
 class CbKernelProfile(ctypes.Structure):
@@ -96,6 +101,16 @@ def lib() -> ctypes.CDLL:
         L.cb_blend_gradual.restype = ctypes.c_int
         L.cb_blend_gradual.argtypes = [vp, vp, i32, vp, ctypes.POINTER(CbChunk), i32, ctypes.POINTER(ctypes.c_double),
                                        i32, vp, vp, vp, vp, ctypes.POINTER(CbStats), vp]
+        L.cb_blend_streamed.restype = ctypes.c_int
+        L.cb_blend_streamed.argtypes = [vp, vp, i32, ctypes.POINTER(CbLayerIO), ctypes.POINTER(CbChunk), i32,
+                                        ctypes.POINTER(ctypes.c_double), i32, vp, vp, vp, vp, ctypes.POINTER(CbStats), vp]
+        L.cb_load_time.restype = ctypes.c_double
+        L.cb_load_time.argtypes = [ctypes.c_double, i64, ctypes.c_double]
+        L.cb_controller_ratio.restype = ctypes.c_double
+        L.cb_controller_ratio.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.c_double]
+        L.cb_pick_storage.restype = i32
+        L.cb_pick_storage.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double), i32,
+                                      ctypes.c_double, i64, ctypes.c_double, ctypes.c_double]
         L.cb_selected_count.restype = i32
         L.cb_selected_count.argtypes = [i32, ctypes.c_double]
         L.cb_profile_enable.restype = ctypes.c_int
@@ -206,6 +221,43 @@ def cb_blend_gradual(handle: int, tokens, n_tokens: int, cached_kv, chunks, rati
     if stats:
         return {f: getattr(st, f) for f, _ in CbStats._fields_}
     return None
+
+
+def cb_blend_streamed(handle: int, tokens, n_tokens: int, cached_kv_host, chunks, ratios, out_kv, out_logits,
+                      out_kv_host=None, out_selected=None, out_dev=None, stream=None, copy_stream=None,
+                      copy_back_stream=None, stats: bool = False):
+    """Layer-wise load pipeline: the chunk caches come from pinned host memory (cached_kv_host), one layer
+    per copy on copy_stream; out_kv_host (optional, pinned) receives each finished layer."""
+    st = CbStats()
+    r = (ctypes.c_double * max(1, len(ratios)))(*[float(x) for x in ratios])
+    io = CbLayerIO(_ptr(cached_kv_host) or None, _ptr(out_kv_host) or None, _stream(copy_stream),
+                   _stream(copy_back_stream) if copy_back_stream is not None else None)
+    _check(lib().cb_blend_streamed(handle, _ptr(tokens), int(n_tokens), ctypes.byref(io), _chunks(chunks), len(chunks),
+                                   r, len(ratios), _ptr(out_kv), _ptr(out_logits), _ptr(out_selected), _ptr(out_dev),
+                                   ctypes.byref(st) if stats else None, _stream(stream)))
+    if stats:
+        return {f: getattr(st, f) for f, _ in CbStats._fields_}
+    return None
+
+
+def cb_load_time(per_token_kv_bytes: float, n_tokens: int, throughput_bytes_per_s: float) -> float:
+    return float(lib().cb_load_time(float(per_token_kv_bytes), int(n_tokens), float(throughput_bytes_per_s)))
+
+
+def cb_controller_ratio(t_prefill_s: float, t_load_s: float, r_min: float = 0.15) -> float:
+    return float(lib().cb_controller_ratio(float(t_prefill_s), float(t_load_s), float(r_min)))
+
+
+def cb_pick_storage(devices, per_token_kv_bytes: float, n_tokens: int, t_prefill_s: float, r_min: float = 0.15) -> int:
+    """devices: list of (throughput bytes/s, cost per GB); returns the chosen index."""
+    n = len(devices)
+    bw = (ctypes.c_double * max(1, n))(*[float(d[0]) for d in devices])
+    cost = (ctypes.c_double * max(1, n))(*[float(d[1]) for d in devices])
+    i = int(lib().cb_pick_storage(bw, cost, n, float(per_token_kv_bytes), int(n_tokens), float(t_prefill_s),
+                                  float(r_min)))
+    if i < 0:
+        raise CacheBlendError(i, cb_last_error())
+    return i
 
 
 def cb_model_status(handle: int, clear: bool = False) -> int:
@@ -332,6 +384,25 @@ class BlendModel:
         out = dict(out_kv=out_kv, logits=logits, counts=counts, sets=sets)
         if want_dev:
             out["devs"] = devs
+        if stats:
+            out["stats"] = st
+        return out
+
+    def blend_streamed(self, tokens, cached_kv_host, chunks, ratios, out_kv=None, out_kv_host=None, stream=None,
+                       copy_stream=None, copy_back_stream=None, stats=False):
+        """Run cb_blend_streamed (chunk caches in pinned host memory, loaded layer by layer); returns
+        dict(out_kv, out_kv_host, logits, stats?).  Asynchronous on `stream`."""
+        import torch
+        n = int(tokens.shape[0])
+        if out_kv is None:
+            out_kv = self.kv_buffer(n)
+        logits = torch.empty(self.shape["vocab"], dtype=torch.float32, device=self.device)
+        if copy_stream is None:
+            copy_stream = torch.cuda.Stream(self.device)
+        st = cb_blend_streamed(self.handle, tokens, n, cached_kv_host, chunks, ratios, out_kv, logits,
+                               out_kv_host=out_kv_host, stream=stream, copy_stream=copy_stream,
+                               copy_back_stream=copy_back_stream, stats=stats)
+        out = dict(out_kv=out_kv, out_kv_host=out_kv_host, logits=logits)
         if stats:
             out["stats"] = st
         return out

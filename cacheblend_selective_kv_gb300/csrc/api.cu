@@ -198,6 +198,7 @@ cb_status cb_model_destroy(cb_model* m) {
     if (!m) return CB_OK;
     cudaDeviceSynchronize();
     for (auto e : m->prof.ev) cudaEventDestroy(e);
+    for (auto e : m->io_ev) cudaEventDestroy(e);
     tc_destroy(*m);
     free_ws(*m);
     delete m;
@@ -355,9 +356,13 @@ namespace {
 // One blend.  ks[l] (l = 1..L-1) is the number of context rows whose hidden state leaves layer l:
 // constant for the blend with one selection at the check layer, non-increasing for gradual filtering
 // (a layer with ks[l] < ks[l-1] compares its candidates again and keeps the top ks[l]).
+// `io` (optional): the layer-wise load pipeline.  The chunk caches then come from pinned host memory,
+// one layer per copy on io->copy_stream, and each layer is re-RoPE'd in place once its copy has landed,
+// just before that layer is computed; each layer's finished K/V can be copied back the same way.
 cb_status blend_impl(Model& m, const int32_t* tokens, int32_t n_tokens, const void* cached_kv, const ChunkTable& t,
                      int n_chunks, int n_ctx, const std::vector<int>& ks, void* out_kv, float* out_logits,
-                     int32_t* out_selected, float* out_dev, cb_stats* stats, cudaStream_t s) {
+                     int32_t* out_selected, float* out_dev, cb_stats* stats, cudaStream_t s,
+                     const cb_layer_io* io = nullptr) {
     const cb_config& c = m.cfg;
     const size_t es = act_size(m);
     const int L = c.n_layers, d = c.d_model, nq = c.n_heads * c.head_dim, nkv = c.n_kv_heads * c.head_dim;
@@ -380,11 +385,46 @@ cb_status blend_impl(Model& m, const int32_t* tokens, int32_t n_tokens, const vo
     };
 
     // re-RoPE placement of the chunk caches (section "位置恢复、KV 存储与加载流水线")
-    if (n_chunks > 0) {
+    cudaStream_t cs = io ? (cudaStream_t)io->copy_stream : nullptr;
+    cudaStream_t bs = io ? (io->copy_back_stream ? (cudaStream_t)io->copy_back_stream : cs) : nullptr;
+    cudaError_t io_err = cudaSuccess;
+    auto io_check = [&](cudaError_t e) { if (e != cudaSuccess && io_err == cudaSuccess) io_err = e; };
+    if (io) {
+        // fork the copy stream off the compute stream, then queue every layer's load in layer order:
+        // layer l's chunk caches land in rows 0..n_ctx-1 of its K and V blocks of out_kv
+        io_check(cudaEventRecord(m.io_ev[2 * L], s));
+        io_check(cudaStreamWaitEvent(cs, m.io_ev[2 * L], 0));
+        if (bs != cs) io_check(cudaStreamWaitEvent(bs, m.io_ev[2 * L], 0));
+        if (n_chunks > 0) {
+            const size_t w = (size_t)n_ctx * nkv * es;
+            for (int l = 0; l < L; ++l) {
+                io_check(cudaMemcpy2DAsync(layer_kv(l), (size_t)N * nkv * es,
+                                           (const char*)io->cached_kv_host + (size_t)l * 2 * w, w, w, 2,
+                                           cudaMemcpyHostToDevice, cs));
+                io_check(cudaEventRecord(m.io_ev[l], cs));
+            }
+            S.k(K_DELTA, 0, 0, [&] { return launch_delta_table(m, t, s); });
+        }
+    } else if (n_chunks > 0) {
         S.k(K_DELTA, 0, 0, [&] { return launch_delta_table(m, t, s); });
         S.k(K_REROPE, 0, (inplace ? 2.0 : 4.0) * L * n_ctx * row,
             [&] { return launch_rerope(m, cached_kv, out_kv, inplace ? N : n_ctx, N, n_ctx, n_chunks, !inplace, s); });
     }
+    // pipeline: layer l's cache must have landed (and be re-rotated) before layer l reads it ...
+    auto layer_in = [&](int l) {
+        if (!io || n_chunks == 0) return;
+        io_check(cudaStreamWaitEvent(s, m.io_ev[l], 0));
+        S.k(K_REROPE, 0, 2.0 * n_ctx * row,
+            [&] { return launch_rerope(m, layer_kv(l), layer_kv(l), N, N, n_ctx, n_chunks, false, s, 1); });
+    };
+    // ... and once layer l's K/V are final (its recomputed rows stored), they can go back to the host
+    auto layer_out = [&](int l) {
+        if (!io || !io->out_kv_host) return;
+        io_check(cudaEventRecord(m.io_ev[L + l], s));
+        io_check(cudaStreamWaitEvent(bs, m.io_ev[L + l], 0));
+        io_check(cudaMemcpyAsync((char*)io->out_kv_host + (size_t)l * 2 * N * nkv * es, layer_kv(l),
+                                 (size_t)2 * N * nkv * es, cudaMemcpyDeviceToHost, bs));
+    };
     S.k(K_EMBED, 0, (double)N * d * (es + 4), [&] { return launch_embed(m, tokens, N, m.h, s); });
     alignas(64) unsigned char kvmap[128];
     const bool attn_tc = m.attn_tc && attn_make_kvmap(m, out_kv, N, kvmap);
@@ -415,7 +455,9 @@ cb_status blend_impl(Model& m, const int32_t* tokens, int32_t n_tokens, const vo
         ekv.k_dst = layer_kv(0);
         ekv.v_dst = layer_v(0);
         S.gemm(K_GEMM_KV, XBUF_X, n_ctx, Q, d, wsel(m, 0, WSEL_KV), 2 * nkv, ekv);
+        layer_in(0);
         attend(0, m.iota, N, keys0);
+        layer_out(0);
         EpiParams er = epi_base(m, EPI_RESID, N);
         er.h = m.h;
         er.ldh = d;
@@ -439,6 +481,7 @@ cb_status blend_impl(Model& m, const int32_t* tokens, int32_t n_tokens, const vo
         ekv.k_dst = m.kf;
         ekv.v_dst = m.vf;
         S.gemm(K_GEMM_KV, XBUF_X, 0, N, d, wsel(m, 1, WSEL_KV), 2 * nkv, ekv);
+        layer_in(1);
         if (n_ctx > 0)
             S.k(K_DEVIATION, 0, (double)n_ctx * 2 * nkv * (4 + es),
                 [&] { return launch_deviation(m, m.kf, m.vf, layer_kv(1), N, nullptr, n_ctx, devp, s); });
@@ -467,6 +510,7 @@ cb_status blend_impl(Model& m, const int32_t* tokens, int32_t n_tokens, const vo
         const int kl = ks[l];
         const int Mp = k_prev + Q, Ml = kl + Q;
         void* xcp = xc == XBUF_X ? m.x : m.xA;
+        if (l >= 2) layer_in(l);
         if (l >= 2 && kl < k_prev) {
             // shrinking layer (Figure 9): fresh K/V of the candidates, their deviation against the
             // re-RoPE'd cache of this layer, the top kl of them, compaction, then Q of the kept rows
@@ -515,6 +559,7 @@ cb_status blend_impl(Model& m, const int32_t* tokens, int32_t n_tokens, const vo
             S.gemm(K_GEMM_QKV, xc, 0, Ml, d, wsel(m, l, WSEL_QKV), nq + 2 * nkv, e);
         }
         attend(l, rows_c, Ml, keys_of(kl));
+        layer_out(l);
         attn_total += attn_flops(keys_of(kl));
         EpiParams er = epi_base(m, EPI_RESID, Ml);
         er.h = hc;
@@ -535,6 +580,15 @@ cb_status blend_impl(Model& m, const int32_t* tokens, int32_t n_tokens, const vo
     S.k(K_LOGITS, 2.0 * d * c.vocab, (double)c.vocab * d * es,
         [&] { return launch_logits(m, h_last, out_logits, s); });
 
+    if (io) {   // join: the compute stream completes only after every copy
+        io_check(cudaEventRecord(m.io_ev[2 * L + 1], cs));
+        io_check(cudaStreamWaitEvent(s, m.io_ev[2 * L + 1], 0));
+        if (bs != cs) {
+            io_check(cudaEventRecord(m.io_ev[2 * L + 2], bs));
+            io_check(cudaStreamWaitEvent(s, m.io_ev[2 * L + 2], 0));
+        }
+    }
+    if (io_err != cudaSuccess) return fail(CB_ERR_CUDA, "layer-wise copies: %s", cudaGetErrorString(io_err));
     if (S.err != cudaSuccess) return fail(CB_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(S.err));
     if (stats) {
         stats->n_tokens = N;
@@ -596,6 +650,47 @@ cb_status cb_blend(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const 
                       out_dev, stats, (cudaStream_t)stream);
 }
 
+cb_status cb_blend_streamed(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const cb_layer_io* io,
+                            const cb_chunk* chunks, int32_t n_chunks, const double* ratios, int32_t n_ratios,
+                            void* out_kv, float* out_logits, int32_t* out_selected, float* out_dev, cb_stats* stats,
+                            void* stream) {
+    g_err[0] = 0;
+    if (!mp) return fail(CB_ERR_INVALID_ARG, "cb_blend_streamed: null model");
+    Model& m = *mp;
+    const int L = m.cfg.n_layers;
+    if (!io) return fail(CB_ERR_INVALID_ARG, "cb_blend_streamed: null io");
+    if (!io->copy_stream || io->copy_stream == stream || (io->copy_back_stream && io->copy_back_stream == stream))
+        return fail(CB_ERR_INVALID_ARG, "cb_blend_streamed: the copy streams must be streams of their own");
+    if (n_chunks > 0 && !io->cached_kv_host) return fail(CB_ERR_INVALID_ARG, "cb_blend_streamed: chunks given but no host cache");
+    if (!ratios || n_ratios != L - 1)
+        return fail(CB_ERR_INVALID_ARG, "cb_blend_streamed: need n_layers - 1 = %d ratios (got %d)", L - 1, n_ratios);
+    for (int i = 0; i < n_ratios; ++i)
+        if (!(ratios[i] >= 0.0 && ratios[i] <= 1.0)) return fail(CB_ERR_INVALID_ARG, "ratio of layer %d outside [0, 1]", i + 1);
+    ChunkTable t;
+    int n_ctx = 0;
+    // validated as an in-place blend: the host cache is copied into out_kv's rows
+    cb_status st = check_blend(m, tokens, n_tokens, out_kv, chunks, n_chunks, out_kv, out_logits, t, n_ctx);
+    if (st != CB_OK) return st;
+    std::vector<int> ks(L, 0);
+    for (int l = 1; l < L; ++l) {
+        ks[l] = cb_selected_count(n_ctx, ratios[l - 1]);
+        if (l >= 2 && ks[l] > ks[l - 1])
+            return fail(CB_ERR_INVALID_ARG, "layer %d keeps %d rows, more than layer %d's %d: the sets must be nested",
+                        l, ks[l], l - 1, ks[l - 1]);
+    }
+    ks[0] = ks[1];
+    if ((int)m.io_ev.size() < 2 * L + 3) {
+        for (int i = (int)m.io_ev.size(); i < 2 * L + 3; ++i) {
+            cudaEvent_t e;
+            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+                return fail(CB_ERR_CUDA, "cb_blend_streamed: cudaEventCreate failed");
+            m.io_ev.push_back(e);
+        }
+    }
+    return blend_impl(m, tokens, n_tokens, out_kv, t, n_chunks, n_ctx, ks, out_kv, out_logits, out_selected, out_dev,
+                      stats, (cudaStream_t)stream, io);
+}
+
 cb_status cb_blend_gradual(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const void* cached_kv,
                            const cb_chunk* chunks, int32_t n_chunks, const double* ratios, int32_t n_ratios,
                            void* out_kv, float* out_logits, int32_t* out_selected, float* out_dev, cb_stats* stats,
@@ -622,6 +717,34 @@ cb_status cb_blend_gradual(cb_model* mp, const int32_t* tokens, int32_t n_tokens
     ks[0] = ks[1];
     return blend_impl(m, tokens, n_tokens, cached_kv, t, n_chunks, n_ctx, ks, out_kv, out_logits, out_selected,
                       out_dev, stats, (cudaStream_t)stream);
+}
+
+double cb_load_time(double per_token_kv_bytes, int64_t n_tokens, double throughput_bytes_per_s) {
+    if (!(throughput_bytes_per_s > 0) || !(per_token_kv_bytes >= 0) || n_tokens < 0) return -1.0;
+    return per_token_kv_bytes * (double)n_tokens / throughput_bytes_per_s;
+}
+
+double cb_controller_ratio(double t_prefill_s, double t_load_s, double r_min) {
+    if (!(t_prefill_s >= 0) || !(t_load_s >= 0) || !(r_min >= 0 && r_min <= 1)) return -1.0;
+    const double r_match = t_prefill_s > 0 ? t_load_s / t_prefill_s : 1.0;
+    const double r = r_match > r_min ? r_match : r_min;
+    return r < 1.0 ? r : 1.0;
+}
+
+int32_t cb_pick_storage(const double* throughput_bytes_per_s, const double* cost_per_gb, int32_t n_devices,
+                        double per_token_kv_bytes, int64_t n_tokens, double t_prefill_s, double r_min) {
+    g_err[0] = 0;
+    if (!throughput_bytes_per_s || !cost_per_gb || n_devices <= 0)
+        return (int32_t)fail(CB_ERR_INVALID_ARG, "cb_pick_storage: no devices");
+    const double budget = r_min * t_prefill_s;      // the recompute time at the quality floor
+    int best = -1, fastest = 0;
+    for (int i = 0; i < n_devices; ++i) {
+        const double tl = cb_load_time(per_token_kv_bytes, n_tokens, throughput_bytes_per_s[i]);
+        if (tl < 0) return (int32_t)fail(CB_ERR_INVALID_ARG, "cb_pick_storage: device %d has no throughput", i);
+        if (throughput_bytes_per_s[i] > throughput_bytes_per_s[fastest]) fastest = i;
+        if (tl <= budget && (best < 0 || cost_per_gb[i] < cost_per_gb[best])) best = i;
+    }
+    return best >= 0 ? best : fastest;
 }
 
 cb_status cb_model_status(cb_model* m, uint32_t* bits, int32_t clear) {

@@ -158,6 +158,7 @@ struct Model {
     alignas(64) unsigned char qmap_lo[128];
     size_t ws_bytes;
     Profile prof;
+    std::vector<cudaEvent_t> io_ev;   // layer-wise load pipeline: [n_layers] loaded, [n_layers] final, fork, 2 joins
 };
 
 // ------------------------------------------------------------------------------------------------
@@ -172,7 +173,7 @@ struct ChunkTable {
 
 cudaError_t launch_delta_table(const Model& m, const ChunkTable& t, cudaStream_t s);
 cudaError_t launch_rerope(const Model& m, const void* src, void* dst, int64_t src_rows, int64_t dst_rows,
-                          int n_ctx, int n_chunks, bool copy_v, cudaStream_t s);
+                          int n_ctx, int n_chunks, bool copy_v, cudaStream_t s, int layers = 0);
 cudaError_t launch_embed(const Model& m, const int* tokens, int n, float* h, cudaStream_t s);
 cudaError_t launch_rmsnorm(const Model& m, const float* h, const void* g, void* out, void* out_lo, int n,
                            cudaStream_t s);

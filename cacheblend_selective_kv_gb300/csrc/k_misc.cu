@@ -114,18 +114,19 @@ __global__ void rerope_kernel(const T* __restrict__ src, T* __restrict__ dst, in
 }
 
 cudaError_t launch_rerope(const Model& m, const void* src, void* dst, int64_t src_rows, int64_t dst_rows, int n_ctx,
-                          int n_chunks, bool copy_v, cudaStream_t s) {
+                          int n_chunks, bool copy_v, cudaStream_t s, int layers) {
     const cb_config& c = m.cfg;
     const int W = c.n_kv_heads * c.head_dim, kvc = copy_v ? 2 : 1;
-    const int64_t items = (int64_t)c.n_layers * kvc * n_ctx * (W / 8);
+    const int L = layers > 0 ? layers : c.n_layers;
+    const int64_t items = (int64_t)L * kvc * n_ctx * (W / 8);
     if (items == 0) return cudaSuccess;
     const int grid = grid_for(items, 256, m.num_sms, 16);
     if (m.bf16)
         rerope_kernel<bf16><<<grid, 256, 0, s>>>((const bf16*)src, (bf16*)dst, src_rows, dst_rows, n_ctx, W,
-                                                 c.head_dim, c.n_layers, kvc, m.chunk_dst, m.delta_cs, n_chunks);
+                                                 c.head_dim, L, kvc, m.chunk_dst, m.delta_cs, n_chunks);
     else
         rerope_kernel<float><<<grid, 256, 0, s>>>((const float*)src, (float*)dst, src_rows, dst_rows, n_ctx, W,
-                                                  c.head_dim, c.n_layers, kvc, m.chunk_dst, m.delta_cs, n_chunks);
+                                                  c.head_dim, L, kvc, m.chunk_dst, m.delta_cs, n_chunks);
     return cudaGetLastError();
 }
 

@@ -181,6 +181,36 @@ cb_status cb_blend_gradual(cb_model* model, const int32_t* tokens, int32_t n_tok
                            void* out_kv, float* out_logits, int32_t* out_selected, float* out_dev, cb_stats* stats,
                            void* stream);
 
+/* Host side of the layer-wise load pipeline (section "位置恢复、KV 存储与加载流水线", Figure 11: while
+ * layer i is recomputed, layer i+1's KV is fetched; before each layer a synchronisation makes sure its
+ * data has arrived). */
+typedef struct {
+    const void* cached_kv_host;  /* host [n_layers][2][n_ctx][n_kv_heads][head_dim] (cfg.dtype): the chunk caches
+                                    in placed order, K still rotated at each chunk's src_pos.  Page-locked
+                                    (pinned) memory, or the copies do not overlap the compute. */
+    void* out_kv_host;           /* host [n_layers][2][n_tokens][n_kv_heads][head_dim] or NULL: each layer's
+                                    blended K/V, copied back as soon as that layer's recomputed rows are stored
+                                    (pinned, as above) */
+    void* copy_stream;           /* cudaStream_t of the host-to-device copies; not the compute stream */
+    void* copy_back_stream;      /* cudaStream_t of the device-to-host copies, or NULL to use copy_stream */
+} cb_layer_io;
+
+/* A blend whose chunk caches stream in from host memory layer by layer (the loading pipeline of
+ * section "位置恢复、KV 存储与加载流水线").  Every layer's cache rows are copied into out_kv (rows
+ * 0..n_ctx-1 of its K and V blocks) on io->copy_stream, in layer order, each followed by an event; the
+ * compute stream waits for layer l's event, re-RoPEs layer l in place and only then computes it, so the
+ * copy of layer l+1 overlaps the recompute of layer l.  With io->out_kv_host set, layer l's blended
+ * K/V (all n_tokens rows) is copied back on io->copy_back_stream once its recomputed rows are stored.
+ *   ratios, n_ratios, out_selected, out_dev: as for cb_blend_gradual (a constant schedule is cb_blend).
+ *   tokens, chunks, out_kv, out_logits, stats: as for cb_blend; out_kv is a device buffer of n_tokens rows.
+ * The call forks the copy streams off `stream` and joins them back: when `stream` has completed, every
+ * copy has too.  Errors: those of cb_blend_gradual, plus CB_ERR_INVALID_ARG for a missing copy stream,
+ * a copy stream equal to `stream`, or chunks without a host cache. */
+cb_status cb_blend_streamed(cb_model* model, const int32_t* tokens, int32_t n_tokens, const cb_layer_io* io,
+                            const cb_chunk* chunks, int32_t n_chunks, const double* ratios, int32_t n_ratios,
+                            void* out_kv, float* out_logits, int32_t* out_selected, float* out_dev, cb_stats* stats,
+                            void* stream);
+
 /* Device status bits recorded by the kernels instead of trapping (cumulative since creation). */
 #define CB_STATUS_BAD_TOKEN    1u  /* a token id outside [0, vocab) was read; its embedding was zeroed */
 #define CB_STATUS_WAIT_TIMEOUT 2u  /* a bounded barrier wait in a tensor-core kernel gave up (~2 s); the
@@ -238,6 +268,20 @@ int32_t cb_profile_read(cb_model* model, cb_kernel_profile* out, int32_t max_ent
 #define CB_STATIC_MAX_CHUNKS 256
 cb_status cb_rerope_static(void* kv, int64_t n_rows, int32_t n_layers, int32_t n_kv_heads, int32_t head_dim,
                            double rope_theta, int32_t dtype, const cb_chunk* chunks, int32_t n_chunks, void* stream);
+
+/* Loading controller (section "位置恢复、KV 存储与加载流水线", Figure 11).  Host arithmetic only.
+ * cb_load_time: T_load = per_token_kv_bytes * n_tokens / throughput (seconds); -1 for a non-positive
+ *   throughput or negative sizes.
+ * cb_controller_ratio: the recompute ratio r whose recompute time r * T_prefill matches T_load, raised
+ *   to the quality floor r_min (the page's r* = 15%) and capped at 1; -1 for negative times or r_min
+ *   outside [0, 1].
+ * cb_pick_storage: among n_devices storage tiers (throughput in bytes/s, cost per GB), the cheapest whose
+ *   T_load does not exceed the recompute time at the floor, r_min * T_prefill (ties to the lower index);
+ *   when none qualifies, the fastest.  Returns the device index, or CB_ERR_INVALID_ARG. */
+double cb_load_time(double per_token_kv_bytes, int64_t n_tokens, double throughput_bytes_per_s);
+double cb_controller_ratio(double t_prefill_s, double t_load_s, double r_min);
+int32_t cb_pick_storage(const double* throughput_bytes_per_s, const double* cost_per_gb, int32_t n_devices,
+                        double per_token_kv_bytes, int64_t n_tokens, double t_prefill_s, double r_min);
 
 /* k = ceil(ratio * n_ctx - 1e-9) clamped to [0, n_ctx]; -1 if ratio is outside [0, 1] or NaN. */
 int32_t cb_selected_count(int32_t n_ctx, double ratio);

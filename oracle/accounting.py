@@ -38,3 +38,15 @@ def controller_ratio(t_prefill_s: float, t_load_s: float, r_min: float = 0.15) -
     but never below the quality floor r* (15% on the page)."""
     r_match = t_load_s / t_prefill_s if t_prefill_s > 0 else 1.0
     return min(1.0, max(r_min, r_match))
+
+
+def pick_storage(devices, per_token_kv_bytes: float, n_tokens: int, t_prefill_s: float, r_min: float = 0.15) -> int:
+    """Storage tier choice of the loading controller: among the tiers whose load time stays within the
+    recompute time at the quality floor (r_min * T_prefill), the cheapest per GB; when none does, fall
+    back to the fastest ("SSD is cheaper than memory: use it when its bandwidth suffices, else memory").
+    ``devices`` is a list of (throughput bytes/s, cost per GB); returns an index (ties: the first)."""
+    budget = r_min * t_prefill_s
+    ok = [i for i, (bw, _) in enumerate(devices) if load_time(per_token_kv_bytes, n_tokens, bw) <= budget]
+    if ok:
+        return min(ok, key=lambda i: (devices[i][1], i))
+    return max(range(len(devices)), key=lambda i: (devices[i][0], -i))

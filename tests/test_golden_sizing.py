@@ -35,3 +35,28 @@ def test_controller_ratio_floor_and_match():
     assert accounting.controller_ratio(t_prefill_s=1.0, t_load_s=0.05) == 0.15
     # slow storage: recompute up to the load time for free
     assert abs(accounting.controller_ratio(t_prefill_s=1.0, t_load_s=0.4) - 0.4) < 1e-12
+
+
+def test_controller_on_the_pages_per_layer_examples():
+    """The page's two per-layer examples run through the controller rule.  Llama-7B, 4K context: 15%
+    recompute takes about 3 ms per layer (so a full layer about 20 ms) while an NVMe layer load takes
+    about 16 ms, so recomputing up to 80% stays hidden behind the load.  Llama-70B: about 7 ms per layer
+    at 15% (about 46.7 ms full) against a 4 ms load, so the ratio stays at the 15% floor and part of the
+    recompute is exposed, as the page says."""
+    r7 = accounting.controller_ratio(t_prefill_s=0.003 / 0.15, t_load_s=0.016)
+    assert abs(r7 - 0.8) < 1e-12 and 0.8 * (0.003 / 0.15) >= 0.016 - 1e-15
+    r70 = accounting.controller_ratio(t_prefill_s=0.007 / 0.15, t_load_s=0.004)
+    assert r70 == 0.15 and 0.15 * (0.007 / 0.15) > 0.004
+
+
+def test_storage_choice_prefers_cheap_tiers_that_keep_up():
+    """SSD is cheaper than memory and is used when its load time stays within the 15% recompute time;
+    otherwise the controller falls back to memory.  Per layer, with the page's 7B numbers the NVMe load
+    (16 ms) exceeds the 3 ms recompute, so memory is chosen; with the 70B numbers (4 ms load against
+    7 ms) the cheaper tier qualifies."""
+    # tiers as (throughput bytes/s, cost per GB): memory fast and dear, NVMe slow and cheap;
+    # throughputs chosen so one layer (per_token bytes x tokens) loads in the page's times
+    layer_bytes = 1.0e6
+    mem, nvme7, nvme70 = (layer_bytes / 0.001, 3.0), (layer_bytes / 0.016, 0.1), (layer_bytes / 0.004, 0.1)
+    assert accounting.pick_storage([mem, nvme7], layer_bytes, 1, t_prefill_s=0.003 / 0.15) == 0
+    assert accounting.pick_storage([mem, nvme70], layer_bytes, 1, t_prefill_s=0.007 / 0.15) == 1

@@ -172,3 +172,29 @@ def test_llama8b_3k_gradual(cb):
     caches = workload.synthetic_cache(shape, seed, spec.n_ctx, workload.kv_std(shape))
     r = tg.compare_gradual(cb, shape, w, req.tokens, caches, req.chunks, ratios, "bf16")
     print(f"8B 3K gradual: {r}")
+
+
+def test_llama8b_3k_streamed_matches_device_resident(cb):
+    """The 8B-shape 3K blend with its chunk caches streamed from pinned host memory layer by layer: K/V
+    and logits within the parity tolerances of the device-resident blend (the residual GEMMs add split-K
+    partial sums in a run-dependent order), and the copied-back K/V equal to the device K/V."""
+    spec = workload.WORKLOADS["llama8b-3k"]
+    shape, seed, ratio = spec.shape, spec.seeds[0], spec.ratios[0]
+    w = workload.make_weights(shape, seed)
+    req = workload.make_request(spec, seed, ratio)
+    caches = workload.synthetic_cache(shape, seed, spec.n_ctx, workload.kv_std(shape))
+    model = cb.BlendModel(shape.as_dict(), w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks)
+    host = torch.from_numpy(caches.view(np.int16)).view(torch.bfloat16).pin_memory()
+    tokens = torch.from_numpy(req.tokens).cuda()
+    a = model.blend(tokens, host.cuda(), req.chunks, ratio)
+    kv_host = torch.empty(a["out_kv"].shape, dtype=torch.bfloat16).pin_memory()
+    b = model.blend_streamed(tokens, host, req.chunks, (ratio,) * (shape.n_layers - 1), out_kv_host=kv_host)
+    torch.cuda.synchronize()
+    assert model.status() == 0
+    assert torch.equal(kv_host, b["out_kv"].cpu())
+    ka, kb = parity.bf16_to_f64(a["out_kv"]), parity.bf16_to_f64(b["out_kv"])
+    # 2e-2, or one bf16 step at the value (two roundings of sums taken in different orders)
+    ulp = np.ldexp(1.0, np.frexp(np.maximum(np.abs(ka), 1e-30))[1] - 8)
+    assert np.all(np.abs(ka - kb) <= np.maximum(2e-2, ulp))
+    assert np.max(np.abs(parity.bf16_to_f64(a["logits"]) - parity.bf16_to_f64(b["logits"]))) <= 3e-2
+    model.close()

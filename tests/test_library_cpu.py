@@ -97,3 +97,26 @@ def test_calls_reject_null_model(lib):
     with pytest.raises(cb.CacheBlendError):
         cb.cb_rerope(0, 4096, 10, [(0, 0, 10)], stream=0)
     assert lib.cb_model_destroy(None) == cb.CB_OK
+
+
+def test_loading_controller_matches_oracle(lib):
+    """The library's loading-controller arithmetic against the oracle's (host code, no GPU)."""
+    from oracle import accounting
+    for ptk in (131072.0, 524288.0, 163840.0):
+        for n in (0, 512, 3072, 4096, 32768):
+            for bw in (4.8e9, 5153960755.2, 2.5e10, 4.5e11):
+                assert cb.cb_load_time(ptk, n, bw) == accounting.load_time(ptk, n, bw)
+    for tp in (0.0, 0.02, 0.4667, 1.0, 3.0):
+        for tl in (0.0, 0.004, 0.016, 0.05, 0.4, 2.0, 5.0):
+            for rmin in (0.0, 0.15, 0.3):
+                assert cb.cb_controller_ratio(tp, tl, rmin) == accounting.controller_ratio(tp, tl, rmin), (tp, tl, rmin)
+    assert cb.cb_load_time(1.0, 1, 0.0) == -1.0
+    assert cb.cb_controller_ratio(1.0, 0.1, 1.5) == -1.0
+    tiers = [(2.0e11, 3.0), (4.8e9, 0.1), (2.5e10, 0.5), (2.5e10, 0.5)]
+    for n in (512, 4096, 32768):
+        for tp in (0.05, 0.5, 5.0, 50.0):
+            for rmin in (0.05, 0.15, 1.0):
+                assert cb.cb_pick_storage(tiers, 524288.0, n, tp, rmin) == \
+                    accounting.pick_storage(tiers, 524288.0, n, tp, rmin), (n, tp, rmin)
+    with pytest.raises(cb.CacheBlendError):
+        cb.cb_pick_storage([], 1.0, 1, 1.0)
