@@ -220,6 +220,8 @@ def main():
     ap.add_argument("--ratio", type=float, default=None)
     ap.add_argument("--gradual", action="store_true",
                     help="gradual filtering: 2r at the check layer, shrinking to r over the next 4 layers")
+    ap.add_argument("--paged", type=int, default=0, metavar="P",
+                    help="keep the chunk caches and the blended K/V in a paged pool of P-row pages (shuffled block table)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-profile", action="store_true")
@@ -286,7 +288,24 @@ def main():
 
     stream = torch.cuda.Stream(dev)
 
+    paged = None
+    if args.paged:
+        P = args.paged
+        nb = (n + P - 1) // P
+        n_pages = nb + 16
+        table = torch.from_numpy(np.random.default_rng(seed).permutation(n_pages)[:nb].astype(np.int32)).to(dev)
+        pool = torch.empty((shape.n_layers, 2, n_pages * P, shape.n_kv_heads, shape.head_dim), dtype=cached.dtype,
+                           device=dev)
+        cb.cb_kv_scatter_pages(model.handle, cached, spec.n_ctx, pool, n_pages, P, table)
+        torch.cuda.synchronize()
+        paged = (pool, n_pages, P, table)
+
     def blend_call(tok, cache, st=False):
+        if paged is not None:
+            pool, n_pages, P, table = paged
+            return cb.cb_blend_paged(model.handle, tok, n, pool, n_pages, P, table, table, req.chunks,
+                                     schedule or (ratio,) * (shape.n_layers - 1), out_kv, logits, sel, None, stream,
+                                     stats=st)
         if schedule:
             return cb.cb_blend_gradual(model.handle, tok, n, cache, req.chunks, schedule, out_kv, logits, sel, None,
                                        stream, stats=st)
@@ -387,7 +406,7 @@ def main():
     # (overlapping the recompute of earlier layers) and copies every finished layer back on another.
     # Serial (for comparison): copy everything in, blend, copy everything out.
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.paged:
         h_tokens = torch.from_numpy(req.tokens).pin_memory()
         h_cached = cached.cpu().pin_memory()
         h_out = torch.empty(out_kv.shape, dtype=out_kv.dtype).pin_memory()
@@ -457,6 +476,8 @@ def main():
                            "seed": seed, "parallelism": "replicas" if ws > 1 else "single",
                            "schedule": ("gradual filtering, per-layer ratios " + ",".join(f"{r:.4g}" for r in schedule))
                            if schedule else "one selection at the check layer",
+                           "kv_layout": (f"paged pool, {args.paged}-row pages, shuffled block table (read and "
+                                         "written in place)") if args.paged else "contiguous",
                            "l2": "inputs exceed L2 (16 GB weights, 384 MiB caches) and a 256 MiB buffer is "
                                  "rewritten between steps outside the timed events",
                            "timing": ("CUDA events around each step on the launching stream, summed over the steps; "

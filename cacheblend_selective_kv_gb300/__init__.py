@@ -24,7 +24,10 @@ CB_PREC_SPLIT, CB_PREC_BF16 = 0, 1
 CB_MAX_CHUNKS = 1024
 EXPORTED = ("cb_model_create", "cb_model_destroy", "cb_rerope", "cb_blend", "cb_blend_gradual", "cb_blend_streamed",
             "cb_selected_count", "cb_last_error", "cb_profile_enable", "cb_profile_read", "cb_model_status",
-            "cb_rerope_static", "cb_model_diag", "cb_load_time", "cb_controller_ratio", "cb_pick_storage")
+            "cb_rerope_static", "cb_model_diag", "cb_load_time", "cb_controller_ratio", "cb_pick_storage",
+            "cb_blend_paged", "cb_kv_gather_pages", "cb_kv_scatter_pages", "cb_pages_create", "cb_pages_destroy",
+            "cb_pages_alloc", "cb_pages_retain", "cb_pages_release", "cb_pages_plan_write", "cb_pages_count",
+            "cb_pages_free")
 CB_STATIC_MAX_CHUNKS = 256
 CB_STATUS_BAD_TOKEN, CB_STATUS_WAIT_TIMEOUT, CB_STATUS_BAD_ROW = 1, 2, 4
 
@@ -60,6 +63,11 @@ class CbStats(ctypes.Structure):
 class CbLayerIO(ctypes.Structure):
     _fields_ = [("cached_kv_host", ctypes.c_void_p), ("out_kv_host", ctypes.c_void_p), ("copy_stream", ctypes.c_void_p),
                 ("copy_back_stream", ctypes.c_void_p)]
+
+
+class CbPagedKV(ctypes.Structure):
+    _fields_ = [("pool", ctypes.c_void_p), ("n_pages", ctypes.c_int64), ("page_size", ctypes.c_int32),
+                ("src_table", ctypes.c_void_p), ("dst_table", ctypes.c_void_p)]
 
 
 class CbKernelProfile(ctypes.Structure):
@@ -111,6 +119,30 @@ def lib() -> ctypes.CDLL:
         L.cb_pick_storage.restype = i32
         L.cb_pick_storage.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double), i32,
                                       ctypes.c_double, i64, ctypes.c_double, ctypes.c_double]
+        L.cb_blend_paged.restype = ctypes.c_int
+        L.cb_blend_paged.argtypes = [vp, vp, i32, ctypes.POINTER(CbPagedKV), ctypes.POINTER(CbChunk), i32,
+                                     ctypes.POINTER(ctypes.c_double), i32, vp, vp, vp, vp, ctypes.POINTER(CbStats), vp]
+        L.cb_kv_gather_pages.restype = ctypes.c_int
+        L.cb_kv_gather_pages.argtypes = [vp, ctypes.POINTER(CbPagedKV), i32, vp, vp]
+        L.cb_kv_scatter_pages.restype = ctypes.c_int
+        L.cb_kv_scatter_pages.argtypes = [vp, vp, i32, ctypes.POINTER(CbPagedKV), vp]
+        ip = ctypes.POINTER(ctypes.c_int32)
+        L.cb_pages_create.restype = ctypes.c_int
+        L.cb_pages_create.argtypes = [i64, ctypes.POINTER(vp)]
+        L.cb_pages_destroy.restype = ctypes.c_int
+        L.cb_pages_destroy.argtypes = [vp]
+        L.cb_pages_alloc.restype = ctypes.c_int
+        L.cb_pages_alloc.argtypes = [vp, i32, ip]
+        L.cb_pages_retain.restype = ctypes.c_int
+        L.cb_pages_retain.argtypes = [vp, ip, i32]
+        L.cb_pages_release.restype = ctypes.c_int
+        L.cb_pages_release.argtypes = [vp, ip, i32]
+        L.cb_pages_plan_write.restype = i32
+        L.cb_pages_plan_write.argtypes = [vp, ip, i32, ip]
+        L.cb_pages_count.restype = i32
+        L.cb_pages_count.argtypes = [vp, i32]
+        L.cb_pages_free.restype = i64
+        L.cb_pages_free.argtypes = [vp]
         L.cb_selected_count.restype = i32
         L.cb_selected_count.argtypes = [i32, ctypes.c_double]
         L.cb_profile_enable.restype = ctypes.c_int
@@ -238,6 +270,84 @@ def cb_blend_streamed(handle: int, tokens, n_tokens: int, cached_kv_host, chunks
     if stats:
         return {f: getattr(st, f) for f, _ in CbStats._fields_}
     return None
+
+
+def _paged(pool, n_pages, page_size, src_table=None, dst_table=None):
+    return CbPagedKV(_ptr(pool) or None, int(n_pages), int(page_size), _ptr(src_table) or None, _ptr(dst_table) or None)
+
+
+def cb_blend_paged(handle: int, tokens, n_tokens: int, pool, n_pages: int, page_size: int, src_table, dst_table, chunks,
+                   ratios, work_kv, out_logits, out_selected=None, out_dev=None, stream=None, stats: bool = False):
+    """Blend over a paged pool: chunk caches read through src_table, blended K/V written through dst_table
+    (device int32 tables); work_kv is the caller's contiguous working copy."""
+    st = CbStats()
+    r = (ctypes.c_double * max(1, len(ratios)))(*[float(x) for x in ratios])
+    pg = _paged(pool, n_pages, page_size, src_table, dst_table)
+    _check(lib().cb_blend_paged(handle, _ptr(tokens), int(n_tokens), ctypes.byref(pg), _chunks(chunks), len(chunks),
+                                r, len(ratios), _ptr(work_kv), _ptr(out_logits), _ptr(out_selected), _ptr(out_dev),
+                                ctypes.byref(st) if stats else None, _stream(stream)))
+    if stats:
+        return {f: getattr(st, f) for f, _ in CbStats._fields_}
+    return None
+
+
+def cb_kv_gather_pages(handle: int, pool, n_pages: int, page_size: int, table, n_rows: int, out_kv, stream=None):
+    pg = _paged(pool, n_pages, page_size, table, None)
+    _check(lib().cb_kv_gather_pages(handle, ctypes.byref(pg), int(n_rows), _ptr(out_kv), _stream(stream)))
+
+
+def cb_kv_scatter_pages(handle: int, kv, n_rows: int, pool, n_pages: int, page_size: int, table, stream=None):
+    pg = _paged(pool, n_pages, page_size, None, table)
+    _check(lib().cb_kv_scatter_pages(handle, _ptr(kv), int(n_rows), ctypes.byref(pg), _stream(stream)))
+
+
+class Pages:
+    """Host-side page bookkeeping of a pool (cb_pages_*): reference counts, allocation, copy-on-write plans."""
+
+    def __init__(self, n_pages: int):
+        h = ctypes.c_void_p()
+        _check(lib().cb_pages_create(int(n_pages), ctypes.byref(h)))
+        self.h = h.value
+
+    @staticmethod
+    def _arr(ids):
+        return (ctypes.c_int32 * max(1, len(ids)))(*[int(i) for i in ids])
+
+    def alloc(self, n: int) -> list:
+        a = (ctypes.c_int32 * max(1, n))()
+        _check(lib().cb_pages_alloc(self.h, int(n), a))
+        return [a[i] for i in range(n)]
+
+    def retain(self, ids):
+        _check(lib().cb_pages_retain(self.h, self._arr(ids), len(ids)))
+
+    def release(self, ids):
+        _check(lib().cb_pages_release(self.h, self._arr(ids), len(ids)))
+
+    def plan_write(self, table) -> tuple:
+        """(dst table, number of copy-on-write pages)."""
+        d = (ctypes.c_int32 * max(1, len(table)))()
+        n = int(lib().cb_pages_plan_write(self.h, self._arr(table), len(table), d))
+        if n < 0:
+            raise CacheBlendError(n, cb_last_error())
+        return [d[i] for i in range(len(table))], n
+
+    def count(self, i: int) -> int:
+        return int(lib().cb_pages_count(self.h, int(i)))
+
+    def free(self) -> int:
+        return int(lib().cb_pages_free(self.h))
+
+    def close(self):
+        if self.h:
+            lib().cb_pages_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def cb_load_time(per_token_kv_bytes: float, n_tokens: int, throughput_bytes_per_s: float) -> float:

@@ -232,7 +232,7 @@ cb_status check_chunks(const cb_chunk* chunks, int32_t n_chunks, int max_chunks,
 
 const char* const kClassName[K_NCLASS] = {"rerope", "embed", "rmsnorm", "gemm_q", "gemm_kv", "gemm_qkv", "gemm_o",
                                          "gemm_gateup", "gemm_down", "attention", "deviation", "topk",
-                                         "gather_scatter", "logits", "delta_table", "refilter"};
+                                         "gather_scatter", "logits", "delta_table", "refilter", "pages"};
 
 // Enqueues launches on one stream; counts them and, when profiling is on, brackets each with events.
 struct Sched {
@@ -362,7 +362,7 @@ namespace {
 cb_status blend_impl(Model& m, const int32_t* tokens, int32_t n_tokens, const void* cached_kv, const ChunkTable& t,
                      int n_chunks, int n_ctx, const std::vector<int>& ks, void* out_kv, float* out_logits,
                      int32_t* out_selected, float* out_dev, cb_stats* stats, cudaStream_t s,
-                     const cb_layer_io* io = nullptr) {
+                     const cb_layer_io* io = nullptr, const cb_paged_kv* pg = nullptr, int page_shift = 0) {
     const cb_config& c = m.cfg;
     const size_t es = act_size(m);
     const int L = c.n_layers, d = c.d_model, nq = c.n_heads * c.head_dim, nkv = c.n_kv_heads * c.head_dim;
@@ -405,6 +405,13 @@ cb_status blend_impl(Model& m, const int32_t* tokens, int32_t n_tokens, const vo
             }
             S.k(K_DELTA, 0, 0, [&] { return launch_delta_table(m, t, s); });
         }
+    } else if (pg && n_chunks > 0) {
+        // paged: the chunk caches are read from their pool pages, re-rotated and placed in the contiguous
+        // working copy (out_kv) in one pass; the pool is written back at the end
+        S.k(K_DELTA, 0, 0, [&] { return launch_delta_table(m, t, s); });
+        S.k(K_REROPE, 0, 4.0 * L * n_ctx * row,
+            [&] { return launch_rerope(m, pg->pool, out_kv, pg->n_pages * (int64_t)pg->page_size, N, n_ctx, n_chunks,
+                                       true, s, 0, pg->src_table, page_shift); });
     } else if (n_chunks > 0) {
         S.k(K_DELTA, 0, 0, [&] { return launch_delta_table(m, t, s); });
         S.k(K_REROPE, 0, (inplace ? 2.0 : 4.0) * L * n_ctx * row,
@@ -580,6 +587,11 @@ cb_status blend_impl(Model& m, const int32_t* tokens, int32_t n_tokens, const vo
     S.k(K_LOGITS, 2.0 * d * c.vocab, (double)c.vocab * d * es,
         [&] { return launch_logits(m, h_last, out_logits, s); });
 
+    if (pg) {   // every row of the blended K/V into its destination page (a copy-on-write page when shared)
+        S.k(K_PAGES, 0, 4.0 * L * N * row,
+            [&] { return launch_page_copy(m, out_kv, N, nullptr, pg->pool, pg->n_pages * (int64_t)pg->page_size,
+                                          pg->dst_table, page_shift, N, s); });
+    }
     if (io) {   // join: the compute stream completes only after every copy
         io_check(cudaEventRecord(m.io_ev[2 * L + 1], cs));
         io_check(cudaStreamWaitEvent(s, m.io_ev[2 * L + 1], 0));
@@ -689,6 +701,76 @@ cb_status cb_blend_streamed(cb_model* mp, const int32_t* tokens, int32_t n_token
     }
     return blend_impl(m, tokens, n_tokens, out_kv, t, n_chunks, n_ctx, ks, out_kv, out_logits, out_selected, out_dev,
                       stats, (cudaStream_t)stream, io);
+}
+
+static cb_status check_pages(const Model& m, const cb_paged_kv* pg, int& shift) {
+    if (!pg || !pg->pool) return fail(CB_ERR_INVALID_ARG, "paged K/V: null pool");
+    if (pg->page_size < 16 || (pg->page_size & (pg->page_size - 1)))
+        return fail(CB_ERR_INVALID_ARG, "paged K/V: page_size %d is not a power of two >= 16", pg->page_size);
+    if (pg->n_pages <= 0 || pg->n_pages * (int64_t)pg->page_size > ((int64_t)1 << 40))
+        return fail(CB_ERR_INVALID_ARG, "paged K/V: bad n_pages");
+    if ((uintptr_t)pg->pool % 16) return fail(CB_ERR_INVALID_ARG, "paged K/V: pool not 16-byte aligned");
+    shift = 0;
+    while ((1 << shift) < pg->page_size) ++shift;
+    (void)m;
+    return CB_OK;
+}
+
+cb_status cb_blend_paged(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const cb_paged_kv* pg,
+                         const cb_chunk* chunks, int32_t n_chunks, const double* ratios, int32_t n_ratios,
+                         void* work_kv, float* out_logits, int32_t* out_selected, float* out_dev, cb_stats* stats,
+                         void* stream) {
+    g_err[0] = 0;
+    if (!mp) return fail(CB_ERR_INVALID_ARG, "cb_blend_paged: null model");
+    Model& m = *mp;
+    const int L = m.cfg.n_layers;
+    int shift = 0;
+    cb_status st = check_pages(m, pg, shift);
+    if (st != CB_OK) return st;
+    if (!pg->dst_table || (n_chunks > 0 && !pg->src_table))
+        return fail(CB_ERR_INVALID_ARG, "cb_blend_paged: missing block table");
+    if (!ratios || n_ratios != L - 1)
+        return fail(CB_ERR_INVALID_ARG, "cb_blend_paged: need n_layers - 1 = %d ratios (got %d)", L - 1, n_ratios);
+    for (int i = 0; i < n_ratios; ++i)
+        if (!(ratios[i] >= 0.0 && ratios[i] <= 1.0)) return fail(CB_ERR_INVALID_ARG, "ratio of layer %d outside [0, 1]", i + 1);
+    ChunkTable t;
+    int n_ctx = 0;
+    st = check_blend(m, tokens, n_tokens, work_kv, chunks, n_chunks, work_kv, out_logits, t, n_ctx);
+    if (st != CB_OK) return st;
+    std::vector<int> ks(L, 0);
+    for (int l = 1; l < L; ++l) {
+        ks[l] = cb_selected_count(n_ctx, ratios[l - 1]);
+        if (l >= 2 && ks[l] > ks[l - 1])
+            return fail(CB_ERR_INVALID_ARG, "layer %d keeps %d rows, more than layer %d's %d: the sets must be nested",
+                        l, ks[l], l - 1, ks[l - 1]);
+    }
+    ks[0] = ks[1];
+    return blend_impl(m, tokens, n_tokens, nullptr, t, n_chunks, n_ctx, ks, work_kv, out_logits, out_selected, out_dev,
+                      stats, (cudaStream_t)stream, nullptr, pg, shift);
+}
+
+cb_status cb_kv_gather_pages(cb_model* mp, const cb_paged_kv* pg, int32_t n_rows, void* out_kv, void* stream) {
+    g_err[0] = 0;
+    if (!mp) return fail(CB_ERR_INVALID_ARG, "cb_kv_gather_pages: null model");
+    int shift = 0;
+    cb_status st = check_pages(*mp, pg, shift);
+    if (st != CB_OK) return st;
+    if (!pg->src_table || !out_kv || n_rows < 0) return fail(CB_ERR_INVALID_ARG, "cb_kv_gather_pages: bad arguments");
+    cudaError_t e = launch_page_copy(*mp, pg->pool, pg->n_pages * (int64_t)pg->page_size, pg->src_table, out_kv, n_rows,
+                                     nullptr, shift, n_rows, (cudaStream_t)stream);
+    return e == cudaSuccess ? CB_OK : fail(CB_ERR_CUDA, "cb_kv_gather_pages: %s", cudaGetErrorString(e));
+}
+
+cb_status cb_kv_scatter_pages(cb_model* mp, const void* kv, int32_t n_rows, const cb_paged_kv* pg, void* stream) {
+    g_err[0] = 0;
+    if (!mp) return fail(CB_ERR_INVALID_ARG, "cb_kv_scatter_pages: null model");
+    int shift = 0;
+    cb_status st = check_pages(*mp, pg, shift);
+    if (st != CB_OK) return st;
+    if (!pg->dst_table || !kv || n_rows < 0) return fail(CB_ERR_INVALID_ARG, "cb_kv_scatter_pages: bad arguments");
+    cudaError_t e = launch_page_copy(*mp, kv, n_rows, nullptr, pg->pool, pg->n_pages * (int64_t)pg->page_size,
+                                     pg->dst_table, shift, n_rows, (cudaStream_t)stream);
+    return e == cudaSuccess ? CB_OK : fail(CB_ERR_CUDA, "cb_kv_scatter_pages: %s", cudaGetErrorString(e));
 }
 
 cb_status cb_blend_gradual(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const void* cached_kv,

@@ -99,7 +99,7 @@ struct TcMaps;   // tensor maps of the tensor-core path (defined in gemm_tc.cu)
 
 // kernel classes for the opt-in per-class timing
 enum KClass { K_REROPE, K_EMBED, K_RMSNORM, K_GEMM_Q, K_GEMM_KV, K_GEMM_QKV, K_GEMM_O, K_GEMM_GATEUP, K_GEMM_DOWN,
-              K_ATTENTION, K_DEVIATION, K_TOPK, K_GATHER, K_LOGITS, K_DELTA, K_REFILTER, K_NCLASS };
+              K_ATTENTION, K_DEVIATION, K_TOPK, K_GATHER, K_LOGITS, K_DELTA, K_REFILTER, K_PAGES, K_NCLASS };
 
 struct Profile {
     bool on = false;
@@ -173,7 +173,11 @@ struct ChunkTable {
 
 cudaError_t launch_delta_table(const Model& m, const ChunkTable& t, cudaStream_t s);
 cudaError_t launch_rerope(const Model& m, const void* src, void* dst, int64_t src_rows, int64_t dst_rows,
-                          int n_ctx, int n_chunks, bool copy_v, cudaStream_t s, int layers = 0);
+                          int n_ctx, int n_chunks, bool copy_v, cudaStream_t s, int layers = 0,
+                          const int* src_pages = nullptr, int page_shift = 0);
+// paged pool <-> contiguous rows (k_paged.cu); a NULL table is the identity
+cudaError_t launch_page_copy(const Model& m, const void* src, int64_t src_rows, const int* src_pages, void* dst,
+                             int64_t dst_rows, const int* dst_pages, int page_shift, int n_rows, cudaStream_t s);
 cudaError_t launch_embed(const Model& m, const int* tokens, int n, float* h, cudaStream_t s);
 cudaError_t launch_rmsnorm(const Model& m, const float* h, const void* g, void* out, void* out_lo, int n,
                            cudaStream_t s);

@@ -70,7 +70,9 @@ cudaError_t launch_delta_table(const Model& m, const ChunkTable& t, cudaStream_t
 
 // ------------------------------------------------------------------------------------------------
 // Re-RoPE placement: dst K row j = R_{delta(chunk of j)} src K row j; dst V row j = src V row j.
-// src and dst are [L][2][rows][W]; they may be the same buffer with the same row count.
+// src and dst are [L][2][rows][W]; they may be the same buffer with the same row count.  With a page
+// table, src row j is row (src_pages[j / P] * P + j % P) of a paged pool (P = 2^page_shift); a page id
+// outside [0, n_pages) is recorded in the status word and its rows are skipped.
 // ------------------------------------------------------------------------------------------------
 __device__ __forceinline__ int chunk_of(const int* dst, int n, int j) {
     int lo = 0, hi = n - 1;
@@ -84,7 +86,8 @@ __device__ __forceinline__ int chunk_of(const int* dst, int n, int j) {
 template <typename T>
 __global__ void rerope_kernel(const T* __restrict__ src, T* __restrict__ dst, int64_t src_rows, int64_t dst_rows,
                               int n_ctx, int W, int hd, int L, int kv_count, const int* __restrict__ cdst,
-                              const float2* __restrict__ cs, int n_chunks) {
+                              const float2* __restrict__ cs, int n_chunks, const int* __restrict__ src_pages,
+                              int page_shift, int64_t n_pages, unsigned* status) {
     const int W8 = W / 8, half = hd / 2;
     const int64_t per_lk = (int64_t)n_ctx * W8;
     const int64_t total = (int64_t)L * kv_count * per_lk;
@@ -94,7 +97,16 @@ __global__ void rerope_kernel(const T* __restrict__ src, T* __restrict__ dst, in
         const int rem = (int)(it - (int64_t)lk * per_lk);
         const int j = rem / W8, e = (rem - j * W8) * 8;
         const int layer = lk / kv_count, kv = lk - layer * kv_count;
-        const T* sp = src + (((int64_t)layer * 2 + kv) * src_rows + j) * W + e;
+        int64_t sj = j;
+        if (src_pages) {
+            const int pg = src_pages[j >> page_shift];
+            if (pg < 0 || pg >= n_pages) {
+                atomicOr(status, ST_BAD_ROW);
+                continue;
+            }
+            sj = ((int64_t)pg << page_shift) + (j & ((1 << page_shift) - 1));
+        }
+        const T* sp = src + (((int64_t)layer * 2 + kv) * src_rows + sj) * W + e;
         T* dp = dst + (((int64_t)layer * 2 + kv) * dst_rows + j) * W + e;
         float f[8];
         Vec8<T>::load(sp, f);
@@ -114,7 +126,7 @@ __global__ void rerope_kernel(const T* __restrict__ src, T* __restrict__ dst, in
 }
 
 cudaError_t launch_rerope(const Model& m, const void* src, void* dst, int64_t src_rows, int64_t dst_rows, int n_ctx,
-                          int n_chunks, bool copy_v, cudaStream_t s, int layers) {
+                          int n_chunks, bool copy_v, cudaStream_t s, int layers, const int* src_pages, int page_shift) {
     const cb_config& c = m.cfg;
     const int W = c.n_kv_heads * c.head_dim, kvc = copy_v ? 2 : 1;
     const int L = layers > 0 ? layers : c.n_layers;
@@ -123,10 +135,12 @@ cudaError_t launch_rerope(const Model& m, const void* src, void* dst, int64_t sr
     const int grid = grid_for(items, 256, m.num_sms, 16);
     if (m.bf16)
         rerope_kernel<bf16><<<grid, 256, 0, s>>>((const bf16*)src, (bf16*)dst, src_rows, dst_rows, n_ctx, W,
-                                                 c.head_dim, L, kvc, m.chunk_dst, m.delta_cs, n_chunks);
+                                                 c.head_dim, L, kvc, m.chunk_dst, m.delta_cs, n_chunks, src_pages,
+                                                 page_shift, src_rows >> page_shift, m.status);
     else
         rerope_kernel<float><<<grid, 256, 0, s>>>((const float*)src, (float*)dst, src_rows, dst_rows, n_ctx, W,
-                                                  c.head_dim, L, kvc, m.chunk_dst, m.delta_cs, n_chunks);
+                                                  c.head_dim, L, kvc, m.chunk_dst, m.delta_cs, n_chunks, src_pages,
+                                                  page_shift, src_rows >> page_shift, m.status);
     return cudaGetLastError();
 }
 

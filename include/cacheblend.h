@@ -211,6 +211,66 @@ cb_status cb_blend_streamed(cb_model* model, const int32_t* tokens, int32_t n_to
                             void* out_kv, float* out_logits, int32_t* out_selected, float* out_dev, cb_stats* stats,
                             void* stream);
 
+/* Paged K/V (section "和前缀缓存、PagedAttention 的分工": find each chunk's physical blocks, assemble the
+ * request's block table, write the recomputed K/V back to the right physical place, copy-on-write for
+ * shared blocks, writes split at page boundaries).
+ * Pool layout: device [n_layers][2][n_pages * page_size][n_kv_heads][head_dim] (cfg.dtype): page p holds
+ * rows p*page_size .. p*page_size+page_size-1 of every (layer, K|V) block.  Logical row j of a block table
+ * t is pool row t[j / page_size] * page_size + j % page_size.  Tables are DEVICE int32 arrays; a page id
+ * outside [0, n_pages) is recorded as CB_STATUS_BAD_ROW and its rows are skipped. */
+typedef struct {
+    void* pool;                  /* device pool, 16-byte aligned */
+    int64_t n_pages;
+    int32_t page_size;           /* rows per page: a power of two >= 16 */
+    const int32_t* src_table;    /* device, ceil(rows / page_size) entries: where the rows are read from */
+    const int32_t* dst_table;    /* device, ceil(rows / page_size) entries: where the rows are written to */
+} cb_paged_kv;
+
+/* A blend whose chunk caches and blended K/V live in a paged pool.  src_table maps the n_ctx context rows
+ * (the chunk caches in placed order, K still rotated at each chunk's src_pos) to their pages; dst_table
+ * maps all n_tokens rows of the blended K/V to the pages that receive it.  A block whose page is shared
+ * with other requests gets a fresh page in dst_table (copy-on-write: the shared page is only read); a
+ * private block may use the same page in both tables (in place).  The chunk caches are read from their
+ * pages, re-rotated and placed into work_kv in one pass, the blend runs there, and every row is then
+ * written to its destination page.
+ *   work_kv      device [n_layers][2][n_tokens][n_kv_heads][head_dim]: the contiguous working copy (the
+ *                caller's memory; holds the blended K/V on return as well).
+ *   ratios, n_ratios, out_selected, out_dev: as for cb_blend_gradual (a constant schedule is cb_blend).
+ *   tokens, chunks, out_logits, stats: as for cb_blend.  Async on `stream`; no allocation.
+ * Errors: those of cb_blend_gradual, plus CB_ERR_INVALID_ARG for a bad pool, page size or missing table. */
+cb_status cb_blend_paged(cb_model* model, const int32_t* tokens, int32_t n_tokens, const cb_paged_kv* paged,
+                         const cb_chunk* chunks, int32_t n_chunks, const double* ratios, int32_t n_ratios,
+                         void* work_kv, float* out_logits, int32_t* out_selected, float* out_dev, cb_stats* stats,
+                         void* stream);
+
+/* Paged <-> contiguous conversion of n_rows rows of every (layer, K|V) block, in the model's layout:
+ * gather reads the pool through src_table into out_kv [n_layers][2][n_rows][n_kv_heads][head_dim];
+ * scatter writes kv (same layout) into the pool through dst_table.  Async on `stream`. */
+cb_status cb_kv_gather_pages(cb_model* model, const cb_paged_kv* paged, int32_t n_rows, void* out_kv, void* stream);
+cb_status cb_kv_scatter_pages(cb_model* model, const void* kv, int32_t n_rows, const cb_paged_kv* paged, void* stream);
+
+/* Host-side page bookkeeping for a pool (reference counts, allocation, copy-on-write planning); host memory
+ * only, no CUDA calls.  A page is free at count 0.
+ *   cb_pages_create   n_pages pages, all free.
+ *   cb_pages_alloc    n free pages (lowest ids first), each with count 1, into ids; CB_ERR_OOM (nothing
+ *                     taken) when fewer are free.
+ *   cb_pages_retain   count += 1 for each id (another request shares the page).
+ *   cb_pages_release  count -= 1 for each id (a page reaching 0 is free again).
+ *   cb_pages_plan_write  for a request about to write its blocks table[0..n): a block whose page is shared
+ *                     (count > 1) gets a fresh page in dst (its count 1) and drops its reference to the
+ *                     shared one; a private block keeps its page.  Returns the number of copy-on-write
+ *                     pages, or CB_ERR_OOM with nothing changed.
+ *   cb_pages_count    the reference count of a page (-1 for a bad id). */
+typedef struct cb_pages cb_pages;
+cb_status cb_pages_create(int64_t n_pages, cb_pages** out);
+cb_status cb_pages_destroy(cb_pages* pages);
+cb_status cb_pages_alloc(cb_pages* pages, int32_t n, int32_t* ids);
+cb_status cb_pages_retain(cb_pages* pages, const int32_t* ids, int32_t n);
+cb_status cb_pages_release(cb_pages* pages, const int32_t* ids, int32_t n);
+int32_t cb_pages_plan_write(cb_pages* pages, const int32_t* table, int32_t n, int32_t* dst);
+int32_t cb_pages_count(const cb_pages* pages, int32_t id);
+int64_t cb_pages_free(const cb_pages* pages);
+
 /* Device status bits recorded by the kernels instead of trapping (cumulative since creation). */
 #define CB_STATUS_BAD_TOKEN    1u  /* a token id outside [0, vocab) was read; its embedding was zeroed */
 #define CB_STATUS_WAIT_TIMEOUT 2u  /* a bounded barrier wait in a tensor-core kernel gave up (~2 s); the
@@ -230,7 +290,7 @@ cb_status cb_model_diag(cb_model* model, uint32_t* words);
  * launch is bracketed by CUDA events recorded on the call's stream (this serialises nothing that was
  * not already serial on that stream, but adds event records between kernels).  Classes: "rerope",
  * "embed", "rmsnorm", "gemm_q", "gemm_kv", "gemm_qkv", "gemm_o", "gemm_gateup", "gemm_down",
- * "attention", "deviation", "topk", "gather_scatter", "logits", "delta_table", "refilter". */
+ * "attention", "deviation", "topk", "gather_scatter", "logits", "delta_table", "refilter", "pages". */
 typedef struct {
     char name[24];
     int32_t launches;        /* launches recorded since the last read */

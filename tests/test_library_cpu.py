@@ -120,3 +120,87 @@ def test_loading_controller_matches_oracle(lib):
                     accounting.pick_storage(tiers, 524288.0, n, tp, rmin), (n, tp, rmin)
     with pytest.raises(cb.CacheBlendError):
         cb.cb_pick_storage([], 1.0, 1, 1.0)
+
+
+class _PagesModel:
+    """Reference of the page bookkeeping rules (host logic): counts, lowest-free-first allocation,
+    copy-on-write for shared pages."""
+
+    def __init__(self, n):
+        self.count = [0] * n
+
+    def alloc(self, k):
+        free = [i for i, c in enumerate(self.count) if c == 0]
+        if k > len(free):
+            return None
+        for i in free[:k]:
+            self.count[i] = 1
+        return free[:k]
+
+    def retain(self, ids):
+        for i in ids:
+            self.count[i] += 1
+
+    def release(self, ids):
+        for i in ids:
+            self.count[i] -= 1
+
+    def plan_write(self, table):
+        need = sum(1 for t in table if self.count[t] > 1)
+        if need > self.count.count(0):
+            return None
+        dst = []
+        for t in table:
+            if self.count[t] > 1:
+                new = self.alloc(1)[0]
+                self.count[t] -= 1
+                dst.append(new)
+            else:
+                dst.append(t)
+        return dst, need
+
+
+def test_page_bookkeeping_matches_reference(lib):
+    import random
+    rng = random.Random(5)
+    n = 64
+    P, M = cb.Pages(n), _PagesModel(n)
+    held = []                                    # tables of live "requests"
+    for step in range(400):
+        op = rng.random()
+        if op < 0.35:
+            k = rng.randint(1, 6)
+            want = M.alloc(k)
+            if want is None:
+                with pytest.raises(cb.CacheBlendError):
+                    P.alloc(k)
+            else:
+                assert P.alloc(k) == want
+                held.append(list(want))
+        elif op < 0.55 and held:
+            t = rng.choice(held)
+            share = t[: rng.randint(1, len(t))]
+            P.retain(share)
+            M.retain(share)
+            held.append(list(share))
+        elif op < 0.75 and held:
+            t = rng.choice(held)
+            want = M.plan_write(t)
+            if want is None:
+                with pytest.raises(cb.CacheBlendError):
+                    P.plan_write(t)
+            else:
+                got = P.plan_write(t)
+                assert got == (want[0], want[1])
+                t[:] = want[0]
+        elif held:
+            t = held.pop(rng.randrange(len(held)))
+            P.release(t)
+            M.release(t)
+        for i in range(n):
+            assert P.count(i) == M.count[i]
+        assert P.free() == M.count.count(0)
+    with pytest.raises(cb.CacheBlendError):
+        P.release([n + 3])
+    assert P.count(-1) == -1
+    P.close()
