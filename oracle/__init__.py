@@ -15,7 +15,8 @@ from .cpu_blend import (attention, blend, blend_gradual, chunk_caches, deviation
                         rerope, rmsnorm, rope, rope_freqs, round_bf16, round_store, select_hkvd, selected_count, silu,
                         to_f64, Model, validate_chunks)
 from . import accounting
+from . import matcher
 
 __all__ = ["attention", "blend", "blend_gradual", "gradual_counts", "chunk_caches", "deviation", "deviation_rows", "prefill", "rerope", "rmsnorm", "rope",
            "rope_freqs", "round_bf16", "round_store", "select_hkvd", "selected_count", "silu", "to_f64",
-           "Model", "validate_chunks", "accounting"]
+           "Model", "validate_chunks", "accounting", "matcher"]
