@@ -222,6 +222,8 @@ def main():
                     help="gradual filtering: 2r at the check layer, shrinking to r over the next 4 layers")
     ap.add_argument("--paged", type=int, default=0, metavar="P",
                     help="keep the chunk caches and the blended K/V in a paged pool of P-row pages (shuffled block table)")
+    ap.add_argument("--matcher", action="store_true",
+                    help="time the GPU fragment matcher instead (32K-token request, 4096 indexed 256-token chunks)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-profile", action="store_true")
@@ -250,6 +252,9 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     import cacheblend_selective_kv_gb300 as cb
+    if args.matcher:
+        run_matcher(args, cb, ws, rank, local)
+        return
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -488,6 +493,49 @@ def main():
                 "gpu_launches": int(st["kernel_launches"]) * args.steps if st else None,
                 "clocks": clocks, "roofline": roofline, "kernels": kernels, "e2e": e2e, "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
+
+
+def run_matcher(args, cb, ws, rank, local):
+    """Fragment lookup of a 32K-token request against 4096 indexed 256-token chunks (half of them planted
+    in the request, the rest absent), timed with CUDA events around each cb_index_match."""
+    import torch
+    torch.cuda.set_device(local)
+    C, V, n_tok, n_idx, seed = 256, 128256, 32768, 4096, 9
+    chunks = np.stack([workload.tokens(seed, 1000 + i, C, V) for i in range(n_idx)]).astype(np.uint32)
+    req = workload.tokens(seed, 1, n_tok, V)
+    rng = np.random.default_rng(seed)
+    for slot, i in enumerate(rng.permutation(n_idx)[: n_tok // C]):
+        req[slot * C:(slot + 1) * C] = chunks[i]
+    index = cb.FragmentIndex(C, chunks, np.arange(n_idx), np.zeros(n_idx, np.int32), np.ones(n_idx, np.int32), n_tok)
+    dev = torch.device("cuda", local)
+    t = torch.from_numpy(req).to(dev)
+    out = torch.empty((4096, 3), dtype=torch.int32, device=dev)
+    cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            index.match_async(t, 1, out, cnt, stream=stream)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            a.record(stream)
+            index.match_async(t, 1, out, cnt, stream=stream)
+            b.record(stream)
+    torch.cuda.synchronize()
+    ms = float(np.median([a.elapsed_time(b) for a, b in evs]))
+    n_match = int(cnt.item())
+    # ALU roofline of the window kernel: one 64-bit multiply-add per token of every window
+    windows = n_tok - C + 1
+    line = {"metric": "fragment match: request tokens/s (GPU matcher)", "value": n_tok / (ms / 1e3),
+            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "dtype": "u64", "data": "synthetic (seeded tokens)",
+            "config": {"workload": f"{n_tok}-token request, {n_idx} indexed {C}-token chunks, stride 1, "
+                                   "leftmost-greedy", "matches": n_match,
+                       "window_hash_macs": windows * C}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    index.close()
 
 
 def load_traffic(kernel: str):

@@ -27,7 +27,7 @@ EXPORTED = ("cb_model_create", "cb_model_destroy", "cb_rerope", "cb_blend", "cb_
             "cb_rerope_static", "cb_model_diag", "cb_load_time", "cb_controller_ratio", "cb_pick_storage",
             "cb_blend_paged", "cb_kv_gather_pages", "cb_kv_scatter_pages", "cb_pages_create", "cb_pages_destroy",
             "cb_pages_alloc", "cb_pages_retain", "cb_pages_release", "cb_pages_plan_write", "cb_pages_count",
-            "cb_pages_free")
+            "cb_pages_free", "cb_index_create", "cb_index_destroy", "cb_index_size", "cb_index_match")
 CB_STATIC_MAX_CHUNKS = 256
 CB_STATUS_BAD_TOKEN, CB_STATUS_WAIT_TIMEOUT, CB_STATUS_BAD_ROW = 1, 2, 4
 
@@ -143,6 +143,14 @@ def lib() -> ctypes.CDLL:
         L.cb_pages_count.argtypes = [vp, i32]
         L.cb_pages_free.restype = i64
         L.cb_pages_free.argtypes = [vp]
+        L.cb_index_create.restype = ctypes.c_int
+        L.cb_index_create.argtypes = [i32, vp, vp, vp, vp, i32, i32, ctypes.POINTER(vp)]
+        L.cb_index_destroy.restype = ctypes.c_int
+        L.cb_index_destroy.argtypes = [vp]
+        L.cb_index_size.restype = i32
+        L.cb_index_size.argtypes = [vp, i32]
+        L.cb_index_match.restype = ctypes.c_int
+        L.cb_index_match.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, vp, vp]
         L.cb_selected_count.restype = i32
         L.cb_selected_count.argtypes = [i32, ctypes.c_double]
         L.cb_profile_enable.restype = ctypes.c_int
@@ -341,6 +349,47 @@ class Pages:
     def close(self):
         if self.h:
             lib().cb_pages_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class FragmentIndex:
+    """cb_index_*: an immutable fragment index on the device (built from host arrays) and its matcher."""
+
+    def __init__(self, chunk_size: int, tokens, occ_ids, old_st, ns, max_tokens: int):
+        t = np.ascontiguousarray(tokens, dtype=np.uint32).reshape(-1)
+        o, s_, n_ = (np.ascontiguousarray(a, dtype=np.int32) for a in (occ_ids, old_st, ns))
+        h = ctypes.c_void_p()
+        _check(lib().cb_index_create(int(chunk_size), t.ctypes.data, o.ctypes.data, s_.ctypes.data, n_.ctypes.data,
+                                     len(o), int(max_tokens), ctypes.byref(h)))
+        self.h, self.chunk_size = h.value, chunk_size
+
+    def size(self, what: int) -> int:
+        return int(lib().cb_index_size(self.h, int(what)))
+
+    def match_async(self, tokens, ns: int, out, out_count, stride: int = 1, greedy: bool = True, stream=None):
+        """Enqueue a match: out (device int32 [max][3]) and out_count (device int32 [1])."""
+        _check(lib().cb_index_match(self.h, _ptr(tokens), int(tokens.shape[0]), int(ns), int(stride),
+                                    1 if greedy else 0, _ptr(out), int(out.shape[0]), _ptr(out_count),
+                                    _stream(stream)))
+
+    def match(self, tokens, ns: int, stride: int = 1, greedy: bool = True, max_out: int = 4096) -> list:
+        """Matches as (occupant id, old_st, cur_st) triples (synchronises)."""
+        import torch
+        out = torch.empty((max_out, 3), dtype=torch.int32, device=tokens.device)
+        cnt = torch.zeros(1, dtype=torch.int32, device=tokens.device)
+        self.match_async(tokens, ns, out, cnt, stride, greedy)
+        n = int(cnt.item())
+        return [tuple(int(v) for v in r) for r in out[:min(n, max_out)].cpu().tolist()]
+
+    def close(self):
+        if self.h:
+            lib().cb_index_destroy(self.h)
             self.h = None
 
     def __del__(self):

@@ -271,6 +271,34 @@ int32_t cb_pages_plan_write(cb_pages* pages, const int32_t* table, int32_t n, in
 int32_t cb_pages_count(const cb_pages* pages, int32_t id);
 int64_t cb_pages_free(const cb_pages* pages);
 
+/* Fragment lookup on the GPU (LMCache coordinator blend-index page, sections "四、数据结构与召回" and
+ * "六、HTTP 接口"): which indexed chunks a request's tokens contain and where, i.e. the (src_pos, dst_pos)
+ * chunk layout of a blend.
+ * cb_index_create builds an immutable index on the host and copies it to the current device (it allocates;
+ * rebuild it to change the indexed set).  Chunk i has chunk_size tokens tokens[i*chunk_size ..], an
+ * occupant id occ_ids[i] (the caller's name for the stored chunk), the position old_st[i] it was stored
+ * at, and a namespace ns[i].  A chunk with old_st < 0 (stored position unknown) is not indexed.  A
+ * chunk's fingerprint is Horner's rule over its tokens (as unsigned 32-bit values) modulo 2^64 with base
+ * 0x9E3779B97F4A7C15; a fingerprint names the first content indexed under it, and a different content
+ * with the same fingerprint is not indexed.  Chunks with identical content are occupants of one content,
+ * kept in the order given.  max_tokens bounds the requests that cb_index_match accepts.
+ * cb_index_match probes the request's windows at positions 0, s, 2s, ... (s = probe_stride); a window
+ * whose fingerprint, content and tokens match a content with an occupant in namespace `ns` is verified.
+ * The t-th verified window of a content (in position order) takes that content's t-th occupant in `ns`:
+ * each occupant matches at most once, at its first place.  Matches are written ascending by position as
+ * int32 triples (occupant id, old_st, cur_st) into out (device, max_out triples); with leftmost_greedy a
+ * match overlapping an earlier kept one is dropped.  *out_count (device int32) receives the number of
+ * matches (which may exceed max_out: only the first max_out are written).  Async on `stream`; no
+ * allocation.  Calls on one index must not overlap (they share its scratch buffers).
+ * cb_index_size: what = 0 contents, 1 occupants, 2 indexed chunks, 3 chunk_size. */
+typedef struct cb_index cb_index;
+cb_status cb_index_create(int32_t chunk_size, const uint32_t* tokens, const int32_t* occ_ids, const int32_t* old_st,
+                          const int32_t* ns, int32_t n_chunks, int32_t max_tokens, cb_index** out);
+cb_status cb_index_destroy(cb_index* index);
+int32_t cb_index_size(const cb_index* index, int32_t what);
+cb_status cb_index_match(cb_index* index, const int32_t* tokens, int32_t n_tokens, int32_t ns, int32_t probe_stride,
+                         int32_t leftmost_greedy, int32_t* out, int32_t max_out, int32_t* out_count, void* stream);
+
 /* Device status bits recorded by the kernels instead of trapping (cumulative since creation). */
 #define CB_STATUS_BAD_TOKEN    1u  /* a token id outside [0, vocab) was read; its embedding was zeroed */
 #define CB_STATUS_WAIT_TIMEOUT 2u  /* a bounded barrier wait in a tensor-core kernel gave up (~2 s); the
