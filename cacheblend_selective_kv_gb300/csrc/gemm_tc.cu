@@ -43,7 +43,9 @@ namespace {
 constexpr int BM = 128, BK = 64, TMEM_COLS = 512, NUM_THREADS = 192;
 constexpr int A_BYTES = BM * BK * 2;        // 16 KB per weight tile
 constexpr int MAX_STAGES = 8;
-constexpr int EPI_SMEM = 4 * 32 * 17 * 4;   // per-epilogue-warp staging (token positions / transposes)
+constexpr int EPI_POS_INTS = 32 * 17;           // per epilogue warp: token positions (QKV) / transposes
+constexpr int EPI_STG_WORDS = 512;               // per epilogue warp: QKV store staging (2 KB)
+constexpr int EPI_SMEM = 4 * (EPI_POS_INTS * 4 + EPI_STG_WORDS * 4);
 
 struct TcArgs {
     int M, K, x_row0, kb_total, splits, ttiles, BN, stages, units, prefetch;
@@ -95,17 +97,20 @@ __device__ __forceinline__ void store_pair<bf16>(bf16* p, float a, float b) {
 }
 
 // QKV epilogue of one tile: RoPE of q/k pairs (partner feature = lane ^ 1), q as bf16 (hi and, in split
-// precision, lo), k/v either into the blended cache at each token's position or as fp32 rows.
-// Positions come from a per-warp shared-memory copy; the (cos, sin) loads of the next 16 tokens are
-// issued before the current 16 are processed.
+// precision, lo), k/v either into the blended cache at each token's position or as fp32 rows.  A warp's 32
+// features are consecutive and lie in one region (regions and segments are multiples of 64 wide), so each
+// 16-token chunk is transposed through the warp's shared-memory staging area and written as 16-byte
+// vectors along the features of each token row.  Positions come from a per-warp shared-memory copy; the
+// (cos, sin) loads of the next 16 tokens are issued before the current 16 are processed.
 __device__ __forceinline__ void qkv_tile(const TcArgs& a, const Unit& w, int row, int lane, int tok0, int ntok,
-                                         uint32_t tbase, const int* wpos) {
+                                         uint32_t tbase, const int* wpos, uint32_t* stg) {
     const EpiParams& e = a.e;
     const int feat = w.lt * BM + row;
-    const bool fv = feat < a.seg_rows[w.seg];
+    const bool fv = feat < a.seg_rows[w.seg];               // uniform across the warp
     const int col = a.seg_base[w.seg] + feat + e.qkv_base;
     int off;
     const int reg = qkv_region(e, col, off);
+    const int off0 = off - lane;                            // the warp's first feature in its region
     const bool even = (lane & 1) == 0;
     const int half = e.head_dim >> 1, pair = (off % e.head_dim) >> 1;
     const bool rot = reg < 2;
@@ -126,39 +131,86 @@ __device__ __forceinline__ void qkv_tile(const TcArgs& a, const Unit& w, int row
             }
         }
         const int nt = min(16, ntok - base);
+        float r0[16], r1[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-            if (j >= nt) break;                     // uniform across the warp
-            const int tok = tok0 + base + j;
             const float x = v[j];
             const float y = __shfl_xor_sync(0xffffffffu, x, 1);
-            if (even && fv) {
-                float x0 = x, x1 = y;
-                if (rot) {
-                    x0 = x * cs[j].x - y * cs[j].y;
-                    x1 = x * cs[j].y + y * cs[j].x;
+            r0[j] = rot ? x * cs[j].x - y * cs[j].y : x;
+            r1[j] = rot ? x * cs[j].y + y * cs[j].x : y;
+        }
+        if (fv) {
+            if (e.kv_fresh && reg > 0) {
+                // fp32 rows: stage [16 tokens][32 features], write 8 x 16 bytes per token
+                float* st = reinterpret_cast<float*>(stg);
+                if (even) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        *reinterpret_cast<float2*>(st + j * 32 + lane) = make_float2(r0[j], r1[j]);
                 }
-                if (reg == 0) {
-                    bf16 h0, l0, h1, l1;
-                    split_bf16(x0, h0, l0);
-                    split_bf16(x1, h1, l1);
-                    *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<bf16*>(e.q_out) + (size_t)tok * e.nq + off) =
-                        __halves2bfloat162(h0, h1);
-                    if (e.q_out_lo)
-                        *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<bf16*>(e.q_out_lo) + (size_t)tok * e.nq +
-                                                           off) = __halves2bfloat162(l0, l1);
-                } else {
-                    void* dst = reg == 1 ? e.k_dst : e.v_dst;
-                    if (e.kv_fresh)
-                        *reinterpret_cast<float2*>(reinterpret_cast<float*>(dst) + (size_t)tok * e.nkv + off) =
-                            make_float2(x0, x1);
-                    else
-                        store_pair<bf16>(reinterpret_cast<bf16*>(dst) + (size_t)wpos[base + j] * e.nkv + off, x0, x1);
+                __syncwarp();
+                float* dst = reinterpret_cast<float*>(reg == 1 ? e.k_dst : e.v_dst) + off0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int t = (lane >> 3) + 4 * k, sg = lane & 7;
+                    if (t < nt)
+                        *reinterpret_cast<float4*>(dst + (size_t)(tok0 + base + t) * e.nkv + sg * 4) =
+                            *reinterpret_cast<const float4*>(st + t * 32 + sg * 4);
                 }
+                __syncwarp();
+            } else {
+                // bf16 rows: stage [16 tokens][16 pairs] (hi, then lo for split q), write 4 x 16 bytes per token
+                const bool lo = reg == 0 && e.q_out_lo != nullptr;
+                if (even) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        bf16 h0, l0, h1, l1;
+                        split_bf16(r0[j], h0, l0);
+                        split_bf16(r1[j], h1, l1);
+                        __nv_bfloat162 hp = __halves2bfloat162(h0, h1), lp = __halves2bfloat162(l0, l1);
+                        stg[j * 16 + (lane >> 1)] = *reinterpret_cast<uint32_t*>(&hp);
+                        if (lo) stg[256 + j * 16 + (lane >> 1)] = *reinterpret_cast<uint32_t*>(&lp);
+                    }
+                }
+                __syncwarp();
+                bf16* hi_base = reinterpret_cast<bf16*>(reg == 0 ? e.q_out : (reg == 1 ? e.k_dst : e.v_dst)) + off0;
+                bf16* lo_base = lo ? reinterpret_cast<bf16*>(e.q_out_lo) + off0 : nullptr;
+                const int ld = reg == 0 ? e.nq : e.nkv;
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int t = (lane >> 2) + 8 * k, sg = lane & 3;
+                    if (t < nt) {
+                        const size_t r = reg == 0 ? (size_t)(tok0 + base + t) : (size_t)wpos[base + t];
+                        *reinterpret_cast<uint4*>(hi_base + r * ld + sg * 8) =
+                            *reinterpret_cast<const uint4*>(stg + t * 16 + sg * 4);
+                        if (lo)
+                            *reinterpret_cast<uint4*>(lo_base + r * ld + sg * 8) =
+                                *reinterpret_cast<const uint4*>(stg + 256 + t * 16 + sg * 4);
+                    }
+                }
+                __syncwarp();
             }
         }
 #pragma unroll
         for (int j = 0; j < 16; ++j) cs[j] = csn[j];
+    }
+}
+
+// warm L2 with the (cos, sin) rows of a tile's tokens for this warp's 16 pairs (one 128-byte line per
+// token), issued while the tile's MMAs run
+__device__ __forceinline__ void qkv_prefetch(const TcArgs& a, const Unit& w, int row, int lane, int tok0, int ntok,
+                                             int* wpos) {
+    const EpiParams& e = a.e;
+    for (int i = lane; i < ntok; i += 32) wpos[i] = epi_pos(e, tok0 + i);
+    __syncwarp();
+    const int feat = w.lt * BM + row;
+    int off;
+    const int reg = qkv_region(e, a.seg_base[w.seg] + feat + e.qkv_base, off);
+    if (reg == 2 || feat >= a.seg_rows[w.seg]) return;
+    const int half = e.head_dim >> 1, pair0 = ((off - lane) % e.head_dim) >> 1;
+    for (int i = lane; i < ntok; i += 32) {
+        const float2* p = e.rope + (size_t)wpos[i] * half + pair0;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
     }
 }
 
@@ -205,11 +257,12 @@ __device__ __forceinline__ void epi_swiglu(const TcArgs& a, const Unit& w, int r
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         const int tok = tok0 + j;
-        if (tok >= a.M) break;
         bf16 hi, lo;
         split_bf16(silu_mul(g[j], u[j]), hi, lo);
-        act[(size_t)tok * e.ld_act + feat] = hi;
-        if (act_lo) act_lo[(size_t)tok * e.ld_act + feat] = lo;
+        if (tok < a.M) {                               // predicated: the 16 tokens stay interleaved
+            act[(size_t)tok * e.ld_act + feat] = hi;
+            if (act_lo) act_lo[(size_t)tok * e.ld_act + feat] = lo;
+        }
     }
 }
 
@@ -370,16 +423,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
             const Unit w = decode_unit(a, u);
-            if (!ptx::mbar_wait(ptx::smem_u32(tfull + acc), acc_phase, abort, a.status)) break;
-            ptx::tc_fence_after();
             const int tok0 = w.t * a.BN;
             const int ntok = min(a.BN, a.M - tok0);
+            int* wpos = spos + (warp - 2) * EPI_POS_INTS;
+            if (EPI == EPI_QKV) qkv_prefetch(a, w, row, lane, tok0, ntok, wpos);
+            if (!ptx::mbar_wait(ptx::smem_u32(tfull + acc), acc_phase, abort, a.status)) break;
+            ptx::tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256;
             if (EPI == EPI_QKV) {
-                int* wpos = spos + (warp - 2) * (32 * 17);
-                for (int i = lane; i < ntok; i += 32) wpos[i] = epi_pos(a.e, tok0 + i);
-                __syncwarp();
-                qkv_tile(a, w, row, lane, tok0, ntok, tbase, wpos);
+                qkv_tile(a, w, row, lane, tok0, ntok, tbase, wpos,
+                         reinterpret_cast<uint32_t*>(spos + 4 * EPI_POS_INTS) + (warp - 2) * EPI_STG_WORDS);
                 __syncwarp();
             }
             for (int c = 0; EPI != EPI_QKV && c * 16 < ntok; ++c) {
@@ -425,7 +478,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // 64 features (the pair covers 128), so each feature's gate and up meet in one CTA's TMEM and the
 // epilogue exchanges them between lane quarters q and q ^ 2 through shared memory.
 // =================================================================================================
-constexpr int EPI_SMEM_PAIR = 4 * 2 * 32 * 17 * 4;   // [quarter][slot][32 x 17] floats
+constexpr int EPI_SMEM_PAIR = 4 * 2 * 32 * 17 * 4 > EPI_SMEM ? 4 * 2 * 32 * 17 * 4 : EPI_SMEM;   // SwiGLU: [quarter][slot][32 x 17] floats
 
 __device__ __forceinline__ void epi_swiglu_pair(const TcArgs& a, int feat, bool fv, int q, int lane, int tok0,
                                                 int ntok_c, int slot, const float* v, float* xs) {
@@ -443,11 +496,12 @@ __device__ __forceinline__ void epi_swiglu_pair(const TcArgs& a, int feat, bool 
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int j = j0 + i;
-            if (j >= ntok_c) break;
             bf16 hi, lo;
             split_bf16(silu_mul(gs[lane * 17 + j], us[lane * 17 + j]), hi, lo);
-            act[(size_t)(tok0 + j) * e.ld_act + feat] = hi;
-            if (act_lo) act_lo[(size_t)(tok0 + j) * e.ld_act + feat] = lo;
+            if (j < ntok_c) {                          // predicated: the 8 tokens stay interleaved
+                act[(size_t)(tok0 + j) * e.ld_act + feat] = hi;
+                if (act_lo) act_lo[(size_t)(tok0 + j) * e.ld_act + feat] = lo;
+            }
         }
     }
     __syncwarp();
@@ -589,16 +643,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         for (int u = cluster; u < a.units; u += nclusters) {
             Unit w = decode_unit(a, u);
             if (!SWIGLU) w.lt = 2 * w.lt + (int)rank;
-            if (!ptx::mbar_wait(ptx::smem_u32(tfull + acc), acc_phase, abort, a.status)) break;
-            ptx::tc_fence_after();
             const int tok0 = w.t * a.BN;
             const int ntok = min(a.BN, a.M - tok0);
+            int* wpos = spos + (warp - 2) * EPI_POS_INTS;
+            if (EPI == EPI_QKV) qkv_prefetch(a, w, row, lane, tok0, ntok, wpos);
+            if (!ptx::mbar_wait(ptx::smem_u32(tfull + acc), acc_phase, abort, a.status)) break;
+            ptx::tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256;
             if (EPI == EPI_QKV) {
-                int* wpos = spos + (warp - 2) * (32 * 17);
-                for (int i = lane; i < ntok; i += 32) wpos[i] = epi_pos(a.e, tok0 + i);
-                __syncwarp();
-                qkv_tile(a, w, row, lane, tok0, ntok, tbase, wpos);
+                qkv_tile(a, w, row, lane, tok0, ntok, tbase, wpos,
+                         reinterpret_cast<uint32_t*>(spos + 4 * EPI_POS_INTS) + (warp - 2) * EPI_STG_WORDS);
                 __syncwarp();
             } else if (EPI == EPI_RESID) {
                 for (int c = 0; c * 16 < ntok; ++c) {
