@@ -115,20 +115,29 @@ __device__ __forceinline__ void qkv_tile(const TcArgs& a, const Unit& w, int row
     const int half = e.head_dim >> 1, pair = (off % e.head_dim) >> 1;
     const bool rot = reg < 2;
     const int nch = (ntok + 15) / 16;
-    float2 cs[16], csn[16];
+    // software pipeline: the accumulator columns of chunk c+1 are loaded from TMEM, and the (cos, sin)
+    // of chunk c+2 from global memory, while chunk c is processed
+    auto rope_at = [&](int t) {
+        return (rot && t < ntok) ? e.rope[(size_t)wpos[t] * half + pair] : make_float2(1.f, 0.f);
+    };
+    float2 cs[16], csn[16], csn2[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-        cs[j] = (rot && j < ntok) ? e.rope[(size_t)wpos[j] * half + pair] : make_float2(1.f, 0.f);
+    for (int j = 0; j < 16; ++j) {
+        cs[j] = rope_at(j);
+        csn[j] = rope_at(16 + j);
+    }
+    uint32_t vn[16];
+    ptx::tmem_ld16_issue(tbase, vn);
     for (int c = 0; c < nch; ++c) {
         float v[16];
-        ptx::tmem_ld16(tbase + c * 16, v);
-        const int base = c * 16;
-        if (c + 1 < nch) {
+        ptx::tmem_ld_wait16(vn);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int t = base + 16 + j;
-                csn[j] = (rot && t < ntok) ? e.rope[(size_t)wpos[t] * half + pair] : make_float2(1.f, 0.f);
-            }
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(vn[j]);
+        if (c + 1 < nch) ptx::tmem_ld16_issue(tbase + (c + 1) * 16, vn);
+        const int base = c * 16;
+        if (c + 2 < nch) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) csn2[j] = rope_at(base + 32 + j);
         }
         const int nt = min(16, ntok - base);
         float r0[16], r1[16];
@@ -192,7 +201,10 @@ __device__ __forceinline__ void qkv_tile(const TcArgs& a, const Unit& w, int row
             }
         }
 #pragma unroll
-        for (int j = 0; j < 16; ++j) cs[j] = csn[j];
+        for (int j = 0; j < 16; ++j) {
+            cs[j] = csn[j];
+            csn[j] = csn2[j];
+        }
     }
 }
 
