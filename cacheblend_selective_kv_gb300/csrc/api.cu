@@ -174,6 +174,10 @@ cb_status cb_model_create(const cb_config* cfg, const cb_weights* w, cb_model** 
         return fail(CB_ERR_CUDA, "table upload failed");
     }
     m->attn_tc = false;
+    {
+        const char* v = getenv("CB_PDL");
+        m->pdl = !(v && v[0] == '0');
+    }
     if (m->bf16) {
         std::string err;
         if (!tc_init(*m, err)) m->tc = nullptr;   // CUDA-core path only

@@ -232,6 +232,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    grid_dep_launch();
+    grid_dep_wait();                                     // q and the blended K/V of the previous kernels
 
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer: Q and K
@@ -561,6 +563,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // One warp per (query, head); each lane owns hd/32 consecutive dims.
 template <int HD>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
+    grid_dep_launch();
+    grid_dep_wait();
     const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (wid >= a.M * a.Hq) return;
     const int qi = wid / a.Hq, head = wid % a.Hq;
@@ -617,7 +621,7 @@ size_t attn_smem() {
 
 template <int HD, bool SPLIT>
 cudaError_t launch_hd(const CUtensorMap& mq, const CUtensorMap& mql, const CUtensorMap& mkv, const AttnArgs& a,
-                      int grid, cudaStream_t s) {
+                      int grid, cudaStream_t s, bool pdl) {
     static bool set = false;
     const size_t sm = attn_smem<HD, SPLIT>();
     if (!set) {
@@ -625,8 +629,7 @@ cudaError_t launch_hd(const CUtensorMap& mq, const CUtensorMap& mql, const CUten
         if (e != cudaSuccess) return e;
         set = true;
     }
-    attn_tc_kernel<HD, SPLIT><<<grid, NUM_THREADS, sm, s>>>(mq, mql, mkv, a);
-    return cudaGetLastError();
+    return launch_ex(pdl, attn_tc_kernel<HD, SPLIT>, dim3(grid), dim3(NUM_THREADS), sm, s, mq, mql, mkv, a);
 }
 
 }  // namespace
@@ -714,9 +717,9 @@ cudaError_t launch_attention_tc(const Model& m, const void* qmap, const void* qm
     const CUtensorMap& mkv = *reinterpret_cast<const CUtensorMap*>(kvmap);
     cudaError_t e;
     if (c.head_dim == 128)
-        e = m.split ? launch_hd<128, true>(mq, mql, mkv, a, grid, s) : launch_hd<128, false>(mq, mql, mkv, a, grid, s);
+        e = m.split ? launch_hd<128, true>(mq, mql, mkv, a, grid, s, m.pdl) : launch_hd<128, false>(mq, mql, mkv, a, grid, s, m.pdl);
     else
-        e = m.split ? launch_hd<64, true>(mq, mql, mkv, a, grid, s) : launch_hd<64, false>(mq, mql, mkv, a, grid, s);
+        e = m.split ? launch_hd<64, true>(mq, mql, mkv, a, grid, s, m.pdl) : launch_hd<64, false>(mq, mql, mkv, a, grid, s, m.pdl);
     if (launches) *launches = 1;
     if (e != cudaSuccess || a.parts == 1) return e;
     const int warps = M * c.n_heads;

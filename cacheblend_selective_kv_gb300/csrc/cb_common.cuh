@@ -31,6 +31,12 @@ __device__ __forceinline__ void split_bf16(float v, bf16& hi, bf16& lo) {
     lo = __float2bfloat16_rn(v - __bfloat162float(hi));
 }
 
+// Programmatic dependent launch.  grid_dep_wait: until the grids this one depends on have completed and
+// their memory is visible (a no-op for a launch without the attribute); every thread calls it before its
+// first global access.  grid_dep_launch: lets the next kernel on the stream start its prologue now.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -157,6 +163,7 @@ struct Model {
     alignas(64) unsigned char qmap[128];   // tensor map of the q workspace (attention)
     alignas(64) unsigned char qmap_lo[128];
     size_t ws_bytes;
+    bool pdl;             // launch the tensor-core kernels with programmatic dependent launch
     Profile prof;
     std::vector<cudaEvent_t> io_ev;   // layer-wise load pipeline: [n_layers] loaded, [n_layers] final, fork, 2 joins
 };
@@ -204,6 +211,24 @@ void tc_destroy(Model& m);
 cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, const GemmW& w, int N,
                            const EpiParams& e, cudaStream_t s, int* launches);
 enum { XBUF_X = 0, XBUF_XA = 1, XBUF_ATTN = 2, XBUF_ACT = 3 };
+
+// Launch `k` on `s`, with programmatic dependent launch when `pdl` (the kernel calls grid_dep_wait
+// before its first global access, so it may start while the previous kernel on the stream drains).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(bool pdl, void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                      Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, args...);
+}
 
 // records a message for cb_last_error() on the calling thread
 void set_last_error(const char* msg);

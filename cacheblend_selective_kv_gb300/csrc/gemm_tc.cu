@@ -327,6 +327,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    grid_dep_launch();
+    grid_dep_wait();                                     // inputs of the previous kernel are visible
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
@@ -569,6 +571,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     ptx::cluster_sync();                                 // barriers of both CTAs initialised
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    grid_dep_launch();
+    grid_dep_wait();                                     // inputs of the previous kernel are visible
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer (both CTAs)
@@ -716,7 +720,7 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
 
 template <int EPI, bool SPLIT>
 cudaError_t launch_kernel(const CUtensorMap& mx, const CUtensorMap& mxl, const CUtensorMap* w0, const CUtensorMap* w1,
-                          const CUtensorMap* w2, const TcArgs& a, int grid, size_t smem, cudaStream_t s) {
+                          const CUtensorMap* w2, const TcArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl) {
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e =
@@ -724,13 +728,13 @@ cudaError_t launch_kernel(const CUtensorMap& mx, const CUtensorMap& mxl, const C
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    gemm_tc_kernel<EPI, SPLIT><<<grid, NUM_THREADS, smem, s>>>(mx, mxl, *w0, w1 ? *w1 : *w0, w2 ? *w2 : *w0, a);
-    return cudaGetLastError();
+    return launch_ex(pdl, gemm_tc_kernel<EPI, SPLIT>, dim3(grid), dim3(NUM_THREADS), smem, s, mx, mxl, *w0,
+                     w1 ? *w1 : *w0, w2 ? *w2 : *w0, a);
 }
 
 template <int EPI, bool SPLIT>
 cudaError_t launch_pair(const CUtensorMap& mx, const CUtensorMap& mxl, const CUtensorMap* w0, const CUtensorMap* w1,
-                        const CUtensorMap* w2, const TcArgs& a, int grid, size_t smem, cudaStream_t s) {
+                        const CUtensorMap* w2, const TcArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl) {
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e =
@@ -738,8 +742,8 @@ cudaError_t launch_pair(const CUtensorMap& mx, const CUtensorMap& mxl, const CUt
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    gemm_pair_kernel<EPI, SPLIT><<<grid, NUM_THREADS, smem, s>>>(mx, mxl, *w0, w1 ? *w1 : *w0, w2 ? *w2 : *w0, a);
-    return cudaGetLastError();
+    return launch_ex(pdl, gemm_pair_kernel<EPI, SPLIT>, dim3(grid), dim3(NUM_THREADS), smem, s, mx, mxl, *w0,
+                     w1 ? *w1 : *w0, w2 ? *w2 : *w0, a);
 }
 
 // clusters of the pair kernel that fit on the device at once (one CTA per SM)
@@ -949,15 +953,15 @@ cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, c
     do {                                                                                             \
         if (split) {                                                                                 \
             switch (e.kind) {                                                                        \
-                case EPI_QKV: return LAUNCH<EPI_QKV, true>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s);     \
-                case EPI_RESID: return LAUNCH<EPI_RESID, true>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s); \
-                default: return LAUNCH<EPI_SWIGLU, true>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s);       \
+                case EPI_QKV: return LAUNCH<EPI_QKV, true>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s, m.pdl);     \
+                case EPI_RESID: return LAUNCH<EPI_RESID, true>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s, m.pdl); \
+                default: return LAUNCH<EPI_SWIGLU, true>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s, m.pdl);       \
             }                                                                                        \
         }                                                                                            \
         switch (e.kind) {                                                                            \
-            case EPI_QKV: return LAUNCH<EPI_QKV, false>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s);        \
-            case EPI_RESID: return LAUNCH<EPI_RESID, false>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s);    \
-            default: return LAUNCH<EPI_SWIGLU, false>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s);          \
+            case EPI_QKV: return LAUNCH<EPI_QKV, false>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s, m.pdl);        \
+            case EPI_RESID: return LAUNCH<EPI_RESID, false>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s, m.pdl);    \
+            default: return LAUNCH<EPI_SWIGLU, false>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s, m.pdl);          \
         }                                                                                            \
     } while (0)
     if (pair) CB_GEMM_DISPATCH(launch_pair);

@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(KB) attn_simt_kernel(const T* __restrict__ q, 
                                                        const T* __restrict__ kv, int64_t kv_rows, int n_keys,
                                                        T* __restrict__ out, T* __restrict__ out_lo, int Hq, int Hkv,
                                                        int hd, float scale) {
+    grid_dep_launch();
+    grid_dep_wait();
     extern __shared__ float sm[];
     const int i = blockIdx.x, g = blockIdx.y, G = Hq / Hkv, tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;

@@ -22,6 +22,8 @@ __device__ __forceinline__ const T* weight_row(const GemmW& w, int c, int K) {
 template <typename T, int EPI>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(const T* __restrict__ X, const T* __restrict__ X_lo, int M,
                                                         int K, GemmW w, int N, EpiParams e) {
+    grid_dep_launch();
+    grid_dep_wait();
     __shared__ float Xs[BK][BM + 4];
     __shared__ float Ws[BK][BN + 4];
     __shared__ float Us[EPI == EPI_SWIGLU ? BK : 1][BN + 4];

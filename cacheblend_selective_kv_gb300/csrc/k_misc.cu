@@ -49,6 +49,8 @@ static inline int grid_for(int64_t items, int threads, int sms, int per_sm = 8) 
 // ------------------------------------------------------------------------------------------------
 __global__ void delta_table_kernel(ChunkTable t, const double* inv_freq, int half, float2* cs, int* dst,
                                    int* delta) {
+    grid_dep_launch();
+    grid_dep_wait();
     const int c = blockIdx.x;
     if (c >= t.n) return;
     if (threadIdx.x == 0) {
@@ -88,6 +90,8 @@ __global__ void rerope_kernel(const T* __restrict__ src, T* __restrict__ dst, in
                               int n_ctx, int W, int hd, int L, int kv_count, const int* __restrict__ cdst,
                               const float2* __restrict__ cs, int n_chunks, const int* __restrict__ src_pages,
                               int page_shift, int64_t n_pages, unsigned* status) {
+    grid_dep_launch();
+    grid_dep_wait();
     const int W8 = W / 8, half = hd / 2;
     const int64_t per_lk = (int64_t)n_ctx * W8;
     const int64_t total = (int64_t)L * kv_count * per_lk;
@@ -150,6 +154,8 @@ cudaError_t launch_rerope(const Model& m, const void* src, void* dst, int64_t sr
 template <typename T>
 __global__ void embed_kernel(const int* __restrict__ tokens, const T* __restrict__ E, int vocab, int d, float* h,
                              unsigned* status) {
+    grid_dep_launch();
+    grid_dep_wait();
     const int r = blockIdx.x;
     const int t = tokens[r];
     float* out = h + (size_t)r * d;
@@ -181,6 +187,8 @@ cudaError_t launch_embed(const Model& m, const int* tokens, int n, float* h, cud
 template <typename T>
 __global__ void rmsnorm_kernel(const float* __restrict__ h, const T* __restrict__ g, T* __restrict__ out,
                                T* __restrict__ out_lo, int d, float eps) {
+    grid_dep_launch();
+    grid_dep_wait();
     const int r = blockIdx.x;
     const float* row = h + (size_t)r * d;
     __shared__ float red[32];
@@ -241,6 +249,8 @@ template <typename T>
 __global__ void deviation_kernel(const float* __restrict__ kf, const float* __restrict__ vf,
                                  const T* __restrict__ kv_layer, int64_t kv_rows, const int* __restrict__ crow,
                                  int n_ctx, int W, float* dev) {
+    grid_dep_launch();
+    grid_dep_wait();
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (warp >= n_ctx) return;
     const int64_t j = crow ? crow[warp] : warp;
@@ -285,6 +295,8 @@ __global__ void gather_scatter_kernel(const int* __restrict__ rows, const float*
                                       const T* __restrict__ x, T* __restrict__ xA, const T* __restrict__ x_lo,
                                       T* __restrict__ xA_lo, const float* __restrict__ kf,
                                       const float* __restrict__ vf, T* kv_layer, int64_t kv_rows, int d, int W) {
+    grid_dep_launch();
+    grid_dep_wait();
     const int i = blockIdx.x;
     const int r = rows[i];
     for (int e = threadIdx.x * 4; e < d; e += blockDim.x * 4)
@@ -334,6 +346,8 @@ __global__ void refilter_kernel(const int* __restrict__ local, const int* __rest
                                 const T* __restrict__ x_old, T* __restrict__ x_new, const T* __restrict__ xlo_old,
                                 T* __restrict__ xlo_new, const float* __restrict__ kf, const float* __restrict__ vf,
                                 T* kv_layer, int64_t kv_rows, int d, int W) {
+    grid_dep_launch();
+    grid_dep_wait();
     const int i = blockIdx.x;
     const int src = local[i];
     const int r = rows_old[src];
@@ -385,6 +399,8 @@ cudaError_t launch_refilter(const Model& m, const int* local, const int* rows_ol
 template <typename T>
 __global__ void logits_kernel(const float* __restrict__ hl, const T* __restrict__ g, const T* __restrict__ Wh,
                               int d, int vocab, float eps, float* __restrict__ out) {
+    grid_dep_launch();
+    grid_dep_wait();
     extern __shared__ float xs[];
     __shared__ float red[32];
     float ss = 0.f;

@@ -15,6 +15,8 @@ template <typename V>
 __global__ void page_copy_kernel(const V* __restrict__ src, int64_t src_rows, const int* __restrict__ src_pages,
                                  V* __restrict__ dst, int64_t dst_rows, const int* __restrict__ dst_pages,
                                  int page_shift, int n_rows, int W16, int L2, unsigned* status) {
+    grid_dep_launch();
+    grid_dep_wait();
     const int64_t per_block = (int64_t)n_rows * W16;             // vectors per (layer, K|V) block
     const int64_t total = (int64_t)L2 * per_block;
     const int mask = (1 << page_shift) - 1;

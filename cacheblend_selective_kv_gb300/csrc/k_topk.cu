@@ -43,6 +43,8 @@ __device__ __forceinline__ int block_excl_count(bool flag, int* warp_tot, int& t
 
 __global__ void __launch_bounds__(TK_THREADS) topk_kernel(const float* __restrict__ dev, int n, int k, int n_query,
                                                           int* __restrict__ rows, int* __restrict__ out_sel) {
+    grid_dep_launch();
+    grid_dep_wait();
     __shared__ unsigned hist[256];
     __shared__ int warp_tot[33];
     __shared__ unsigned s_digit;
