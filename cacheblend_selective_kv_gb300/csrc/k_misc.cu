@@ -87,20 +87,20 @@ __device__ __forceinline__ int chunk_of(const int* dst, int n, int j) {
 
 template <typename T>
 __global__ void rerope_kernel(const T* __restrict__ src, T* __restrict__ dst, int64_t src_rows, int64_t dst_rows,
-                              int n_ctx, int W, int hd, int L, int kv_count, const int* __restrict__ cdst,
+                              int n_ctx, int W, int hd, int kv_count, const int* __restrict__ cdst,
                               const float2* __restrict__ cs, int n_chunks, const int* __restrict__ src_pages,
                               int page_shift, int64_t n_pages, unsigned* status) {
     grid_dep_launch();
     grid_dep_wait();
+    // blockIdx.y = (layer, K|V) block; 32-bit indices within it (n_ctx * W / 8 < 2^31)
+    const int lk = blockIdx.y;
+    const int layer = lk / kv_count, kv = lk - layer * kv_count;
     const int W8 = W / 8, half = hd / 2;
-    const int64_t per_lk = (int64_t)n_ctx * W8;
-    const int64_t total = (int64_t)L * kv_count * per_lk;
-    for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
-         it += (int64_t)gridDim.x * blockDim.x) {
-        const int lk = (int)(it / per_lk);
-        const int rem = (int)(it - (int64_t)lk * per_lk);
-        const int j = rem / W8, e = (rem - j * W8) * 8;
-        const int layer = lk / kv_count, kv = lk - layer * kv_count;
+    const int per_lk = n_ctx * W8;
+    const T* sblk = src + ((int64_t)layer * 2 + kv) * src_rows * W;
+    T* dblk = dst + ((int64_t)layer * 2 + kv) * dst_rows * W;
+    for (int it = blockIdx.x * blockDim.x + threadIdx.x; it < per_lk; it += gridDim.x * blockDim.x) {
+        const int j = it / W8, e = (it - j * W8) * 8;
         int64_t sj = j;
         if (src_pages) {
             const int pg = src_pages[j >> page_shift];
@@ -110,10 +110,8 @@ __global__ void rerope_kernel(const T* __restrict__ src, T* __restrict__ dst, in
             }
             sj = ((int64_t)pg << page_shift) + (j & ((1 << page_shift) - 1));
         }
-        const T* sp = src + (((int64_t)layer * 2 + kv) * src_rows + sj) * W + e;
-        T* dp = dst + (((int64_t)layer * 2 + kv) * dst_rows + j) * W + e;
         float f[8];
-        Vec8<T>::load(sp, f);
+        Vec8<T>::load(sblk + sj * W + e, f);
         if (kv == 0) {
             const int c = chunk_of(cdst, n_chunks, j);
             const float2* t = cs + (size_t)c * half + (e % hd) / 2;
@@ -125,7 +123,7 @@ __global__ void rerope_kernel(const T* __restrict__ src, T* __restrict__ dst, in
                 f[2 * p + 1] = x0 * r.y + x1 * r.x;
             }
         }
-        Vec8<T>::store(dp, f);
+        Vec8<T>::store(dblk + (int64_t)j * W + e, f);
     }
 }
 
@@ -134,16 +132,21 @@ cudaError_t launch_rerope(const Model& m, const void* src, void* dst, int64_t sr
     const cb_config& c = m.cfg;
     const int W = c.n_kv_heads * c.head_dim, kvc = copy_v ? 2 : 1;
     const int L = layers > 0 ? layers : c.n_layers;
-    const int64_t items = (int64_t)L * kvc * n_ctx * (W / 8);
-    if (items == 0) return cudaSuccess;
-    const int grid = grid_for(items, 256, m.num_sms, 16);
+    const int64_t per_lk = (int64_t)n_ctx * (W / 8);
+    if (per_lk == 0) return cudaSuccess;
+    // about 16 resident blocks per SM over all (layer, K|V) blocks
+    int64_t bx = ((int64_t)m.num_sms * 16 + (int64_t)L * kvc - 1) / ((int64_t)L * kvc);
+    const int64_t need = (per_lk + 255) / 256;
+    if (bx > need) bx = need;
+    if (bx < 1) bx = 1;
+    const dim3 grid((unsigned)bx, (unsigned)(L * kvc));
     if (m.bf16)
         rerope_kernel<bf16><<<grid, 256, 0, s>>>((const bf16*)src, (bf16*)dst, src_rows, dst_rows, n_ctx, W,
-                                                 c.head_dim, L, kvc, m.chunk_dst, m.delta_cs, n_chunks, src_pages,
+                                                 c.head_dim, kvc, m.chunk_dst, m.delta_cs, n_chunks, src_pages,
                                                  page_shift, src_rows >> page_shift, m.status);
     else
         rerope_kernel<float><<<grid, 256, 0, s>>>((const float*)src, (float*)dst, src_rows, dst_rows, n_ctx, W,
-                                                  c.head_dim, L, kvc, m.chunk_dst, m.delta_cs, n_chunks, src_pages,
+                                                  c.head_dim, kvc, m.chunk_dst, m.delta_cs, n_chunks, src_pages,
                                                   page_shift, src_rows >> page_shift, m.status);
     return cudaGetLastError();
 }
