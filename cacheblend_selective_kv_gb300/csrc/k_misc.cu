@@ -38,6 +38,17 @@ template <> struct Vec8<float> {
     }
 };
 
+// each value rounded to T and back to float (identity for float)
+template <typename T> __device__ __forceinline__ void round_to(const float* v, float* out);
+template <> __device__ __forceinline__ void round_to<bf16>(const float* v, float* out) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) out[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+}
+template <> __device__ __forceinline__ void round_to<float>(const float* v, float* out) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) out[i] = v[i];
+}
+
 static inline int grid_for(int64_t items, int threads, int sms, int per_sm = 8) {
     int64_t b = (items + threads - 1) / threads;
     int64_t cap = (int64_t)sms * per_sm;
@@ -192,40 +203,64 @@ __global__ void rmsnorm_kernel(const float* __restrict__ h, const T* __restrict_
                                T* __restrict__ out_lo, int d, float eps) {
     grid_dep_launch();
     grid_dep_wait();
-    const int r = blockIdx.x;
+    // one CTA per row; the first RC eight-element chunks of each thread stay in registers between the
+    // sum of squares and the scaled write, so a row of up to RC * 8 * blockDim.x elements is read once
+    constexpr int RC = 4;
+    const int r = blockIdx.x, bd = blockDim.x, tid = threadIdx.x;
     const float* row = h + (size_t)r * d;
     __shared__ float red[32];
+    float f[RC][8];
     float ss = 0.f;
-    for (int e = threadIdx.x * 4; e < d; e += blockDim.x * 4) {
-        float4 v = *reinterpret_cast<const float4*>(row + e);
-        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+#pragma unroll
+    for (int c = 0; c < RC; ++c) {
+        const int e = (tid + c * bd) * 8;
+        if (e < d) {
+            Vec8<float>::load(row + e, f[c]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ss += f[c][i] * f[c][i];
+        }
+    }
+    for (int e = (tid + RC * bd) * 8; e < d; e += bd * 8) {
+        float t[8];
+        Vec8<float>::load(row + e, t);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss += t[i] * t[i];
     }
     ss = warp_sum(ss);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    if ((tid & 31) == 0) red[tid >> 5] = ss;
     __syncthreads();
-    if (threadIdx.x < 32) {
-        float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    if (tid < 32) {
+        float v = tid < (bd >> 5) ? red[tid] : 0.f;
         v = warp_sum(v);
-        if (threadIdx.x == 0) red[0] = v;
+        if (tid == 0) red[0] = v;
     }
     __syncthreads();
     const float scale = 1.0f / sqrtf(red[0] / (float)d + eps);
     T* o = out + (size_t)r * d;
-    for (int e = threadIdx.x * 8; e < d; e += blockDim.x * 8) {
-        float f[8], gg[8];
-        float4 a = *reinterpret_cast<const float4*>(row + e), b = *reinterpret_cast<const float4*>(row + e + 4);
-        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    T* ol = out_lo ? out_lo + (size_t)r * d : nullptr;
+    auto emit = [&](int e, float* v) {
+        float gg[8];
         Vec8<T>::load(g + e, gg);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = f[i] * scale * gg[i];
-        Vec8<T>::store(o + e, f);
-        if (out_lo) {            // remainder after rounding to T (split precision)
-            float r[8];
-            Vec8<T>::load(o + e, r);
+        for (int i = 0; i < 8; ++i) v[i] = v[i] * scale * gg[i];
+        Vec8<T>::store(o + e, v);
+        if (ol) {                // remainder after rounding to T (split precision)
+            float hi[8];
+            round_to<T>(v, hi);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) r[i] = f[i] - r[i];
-            Vec8<T>::store(out_lo + (size_t)blockIdx.x * d + e, r);
+            for (int i = 0; i < 8; ++i) hi[i] = v[i] - hi[i];
+            Vec8<T>::store(ol + e, hi);
         }
+    };
+#pragma unroll
+    for (int c = 0; c < RC; ++c) {
+        const int e = (tid + c * bd) * 8;
+        if (e < d) emit(e, f[c]);
+    }
+    for (int e = (tid + RC * bd) * 8; e < d; e += bd * 8) {
+        float t[8];
+        Vec8<float>::load(row + e, t);
+        emit(e, t);
     }
 }
 
