@@ -40,7 +40,7 @@ size_t act_size(const Model& m) { return m.bf16 ? 2 : 4; }
 void free_ws(Model& m) {
     void* ptrs[] = {m.h, m.hA, m.x, m.xA, m.q, m.attn, m.act, m.kf, m.vf, m.dev, m.rows, m.rows2, m.sel_local, m.iota,
                     m.rope, m.inv_freq, m.delta_cs, m.chunk_dst, m.chunk_delta, m.xfinal, m.status,
-                    m.x_lo, m.xA_lo, m.attn_lo, m.act_lo, m.q_lo, m.part_o, m.part_ml};
+                    m.x_lo, m.xA_lo, m.attn_lo, m.act_lo, m.q_lo, m.part_o, m.part_ml, m.attn_sched};
     for (void* p : ptrs)
         if (p) cudaFree(p);
 }
@@ -102,6 +102,7 @@ cb_status cb_model_create(const cb_config* cfg, const cb_weights* w, cb_model** 
     m->split = m->bf16 && c.precision == CB_PREC_SPLIT;
     m->x_lo = m->xA_lo = m->attn_lo = m->act_lo = m->q_lo = nullptr;
     m->part_o = m->part_ml = nullptr;
+    m->attn_sched = nullptr;
     if (cudaGetDevice(&m->device) != cudaSuccess) { delete m; return fail(CB_ERR_CUDA, "no CUDA device"); }
     cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device);
     m->part_items = m->bf16 ? 8 * m->num_sms : 0;
@@ -140,7 +141,8 @@ cb_status cb_model_create(const cb_config* cfg, const cb_weights* w, cb_model** 
         {&m->attn_lo, m->split ? T * nq * as : 0}, {&m->act_lo, m->split ? T * F * as : 0},
         {&m->q_lo, m->split ? T * nq * as : 0},
         {(void**)&m->part_o, (size_t)m->part_items * 128 * c.head_dim * 4},
-        {(void**)&m->part_ml, (size_t)m->part_items * 128 * 2 * 4}};
+        {(void**)&m->part_ml, (size_t)m->part_items * 128 * 2 * 4},
+        {(void**)&m->attn_sched, 64}};
     size_t total = 0;
     for (auto& a : allocs) {
         if (a.bytes == 0) continue;

@@ -36,6 +36,8 @@ constexpr int ROWS = 128;                // TMEM lanes per unit
 constexpr int NUM_THREADS = 352;         // K producer, MMA, 8 softmax warps, V producer
 constexpr int K_STAGES = 3, V_STAGES = 2;
 constexpr float RESCALE_LOG2 = 8.0f;     // lazy-rescale threshold (P <= 2^8)
+constexpr int SCHED_SLOTS = 4;           // work items published ahead to the consumer roles
+constexpr int SCHED_READERS = 10;        // V producer, MMA issuer, 8 softmax warps
 
 struct AttnArgs {
     int M;              // recomputed query rows
@@ -56,6 +58,7 @@ struct AttnArgs {
     float scale_log2;   // log2(e) / sqrt(hd)
     uint32_t idesc_qk, idesc_pv;
     unsigned* status;
+    unsigned* sched;    // [0] next work item to claim, [1] CTAs finished claiming; both zero between launches
 };
 
 // 2^x on the special-function unit (about 2 ulp; the result feeds a bf16 hi+lo pair)
@@ -194,7 +197,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t* o_free = o_full + 4;
     uint64_t* cmb_bar = o_free + 1;
     uint64_t* drain = cmb_bar + 1;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* sched_full = drain + 1;                 // [slot]: a work item (or -1: none left) published
+    uint64_t* sched_empty = sched_full + SCHED_SLOTS; // [slot]: every consumer role has read it
+    int* sched_u = reinterpret_cast<int*>(sched_empty + SCHED_SLOTS);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sched_u + SCHED_SLOTS);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -218,6 +224,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::mbar_init(ptx::smem_u32(o_free), 4);
         ptx::mbar_init(ptx::smem_u32(cmb_bar), 4);
         ptx::mbar_init(ptx::smem_u32(drain), 1);
+        for (int i = 0; i < SCHED_SLOTS; ++i) {
+            ptx::mbar_init(ptx::smem_u32(sched_full + i), 1);
+            ptx::mbar_init(ptx::smem_u32(sched_empty + i), SCHED_READERS);
+        }
         *abort = 0;
         ptx::fence_barrier_init();
         ptx::prefetch_tmap(&mq);
@@ -235,6 +245,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     grid_dep_launch();
     grid_dep_wait();                                     // q and the blended K/V of the previous kernels
 
+    // Work items are claimed at run time from a global counter, in unit order (longest query tiles
+    // first), by the Q/K producer, which skips empty items and publishes each claim through a ring of
+    // SCHED_SLOTS shared-memory slots; every other role reads the same sequence from the ring.  Returns
+    // the item, -1 when none is left, -2 when a wait gave up.  Called by a whole softmax warp or by the
+    // single thread of the V producer and the MMA issuer.
+    uint32_t sched_cnt = 0;
+    auto next_unit = [&](bool warp_wide) -> int {
+        const uint32_t slot = sched_cnt % SCHED_SLOTS, par = (sched_cnt / SCHED_SLOTS) & 1u;
+        if (!await(ptx::smem_u32(sched_full + slot), par, abort, a.status, 61, sched_cnt, -1)) return -2;
+        const int v = *reinterpret_cast<volatile int*>(sched_u + slot);
+        if (warp_wide) __syncwarp();
+        if (!warp_wide || lane == 0) ptx::mbar_arrive(ptx::smem_u32(sched_empty + slot));
+        ++sched_cnt;
+        return v;
+    };
+
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer: Q and K
         if (lane == 0) {
@@ -243,11 +269,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool q_issued = false;
             uint32_t q_par = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-                int qt, g, part, b0, b1;
-                unit_of(a, u, qt, g, part);
-                item_blocks(a, qt, part, b0, b1);
-                if (b0 >= b1) continue;
+            while (ok) {
+                int u, qt = 0, g = 0, part = 0, b0 = 0, b1 = 0;
+                do {                                     // claim the next non-empty item
+                    u = (int)atomicAdd(a.sched, 1u);
+                    if (u >= a.units) break;
+                    unit_of(a, u, qt, g, part);
+                    item_blocks(a, qt, part, b0, b1);
+                } while (b0 >= b1);
+                const bool none = u >= a.units;
+                {
+                    const uint32_t slot = sched_cnt % SCHED_SLOTS, par = (sched_cnt / SCHED_SLOTS) & 1u;
+                    if (!await(ptx::smem_u32(sched_empty + slot), par ^ 1u, abort, a.status, 60, sched_cnt, u)) break;
+                    sched_u[slot] = none ? -1 : u;
+                    ptx::mbar_arrive(ptx::smem_u32(sched_full + slot));
+                    ++sched_cnt;
+                }
+                if (none) break;
                 if (!await(ptx::smem_u32(q_empty), (q_cnt & 1u) ^ 1u, abort, a.status, 1, q_cnt, u)) break;
                 const uint32_t qb = ptx::smem_u32(q_full);
                 ptx::mbar_arrive_expect_tx(qb, NP * Q_BYTES);
@@ -273,6 +311,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ++k_cnt;
                 }
             }
+            // claiming is over for this CTA; the last CTA to get here re-arms the counter for the next launch
+            __threadfence();
+            if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
+                atomicExch(a.sched, 0u);
+                atomicExch(a.sched + 1, 0u);
+            }
             // every load this thread issued has landed before the CTA may exit
             if (q_issued) drain_wait(ptx::smem_u32(q_full), q_par, a.status);
             for (int i = 0; i < K_STAGES; ++i)
@@ -283,7 +327,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             uint32_t v_cnt = 0, issued = 0, issued_par = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+            while (ok) {
+                const int u = next_unit(false);
+                if (u < 0) break;
                 int qt, g, part, b0, b1;
                 unit_of(a, u, qt, g, part);
                 item_blocks(a, qt, part, b0, b1);
@@ -336,11 +382,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ptx::mma_commit(ptx::smem_u32(v_empty + st));
                 return true;
             };
-            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+            while (ok) {
+                const int u = next_unit(false);
+                if (u < 0) break;
                 int qt, g, part, b0, b1;
                 unit_of(a, u, qt, g, part);
                 item_blocks(a, qt, part, b0, b1);
-                if (b0 >= b1) continue;
                 const int nb = b1 - b0;
                 if (!await(ptx::smem_u32(q_full), q_cnt & 1u, abort, a.status, 4, q_cnt, u)) break;
                 ++q_cnt;
@@ -389,11 +436,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t o_tm = tmem + lane_base + O_COL + hf * HD;
         uint32_t sc = 0, unit_cnt = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+        while (ok) {
+            const int u = next_unit(true);
+            if (u < 0) break;
             int qt, g, part, b0, b1;
             unit_of(a, u, qt, g, part);
             item_blocks(a, qt, part, b0, b1);
-            if (b0 >= b1) continue;
             const int nb = b1 - b0;
             const int qi = qt * a.QT + row / a.G;
             const bool valid = qi < a.M;
@@ -616,7 +664,7 @@ bool get_encode() {
 template <int HD, bool SPLIT>
 size_t attn_smem() {
     const size_t np = SPLIT ? 2 : 1;
-    return 1024 + np * ROWS * HD * 2 + (size_t)(K_STAGES + V_STAGES) * BKV * HD * 2 + 2 * ROWS * sizeof(float) + 256;
+    return 1024 + np * ROWS * HD * 2 + (size_t)(K_STAGES + V_STAGES) * BKV * HD * 2 + 2 * ROWS * sizeof(float) + 512;
 }
 
 template <int HD, bool SPLIT>
@@ -711,6 +759,7 @@ cudaError_t launch_attention_tc(const Model& m, const void* qmap, const void* qm
     a.idesc_qk = ptx::idesc_bf16(ROWS, BKV);
     a.idesc_pv = ptx::idesc_bf16(ROWS, c.head_dim) | (1u << 16);    // B (V) is MN-major
     a.status = m.status;
+    a.sched = m.attn_sched;
     const int grid = a.units < m.num_sms ? a.units : m.num_sms;
     const CUtensorMap& mq = *reinterpret_cast<const CUtensorMap*>(qmap);
     const CUtensorMap& mql = *reinterpret_cast<const CUtensorMap*>(m.split ? qmap_lo : qmap);

@@ -143,6 +143,7 @@ struct Model {
     void* q_lo;           // low part of q (split precision only)
     float* part_o;        // attention key-range partials: [part_items][128][head_dim]
     float* part_ml;       // [part_items][128][2]
+    unsigned* attn_sched; // attention work-item counter and finished-CTA count (zero between launches)
     int part_items;
     float* kf;            // [max_tokens][nkv] fresh K at the check layer (fp32)
     float* vf;            // [max_tokens][nkv] fresh V at the check layer (fp32)
