@@ -738,7 +738,7 @@ cudaError_t launch_attention_tc(const Model& m, const void* qmap, const void* qm
     a.parts = 1;
     const int nb_max = (n_keys + BKV - 1) / BKV;
     a.part_blocks = nb_max;
-    int per_sm = 4;                              // work items aimed at per SM
+    int per_sm = 2;                              // work items aimed at per SM (measured best with run-time claiming)
     if (const char* v = getenv("CB_TUNE_ATTN_ITEMS")) per_sm = std::max(1, atoi(v));
     if (m.part_o && a.units < 2 * m.num_sms && nb_max > 4) {
         int parts = (per_sm * m.num_sms + a.units - 1) / a.units;
