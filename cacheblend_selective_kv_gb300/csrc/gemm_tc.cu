@@ -101,7 +101,9 @@ __device__ __forceinline__ void store_pair<bf16>(bf16* p, float a, float b) {
 // features are consecutive and lie in one region (regions and segments are multiples of 64 wide), so each
 // 16-token chunk is transposed through the warp's shared-memory staging area and written as 16-byte
 // vectors along the features of each token row.  Positions come from a per-warp shared-memory copy; the
-// (cos, sin) loads of the next 16 tokens are issued before the current 16 are processed.
+// (cos, sin) loads run DEEP ? two : one chunk of 16 tokens ahead (the shallow form saves 32 registers
+// for kernels with twice the epilogue warps, whose extra warps hide the latency instead).
+template <bool DEEP>
 __device__ __forceinline__ void qkv_tile(const TcArgs& a, const Unit& w, int row, int lane, int tok0, int ntok,
                                          uint32_t tbase, const int* wpos, uint32_t* stg) {
     const EpiParams& e = a.e;
@@ -120,11 +122,11 @@ __device__ __forceinline__ void qkv_tile(const TcArgs& a, const Unit& w, int row
     auto rope_at = [&](int t) {
         return (rot && t < ntok) ? e.rope[(size_t)wpos[t] * half + pair] : make_float2(1.f, 0.f);
     };
-    float2 cs[16], csn[16], csn2[16];
+    float2 cs[16], csn[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         cs[j] = rope_at(j);
-        csn[j] = rope_at(16 + j);
+        if constexpr (DEEP) csn[j] = rope_at(16 + j);
     }
     uint32_t vn[16];
     ptx::tmem_ld16_issue(tbase, vn);
@@ -135,9 +137,15 @@ __device__ __forceinline__ void qkv_tile(const TcArgs& a, const Unit& w, int row
         for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(vn[j]);
         if (c + 1 < nch) ptx::tmem_ld16_issue(tbase + (c + 1) * 16, vn);
         const int base = c * 16;
-        if (c + 2 < nch) {
+        float2 csn2[16];
+        if constexpr (DEEP) {
+            if (c + 2 < nch) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) csn2[j] = rope_at(base + 32 + j);
+                for (int j = 0; j < 16; ++j) csn2[j] = rope_at(base + 32 + j);
+            }
+        } else if (c + 1 < nch) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) csn[j] = rope_at(base + 16 + j);
         }
         const int nt = min(16, ntok - base);
         float r0[16], r1[16];
@@ -203,7 +211,7 @@ __device__ __forceinline__ void qkv_tile(const TcArgs& a, const Unit& w, int row
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             cs[j] = csn[j];
-            csn[j] = csn2[j];
+            if constexpr (DEEP) csn[j] = csn2[j];
         }
     }
 }
@@ -445,8 +453,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256;
             if (EPI == EPI_QKV) {
-                qkv_tile(a, w, row, lane, tok0, ntok, tbase, wpos,
-                         reinterpret_cast<uint32_t*>(spos + 4 * EPI_POS_INTS) + (warp - 2) * EPI_STG_WORDS);
+                qkv_tile<true>(a, w, row, lane, tok0, ntok, tbase, wpos,
+                               reinterpret_cast<uint32_t*>(spos + 4 * EPI_POS_INTS) + (warp - 2) * EPI_STG_WORDS);
                 __syncwarp();
             }
             for (int c = 0; EPI != EPI_QKV && c * 16 < ntok; ++c) {
@@ -492,7 +500,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // 64 features (the pair covers 128), so each feature's gate and up meet in one CTA's TMEM and the
 // epilogue exchanges them between lane quarters q and q ^ 2 through shared memory.
 // =================================================================================================
-constexpr int EPI_SMEM_PAIR = 4 * 2 * 32 * 17 * 4 > EPI_SMEM ? 4 * 2 * 32 * 17 * 4 : EPI_SMEM;   // SwiGLU: [quarter][slot][32 x 17] floats
+// Pair kernel epilogue warps: two per TMEM lane quarter (each takes half of a tile's 16-token chunks) for
+// the QKV and residual epilogues, whose last tile is exposed after the main loop; one per quarter for
+// SwiGLU, whose exchange buffers ([quarter][slot][32 x 17] floats) would otherwise cost a pipeline stage.
+constexpr int pair_epi_warps(int epi) { return epi == EPI_SWIGLU ? 4 : 8; }
+constexpr int pair_threads(int epi) { return 64 + 32 * pair_epi_warps(epi); }
+constexpr int pair_epi_smem(int epi) {
+    return epi == EPI_SWIGLU ? 4 * 2 * 32 * 17 * 4 : pair_epi_warps(epi) * (EPI_POS_INTS + EPI_STG_WORDS) * 4;
+}
 
 __device__ __forceinline__ void epi_swiglu_pair(const TcArgs& a, int feat, bool fv, int q, int lane, int tok0,
                                                 int ntok_c, int slot, const float* v, float* xs) {
@@ -522,11 +537,12 @@ __device__ __forceinline__ void epi_swiglu_pair(const TcArgs& a, int feat, bool 
 }
 
 template <int EPI, bool SPLIT>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mxl,
                      const __grid_constant__ CUtensorMap mw0, const __grid_constant__ CUtensorMap mw1,
                      const __grid_constant__ CUtensorMap mw2, const TcArgs a) {
     constexpr bool SWIGLU = EPI == EPI_SWIGLU;
+    constexpr int EW = pair_epi_warps(EPI);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int bh_bytes = (a.BN / 2) * 128;               // this CTA's half of a token tile (hi or lo)
@@ -552,7 +568,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(ptx::smem_u32(tfull + i), 1);
-            ptx::mbar_init(ptx::smem_u32(tempty + i), 8);
+            ptx::mbar_init(ptx::smem_u32(tempty + i), 2 * EW);     // every epilogue warp of both CTAs
         }
         ptx::mbar_init(ptx::smem_u32(drain), 1);
         *abort = 0;
@@ -651,7 +667,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
     } else {
         // ------------------------------------------------------------------ epilogue (both CTAs)
-        const int q = warp & 3;
+        const int q = warp & 3;                          // TMEM lane quarter this warp may access
+        const int ew = warp - 2;                         // epilogue warp index
+        const int hs = ew >> 2;                          // which half of a tile's chunks (EW == 8)
         const int row = q * 32 + lane;
         const uint32_t tempty0 = ptx::map_to_rank(ptx::smem_u32(tempty), 0);
         int acc = 0, gc = 0;
@@ -661,20 +679,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             if (!SWIGLU) w.lt = 2 * w.lt + (int)rank;
             const int tok0 = w.t * a.BN;
             const int ntok = min(a.BN, a.M - tok0);
-            int* wpos = spos + (warp - 2) * EPI_POS_INTS;
-            if (EPI == EPI_QKV) qkv_prefetch(a, w, row, lane, tok0, ntok, wpos);
+            // this warp's tokens [ta, tb) of the tile: with two warps per quarter the first takes the
+            // first ceil(chunks / 2) chunks of 16, the second the rest (possibly none)
+            int ta = 0, tb = ntok;
+            if (EW == 8) {
+                const int mid = min(ntok, ((ntok + 31) / 32) * 16);
+                ta = hs ? mid : 0;
+                tb = hs ? ntok : mid;
+            }
+            int* wpos = spos + ew * EPI_POS_INTS;
+            if (EPI == EPI_QKV && tb > ta) qkv_prefetch(a, w, row, lane, tok0 + ta, tb - ta, wpos);
             if (!ptx::mbar_wait(ptx::smem_u32(tfull + acc), acc_phase, abort, a.status)) break;
             ptx::tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256;
             if (EPI == EPI_QKV) {
-                qkv_tile(a, w, row, lane, tok0, ntok, tbase, wpos,
-                         reinterpret_cast<uint32_t*>(spos + 4 * EPI_POS_INTS) + (warp - 2) * EPI_STG_WORDS);
+                if (tb > ta)
+                    qkv_tile<EW == 4>(a, w, row, lane, tok0 + ta, tb - ta, tbase + ta, wpos,
+                                      reinterpret_cast<uint32_t*>(spos + EW * EPI_POS_INTS) + ew * EPI_STG_WORDS);
                 __syncwarp();
             } else if (EPI == EPI_RESID) {
-                for (int c = 0; c * 16 < ntok; ++c) {
+                for (int c = ta / 16; c * 16 < tb; ++c) {
                     float v[16];
                     ptx::tmem_ld16(tbase + c * 16, v);
-                    epi_resid(a, w, row, lane, tok0 + c * 16, v, sepi + (warp - 2) * (32 * 17));
+                    epi_resid(a, w, row, lane, tok0 + c * 16, v, sepi + ew * (32 * 17));
                 }
             } else {
                 const int feat = w.lt * 128 + (int)rank * 64 + (q & 1) * 32 + lane;
@@ -742,7 +769,7 @@ cudaError_t launch_pair(const CUtensorMap& mx, const CUtensorMap& mxl, const CUt
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    return launch_ex(pdl, gemm_pair_kernel<EPI, SPLIT>, dim3(grid), dim3(NUM_THREADS), smem, s, mx, mxl, *w0,
+    return launch_ex(pdl, gemm_pair_kernel<EPI, SPLIT>, dim3(grid), dim3(pair_threads(EPI)), smem, s, mx, mxl, *w0,
                      w1 ? *w1 : *w0, w2 ? *w2 : *w0, a);
 }
 
@@ -753,7 +780,7 @@ int pair_capacity(size_t smem) {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.blockDim = dim3(pair_threads(EPI), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -884,7 +911,7 @@ cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, c
     }
     a.ttiles = best_T;
     a.BN = best_BN;
-    const int epi_smem = pair ? EPI_SMEM_PAIR : EPI_SMEM;
+    const int epi_smem = pair ? pair_epi_smem(e.kind) : EPI_SMEM;
     const int b_rows = pair ? a.BN / 2 : a.BN;                 // token rows one CTA stages
     const int stage_bytes = (swiglu && !pair ? 2 * A_BYTES : A_BYTES) + (split ? 2 : 1) * b_rows * 128;
     const int budget = 227 * 1024 - 1024 - 256 - epi_smem;
