@@ -25,6 +25,12 @@ template <typename T> __device__ __forceinline__ T from_f(float x);
 template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
 template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
 
+// the pair (x0, x1) rotated by the angle whose (cos, sin) is r, with its roundings fixed (one rounded
+// product, then one fused multiply-add) so that every re-RoPE kernel produces the same bits
+__device__ __forceinline__ float2 rotate_pair(float x0, float x1, float2 r) {
+    return make_float2(__fmaf_rn(x0, r.x, -__fmul_rn(x1, r.y)), __fmaf_rn(x0, r.y, __fmul_rn(x1, r.x)));
+}
+
 // split of an fp32 value into two bf16 numbers: hi = rn(v), lo = rn(v - hi)
 __device__ __forceinline__ void split_bf16(float v, bf16& hi, bf16& lo) {
     hi = __float2bfloat16_rn(v);

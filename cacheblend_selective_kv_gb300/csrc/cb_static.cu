@@ -117,10 +117,9 @@ __global__ void static_rerope_kernel(T* kv, int64_t rows, int n_ctx, int W, int 
         load8<T>(p, f);
         const float2* t = cs + (size_t)lo * kMaxHalf + (e % hd) / 2;
         for (int q = 0; q < 4; ++q) {
-            const float2 r = t[q];
-            const float x0 = f[2 * q], x1 = f[2 * q + 1];
-            f[2 * q] = x0 * r.x - x1 * r.y;
-            f[2 * q + 1] = x0 * r.y + x1 * r.x;
+            const float2 y = cb::rotate_pair(f[2 * q], f[2 * q + 1], t[q]);
+            f[2 * q] = y.x;
+            f[2 * q + 1] = y.y;
         }
         store8<T>(p, f);
     }

@@ -128,10 +128,9 @@ __global__ void rerope_kernel(const T* __restrict__ src, T* __restrict__ dst, in
             const float2* t = cs + (size_t)c * half + (e % hd) / 2;
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
-                const float2 r = t[p];
-                const float x0 = f[2 * p], x1 = f[2 * p + 1];
-                f[2 * p] = x0 * r.x - x1 * r.y;
-                f[2 * p + 1] = x0 * r.y + x1 * r.x;
+                const float2 y = rotate_pair(f[2 * p], f[2 * p + 1], t[p]);
+                f[2 * p] = y.x;
+                f[2 * p + 1] = y.y;
             }
         }
         Vec8<T>::store(dblk + (int64_t)j * W + e, f);

@@ -145,6 +145,15 @@ def test_inplace_blend_equals_out_of_place(cb):
     model.close()
 
 
+def rotation_tol(base_k, ref_k):
+    """Bound on |GPU - oracle| for a K rotated in fp32 with fp32 (cos, sin) and rounded once to bf16:
+    one bf16 ulp of the result, plus the fp32 rounding of the products, a few 2^-24 of the rotated
+    pair's magnitude |x0| + |x1| (it dominates where the result cancels to near zero)."""
+    ulp = np.ldexp(1.0, np.frexp(np.abs(ref_k))[1] - 8)
+    pair = np.abs(base_k.reshape(base_k.shape[:-1] + (-1, 2))).sum(-1)
+    return ulp + np.ldexp(np.repeat(pair, 2, axis=-1), -20)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_rerope_in_place(cb, dtype):
     """cb_rerope rotates K of every layer by each chunk's delta and leaves V alone."""
@@ -166,11 +175,36 @@ def test_rerope_in_place(cb, dtype):
     assert np.array_equal(got[:, :, n_ctx:], base[:, :, n_ctx:]), "rows past the chunks changed"
     tol = 1e-5 if dtype == "f32" else 0.0
     err = np.abs(got[:, 0, :n_ctx] - ref[:, 0, :n_ctx])
-    if dtype == "bf16":   # a rotation rounded once to bf16: allow one ulp of the result
-        ulp = np.ldexp(1.0, np.frexp(np.abs(ref[:, 0, :n_ctx]))[1] - 8)
-        assert np.all(err <= ulp), float(err.max())
+    if dtype == "bf16":
+        assert np.all(err <= rotation_tol(base[:, 0, :n_ctx], ref[:, 0, :n_ctx])), float(err.max())
     else:
         assert err.max() <= tol, float(err.max())
+    model.close()
+
+
+def test_rerope_in_place_many_slabs(cb):
+    """cb_rerope over 2 KB rows (8 KV heads x 128, bf16): many 16-row slabs per layer, a ragged last slab,
+    chunk boundaries inside slabs, a one-row chunk, rows past the chunks left alone."""
+    ms = workload.ModelShape(2, 1024, 8, 8, 128, 256, 64, 5e5, "bf16")
+    w = workload.make_weights(ms, 0)
+    model = cb.BlendModel(ms.as_dict(), w, max_tokens=1100, max_chunks=16)
+    rng = np.random.default_rng(11)
+    chunks, dst = [], 0
+    for ln in (37, 200, 1, 333, 64, 299):
+        chunks.append((int(rng.integers(0, 30000)), dst, ln))
+        dst += ln
+    n_ctx, n_rows = dst, 1000
+    raw = workload.normal(6, 91, (2, 2, n_rows, 8, 128), 1.0, "bf16")
+    ref = oracle.rerope(raw, chunks, ms.rope_theta, "bf16")
+    kv = cb.to_device(raw)
+    cb.cb_rerope(model.handle, kv, n_rows, chunks)
+    torch.cuda.synchronize()
+    got = parity.bf16_to_f64(kv)
+    base = oracle.to_f64(raw)
+    assert np.array_equal(got[:, 1], base[:, 1]), "V changed"
+    assert np.array_equal(got[:, :, n_ctx:], base[:, :, n_ctx:]), "rows past the chunks changed"
+    err = np.abs(got[:, 0, :n_ctx] - ref[:, 0, :n_ctx])
+    assert np.all(err <= rotation_tol(base[:, 0, :n_ctx], ref[:, 0, :n_ctx])), float(err.max())
     model.close()
 
 
