@@ -124,6 +124,7 @@ def oracle_sample(spec: workload.WorkloadSpec, seed: int, ratio: float, sample_l
     once and kept; only the oracle's blend is timed."""
     import oracle
     shape = spec.shape
+    sample_layers = min(sample_layers, shape.n_layers)
     trunc = workload.ModelShape(**dict(shape.as_dict(), n_layers=sample_layers))
     key = (spec.name, seed, ratio, sample_layers)
     if key not in _SAMPLE:
@@ -137,8 +138,11 @@ def oracle_sample(spec: workload.WorkloadSpec, seed: int, ratio: float, sample_l
     dt = time.perf_counter() - t0
     scale = blend_flops(shape, shape.n_layers, spec.n_ctx, spec.n_query, k) / \
         blend_flops(shape, sample_layers, spec.n_ctx, spec.n_query, k)
-    desc = (f"fp64 numpy oracle, {spec.name} request (r={ratio}) on the first {sample_layers} of "
-            f"{shape.n_layers} layers; time scaled to the full blend by the FLOP ratio {scale:.2f}")
+    if sample_layers == shape.n_layers:
+        desc = f"fp64 numpy oracle, {spec.name} request (r={ratio}), the whole blend ({shape.n_layers} layers)"
+    else:
+        desc = (f"fp64 numpy oracle, {spec.name} request (r={ratio}) on the first {sample_layers} of "
+                f"{shape.n_layers} layers; time scaled to the full blend by the FLOP ratio {scale:.2f}")
     return dt, scale, desc
 
 
