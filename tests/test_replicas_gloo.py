@@ -53,3 +53,16 @@ def test_single_rank_needs_no_process_group():
     import bench
     value, ms = bench.replica_throughput(1, 100, 4, 200.0)
     assert value == pytest.approx(100 * 4 / 0.2) and ms == pytest.approx(50.0)
+
+
+def test_blend_floor_takes_the_larger_bound_per_class():
+    """Roofline time of a blend: per kernel class the larger of FLOPs / tensor peak and bytes / HBM peak."""
+    import bench
+    prof = [
+        {"name": "gemm", "flops": 2 * 1e12, "bytes": 2 * 1e9},     # per step: 1 TFLOP -> 1 ms at 1000 TF/s
+        {"name": "copy", "flops": 0, "bytes": 2 * 5e9},             # per step: 5 GB -> 1 ms at 5000 GB/s
+        {"name": "mixed", "flops": 2 * 1e9, "bytes": 2 * 10e9},     # bytes bound: 2 ms
+    ]
+    assert abs(bench.blend_floor_ms(prof, 2, 1000.0, 5000.0) - 4.0) < 1e-9
+    # no tensor peak (fp32 configuration): bytes only
+    assert abs(bench.blend_floor_ms(prof, 2, None, 5000.0) - (0.2 + 1.0 + 2.0)) < 1e-9
