@@ -89,12 +89,6 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, unsign
 }
 
 // ---- epilogues: one thread = one feature (TMEM lane), 16 consecutive token rows -------------------
-template <typename T>
-__device__ __forceinline__ void store_pair(T* p, float a, float b);
-template <>
-__device__ __forceinline__ void store_pair<bf16>(bf16* p, float a, float b) {
-    *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
-}
 
 // QKV epilogue of one tile: RoPE of q/k pairs (partner feature = lane ^ 1), q as bf16 (hi and, in split
 // precision, lo), k/v either into the blended cache at each token's position or as fp32 rows.  A warp's 32
@@ -777,8 +771,7 @@ cudaError_t launch_pair(const CUtensorMap& mx, const CUtensorMap& mxl, const CUt
 template <int EPI, bool SPLIT>
 int pair_capacity(size_t smem) {
     cudaFuncSetAttribute(gemm_pair_kernel<EPI, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof cfg);
+    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(pair_threads(EPI), 1, 1);
     cfg.dynamicSmemBytes = smem;

@@ -49,12 +49,6 @@ template <> __device__ __forceinline__ void round_to<float>(const float* v, floa
     for (int i = 0; i < 8; ++i) out[i] = v[i];
 }
 
-static inline int grid_for(int64_t items, int threads, int sms, int per_sm = 8) {
-    int64_t b = (items + threads - 1) / threads;
-    int64_t cap = (int64_t)sms * per_sm;
-    return (int)(b < cap ? (b > 0 ? b : 1) : cap);
-}
-
 // ------------------------------------------------------------------------------------------------
 // (cos, sin) of each chunk's position delta, in float64, and the chunk tables.
 // ------------------------------------------------------------------------------------------------
