@@ -206,7 +206,7 @@ def run_reference(args, spec, ws, rank):
         return
     ratio = args.ratio if args.ratio is not None else spec.ratios[0]
     seed = spec.seeds[0]
-    for _ in range(min(args.warmup, 1)):
+    for _ in range(args.warmup):
         oracle_sample(spec, seed, ratio)
     times, scale, desc = [], 1.0, ""
     for _ in range(args.steps):
@@ -215,13 +215,13 @@ def run_reference(args, spec, ws, rank):
     t = float(np.sum(times))
     value = spec.n_ctx * args.steps / t
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
-            "steps": args.steps, "warmup": min(args.warmup, 1), "ms_per_step": 1e3 * t / args.steps,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
             "latency_ms": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": spec.name, "n_ctx": spec.n_ctx, "n_query": spec.n_query, "ratio": ratio,
                        "seed": seed, "parallelism": "cpu"},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-                             "sample": desc + "; warm-up capped at one sample (nothing to warm on a CPU)"},
+                             "sample": desc},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
