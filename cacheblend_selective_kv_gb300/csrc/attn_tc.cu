@@ -670,13 +670,10 @@ size_t attn_smem() {
 template <int HD, bool SPLIT>
 cudaError_t launch_hd(const CUtensorMap& mq, const CUtensorMap& mql, const CUtensorMap& mkv, const AttnArgs& a,
                       int grid, cudaStream_t s, bool pdl) {
-    static bool set = false;
+    static std::atomic<uint64_t> done{0};
     const size_t sm = attn_smem<HD, SPLIT>();
-    if (!set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-        if (e != cudaSuccess) return e;
-        set = true;
-    }
+    const cudaError_t e = smem_limit_once(attn_tc_kernel<HD, SPLIT>, (int)sm, done);
+    if (e != cudaSuccess) return e;
     return launch_ex(pdl, attn_tc_kernel<HD, SPLIT>, dim3(grid), dim3(NUM_THREADS), sm, s, mq, mql, mkv, a);
 }
 

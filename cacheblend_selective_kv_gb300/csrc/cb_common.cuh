@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <string>
 #include <vector>
 
@@ -218,6 +219,20 @@ void tc_destroy(Model& m);
 cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, const GemmW& w, int N,
                            const EpiParams& e, cudaStream_t s, int* launches);
 enum { XBUF_X = 0, XBUF_XA = 1, XBUF_ATTN = 2, XBUF_ACT = 3 };
+
+// Raise kernel `k`'s dynamic shared-memory limit to `bytes` on the current device, once per device (CUDA
+// keeps the attribute per device; `done` holds one bit per device ordinal below 64).
+template <typename... KArgs>
+cudaError_t smem_limit_once(void (*k)(KArgs...), int bytes, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 // Launch `k` on `s`, with programmatic dependent launch when `pdl` (the kernel calls grid_dep_wait
 // before its first global access, so it may start while the previous kernel on the stream drains).

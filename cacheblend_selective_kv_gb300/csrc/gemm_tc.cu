@@ -742,13 +742,9 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
 template <int EPI, bool SPLIT>
 cudaError_t launch_kernel(const CUtensorMap& mx, const CUtensorMap& mxl, const CUtensorMap* w0, const CUtensorMap* w1,
                           const CUtensorMap* w2, const TcArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e =
-            cudaFuncSetAttribute(gemm_tc_kernel<EPI, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> done{0};
+    const cudaError_t e = smem_limit_once(gemm_tc_kernel<EPI, SPLIT>, 232448, done);
+    if (e != cudaSuccess) return e;
     return launch_ex(pdl, gemm_tc_kernel<EPI, SPLIT>, dim3(grid), dim3(NUM_THREADS), smem, s, mx, mxl, *w0,
                      w1 ? *w1 : *w0, w2 ? *w2 : *w0, a);
 }
@@ -756,13 +752,9 @@ cudaError_t launch_kernel(const CUtensorMap& mx, const CUtensorMap& mxl, const C
 template <int EPI, bool SPLIT>
 cudaError_t launch_pair(const CUtensorMap& mx, const CUtensorMap& mxl, const CUtensorMap* w0, const CUtensorMap* w1,
                         const CUtensorMap* w2, const TcArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e =
-            cudaFuncSetAttribute(gemm_pair_kernel<EPI, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> done{0};
+    const cudaError_t e = smem_limit_once(gemm_pair_kernel<EPI, SPLIT>, 232448, done);
+    if (e != cudaSuccess) return e;
     return launch_ex(pdl, gemm_pair_kernel<EPI, SPLIT>, dim3(grid), dim3(pair_threads(EPI)), smem, s, mx, mxl, *w0,
                      w1 ? *w1 : *w0, w2 ? *w2 : *w0, a);
 }
