@@ -1,7 +1,13 @@
-"""Plant plausible mistakes in the CPU oracle and confirm that a pin catches each one.
+"""Plant plausible mistakes in the CPU oracle and confirm that a pin catches each one: in its building
+blocks (RoPE, attention, RMSNorm, deviation, selection, rounding, gradual counts) and in the blend's own
+control flow (which rows compete for selection, scatter before attention, which keys later layers see,
+which row gives the logits).
 
 Every mistake is planted in the oracle module on the CPU (monkeypatch), never in the
 CUDA path."""
+import inspect
+import textwrap
+
 import numpy as np
 import pytest
 
@@ -12,6 +18,7 @@ _orig_rope, _orig_attention, _orig_rmsnorm = ob.rope, ob.attention, ob.rmsnorm
 _orig_dev, _orig_sel, _orig_freqs, _orig_silu = ob.deviation, ob.select_hkvd, ob.rope_freqs, ob.silu
 _orig_rerope, _orig_round = ob.rerope, ob.round_bf16
 _orig_counts = ob.gradual_counts
+_orig_blend = ob.blend
 
 
 def rope_sign_flipped(x, pos, theta):
@@ -97,6 +104,50 @@ def gradual_counts_first_only(n_ctx, ratios):
     return [ks[0]] * len(ks)
 
 
+def rerope_rotates_v(cached_kv, chunks, theta, store):
+    """V rotated by the position delta as well as K."""
+    out = _orig_rerope(cached_kv, chunks, theta, store)
+    swapped = np.ascontiguousarray(np.asarray(cached_kv)[:, ::-1])
+    out[:, 1] = _orig_rerope(swapped, chunks, theta, store)[:, 0]
+    return out
+
+
+def _mutated(fn, *edits):
+    """`fn` recompiled from its own source with snippets replaced, given as (old, new) pairs.  Each old
+    snippet must occur once, so a change to the oracle that removes it fails loudly here instead of
+    planting nothing."""
+    src = textwrap.dedent(inspect.getsource(fn))
+    for old, new in edits:
+        assert src.count(old) == 1, f"mutation anchor not found once in {fn.__name__}: {old!r}"
+        src = src.replace(old, new)
+    ns = dict(vars(ob))
+    exec(compile(src, f"<mutated {fn.__name__}>", "exec"), ns)
+    return ns[fn.__name__]
+
+
+# the blend's own control flow
+blend_query_rows_in_pool = _mutated(          # query rows (no cache: compared with zeros) compete for the k slots
+    _orig_blend,
+    ("sel = select_hkvd(dev, kk) if selected is None",
+     "sel = select_hkvd(np.concatenate([dev, deviation(k_new[n_ctx:], v_new[n_ctx:], 0 * k_new[n_ctx:], "
+     "0 * v_new[n_ctx:])]), kk) if selected is None"))
+blend_query_rows_in_pool.__name__ = "blend_query_rows_in_pool"
+blend_attends_before_scatter = _mutated(
+    _orig_blend,
+    ("    out_kv[1, 0, A] = round_store(k_new[A], store)\n",
+     "    stale = out_kv[1].astype(np.float64).copy()\n    out_kv[1, 0, A] = round_store(k_new[A], store)\n"),
+    ("o = attention(q[A], out_kv[1, 0].astype(np.float64), out_kv[1, 1].astype(np.float64), A, pos, Hkv)",
+     "o = attention(q[A], stale[0], stale[1], A, pos, Hkv)"))
+blend_attends_before_scatter.__name__ = "blend_attends_before_scatter"
+blend_attends_recomputed_rows_only = _mutated(
+    _orig_blend,
+    ("o = attention(q, out_kv[layer, 0].astype(np.float64), out_kv[layer, 1].astype(np.float64), A, pos, Hkv)",
+     "o = attention(q, out_kv[layer, 0, A].astype(np.float64), out_kv[layer, 1, A].astype(np.float64), A, A, Hkv)"))
+blend_attends_recomputed_rows_only.__name__ = "blend_attends_recomputed_rows_only"
+blend_logits_of_first_row = _mutated(_orig_blend, ("logits = m.logits(hA[-1])", "logits = m.logits(hA[0])"))
+blend_logits_of_first_row.__name__ = "blend_logits_of_first_row"
+
+
 MUTATIONS = [
     ("rope", rope_sign_flipped), ("rope_freqs", rope_freq_halved), ("rope", rope_half_split),
     ("attention", attention_gqa_modulo), ("attention", attention_no_scale), ("attention", attention_strict_causal),
@@ -105,6 +156,9 @@ MUTATIONS = [
     ("select_hkvd", select_ties_high), ("select_hkvd", select_smallest),
     ("rerope", rerope_wrong_direction), ("round_bf16", round_truncates),
     ("gradual_counts", gradual_counts_floor), ("gradual_counts", gradual_counts_first_only),
+    ("rerope", rerope_rotates_v),
+    ("blend", blend_query_rows_in_pool), ("blend", blend_attends_before_scatter),
+    ("blend", blend_attends_recomputed_rows_only), ("blend", blend_logits_of_first_row),
 ]
 
 
