@@ -414,7 +414,7 @@ def main():
         top = max(kernels, key=lambda n_: kernels[n_]["ms_total"])
         e = kernels[top]
         pinfo = next(p for p in prof if p["name"] == top)
-        traffic = load_traffic(top)
+        traffic = load_traffic(top, spec.name)
         if (top.startswith("gemm") or top == "attention") and shape.dtype == "bf16":
             ach = pinfo["flops"] / pinfo["launches"] / (e["ms_total"] / e["launches"] / 1e3) / 1e12
             roofline = {"kernel": top, "bound": "tensor", "achieved": ach, "peak": tensor_peak, "unit": "TFLOP/s",
@@ -558,16 +558,16 @@ def run_matcher(args, cb, ws, rank, local):
     index.close()
 
 
-def load_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it still matches the
-    source it was taken from (else None)."""
+def load_traffic(kernel: str, workload_name: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was captured on this
+    workload's per-layer shapes and still matches the source it was taken from (else None)."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
     try:
         d = json.load(open(p))
         ent = d.get(kernel)
-        if not ent:
+        if not ent or ent.get("workload") != workload_name:
             return None
         import hashlib
         src = os.path.join(ROOT, ent["source"])

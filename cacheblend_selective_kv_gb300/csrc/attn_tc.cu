@@ -18,7 +18,8 @@
 // S/P is double buffered in TMEM; a buffer is reused for S once the PV MMAs that read its P are done.
 // K blocks are released as soon as their S MMAs complete and V blocks once their PV MMAs do, so the
 // K loads run up to three blocks ahead.  V is consumed as an MN-major operand from its [key][dim]
-// layout.
+// layout.  The persistent CTAs claim units at run time (longest query tiles first) from a counter in
+// global memory; long key ranges are cut into parts merged by attn_combine_kernel.
 #include <cudaTypedefs.h>
 
 #include <algorithm>

@@ -66,3 +66,17 @@ def test_blend_floor_takes_the_larger_bound_per_class():
     assert abs(bench.blend_floor_ms(prof, 2, 1000.0, 5000.0) - 4.0) < 1e-9
     # no tensor peak (fp32 configuration): bytes only
     assert abs(bench.blend_floor_ms(prof, 2, None, 5000.0) - (0.2 + 1.0 + 2.0)) < 1e-9
+
+
+def test_traffic_lookup_needs_matching_workload_and_source():
+    """The committed DRAM-traffic figure of a kernel is used only for the workload it was captured on,
+    and only while the kernel's source is the one it was taken from."""
+    import json
+    import os
+    import bench
+    d = json.load(open(os.path.join(bench.ROOT, "profiles", "ncu_traffic.json")))
+    for kernel, ent in d.items():
+        got = bench.load_traffic(kernel, ent["workload"])
+        assert got in (None, ent["dram_bytes_per_launch_full"])
+        assert bench.load_traffic(kernel, "llama8b-32k" if ent["workload"] != "llama8b-32k" else "llama8b-3k") is None
+    assert bench.load_traffic("no-such-kernel", "llama8b-3k") is None
