@@ -208,6 +208,20 @@ def test_rerope_in_place_many_slabs(cb):
     model.close()
 
 
+def test_diag_words_after_a_clean_blend(cb):
+    """cb_model_diag: 16 words; after a blend that met no error, the status bits and the record of a
+    bounded wait that gave up are both zero."""
+    spec, w, req, caches, ratio = setup_case("tiny-fp32")
+    model = cb.BlendModel(spec.shape.as_dict(), w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks)
+    tokens = torch.from_numpy(req.tokens).cuda()
+    model.blend(tokens, cached_tensor(caches, "f32"), req.chunks, ratio)
+    words = cb.cb_model_diag(model.handle)
+    assert len(words) == 16
+    assert words[0] == 0 and words[1] == 0, words[:8]
+    assert model.status() == 0
+    model.close()
+
+
 def test_topk_is_exact_on_gpu_deviations(cb):
     """The GPU's set is exactly the top-k (ties to the lower row) of the GPU's own deviations."""
     spec, w, req, caches, _ = setup_case("small-bf16")
