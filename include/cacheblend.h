@@ -33,7 +33,7 @@ extern "C" {
 typedef enum {
     CB_OK = 0,
     CB_ERR_INVALID_ARG = -1,   /* a pointer, size, layout or ratio is out of range */
-    CB_ERR_UNSUPPORTED = -2,   /* valid but not supported by this build (e.g. head_dim) */
+    CB_ERR_UNSUPPORTED = -2,   /* valid but not supported by this library (e.g. head_dim) */
     CB_ERR_OOM = -3,           /* workspace allocation failed at model creation */
     CB_ERR_CUDA = -4,          /* a CUDA call or kernel launch failed */
     CB_ERR_INTERNAL = -5

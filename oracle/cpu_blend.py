@@ -8,7 +8,7 @@ Source of every step: the CacheBlend deep-dive page ("CacheBlend 完全拆解:RA
 KV 缓存拼接,为什么还要重算一小部分 token").  Section names are quoted in the
 docstrings below.
 
-Readings taken where the page leaves a step open (each is listed in the design doc):
+Readings taken where the page leaves a step open:
   R1  the check layer (full computation + deviation + selection) is layer index 1,
       the first layer whose input has seen other chunks; layer 0 recomputes hidden
       states for every row but reuses the (context-free) cached layer-0 K/V.

@@ -6,7 +6,7 @@ filter, resolve, choose the requester's occupant, verify tokens, mark seen), "å…
 (chunk, old_st, cur_st) ascending by cur_st, at most one per chunk, overlaps resolved by the caller with
 leftmost-greedy) and "ä¸ƒ" (the blend keeps the earlier of two overlapping matches).
 
-Readings (listed in DESIGN.md):
+Readings where the pages leave a step open:
   M1  fingerprint of a window t_0..t_{C-1}: Horner's rule h = h * B + t_j over the tokens in order,
       modulo 2^64, tokens as unsigned 32-bit values, B = 0x9E3779B97F4A7C15 (the page's fleet constant).
   M2  a fingerprint names one content: the first content stored under it; a different content with the
