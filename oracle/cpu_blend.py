@@ -229,19 +229,23 @@ def select_hkvd(dev: np.ndarray, k: int) -> np.ndarray:
     return np.sort(order[:k]).astype(np.int64)
 
 
-def rerope(cached_kv: np.ndarray, chunks, theta: float, store: str) -> np.ndarray:
+def rerope(cached_kv: np.ndarray, chunks, theta: float, store: str, out=None) -> np.ndarray:
     """Place chunk caches at their new offsets: K <- R_{dst-src} K, V unchanged.
 
     Section "位置恢复、KV 存储与加载流水线": a key cached at position p as k_p = R_p k
     becomes R_{n-p} k_p = R_n k at its new position n; V carries no position.
     cached_kv [L][2][n_ctx][Hkv][hd] holds the context rows in placed (dst) order.
-    Returns float64 values rounded to the storage type."""
-    kv = to_f64(cached_kv).copy()
-    for src, dst, ln in chunks:
-        delta = dst - src
-        rows = slice(dst, dst + ln)
-        for layer in range(kv.shape[0]):
-            kv[layer, 0, rows] = round_store(rope(kv[layer, 0, rows], np.full(ln, delta), theta), store)
+    Returns float64 values rounded to the storage type (``out``, if given, receives them instead:
+    any float array of the same shape that holds the storage type exactly)."""
+    cached_kv = np.asarray(cached_kv)
+    kv = np.empty(cached_kv.shape, np.float64) if out is None else out
+    for layer in range(cached_kv.shape[0]):          # one layer at a time (memory only)
+        kl = np.array(to_f64(cached_kv[layer, 0]), np.float64, copy=True)   # never a view of the input
+        for src, dst, ln in chunks:
+            rows = slice(dst, dst + ln)
+            kl[rows] = round_store(rope(kl[rows], np.full(ln, dst - src), theta), store)
+        kv[layer, 0] = kl
+        kv[layer, 1] = to_f64(cached_kv[layer, 1])
     return kv
 
 
@@ -268,7 +272,7 @@ def validate_chunks(chunks, n_tokens: int) -> int:
 
 
 def blend(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratio: float, store: str, selected=None,
-          keep_exact: bool = False) -> dict:
+          keep_exact: bool = False, exact_layers=None) -> dict:
     """One CacheBlend blend (sections "核心思想" and "选 token", Figures 5 and 9).
 
     1. re-RoPE the cached chunk K/V to their placed positions (V copied);
@@ -283,6 +287,9 @@ def blend(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratio: float, sto
 
     ``keep_exact`` also returns ``out_kv_exact``: the values before their rounding to the
     storage type (used to compare another implementation's rounded output against them).
+    ``exact_layers`` (optional, a set of layer indices) returns ``exact_rows``: for each of those
+    layers, (rows, K, V) of the rows computed fresh there, before rounding -- the same values as
+    ``out_kv_exact`` at those rows, without a float64 copy of the whole cache.
     ``selected`` (optional) replaces the top-k choice by a given set of k rows -- used only
     to follow another implementation through a tie inside the comparison band.
 
@@ -298,11 +305,17 @@ def blend(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratio: float, sto
     kv_dtype = np.float64 if store == "f64" else np.float32   # bf16/f32 values are exact in f32
     out_kv = np.zeros((L, 2, N, Hkv, hd), kv_dtype)
     if n_ctx:
-        out_kv[:, :, :n_ctx] = rerope(cached_kv, chunks, m.theta, store)
+        rerope(cached_kv, chunks, m.theta, store, out=out_kv[:, :, :n_ctx])
     # unrounded values of everything stored (re-RoPE'd rows: the rotation before rounding)
     exact = np.zeros((L, 2, N, Hkv, hd), np.float64) if keep_exact else None
     if keep_exact and n_ctx:
-        exact[:, :, :n_ctx] = rerope(cached_kv, chunks, m.theta, "f64")
+        rerope(cached_kv, chunks, m.theta, "f64", out=exact[:, :, :n_ctx])
+    exact_layers = set(exact_layers or ())
+    exact_rows = {}
+
+    def keep_rows(layer, rows, k_new, v_new):
+        if layer in exact_layers:
+            exact_rows[layer] = (np.asarray(rows).copy(), np.array(k_new, np.float64), np.array(v_new, np.float64))
 
     h = m.embed_rows(tokens)
 
@@ -314,6 +327,7 @@ def blend(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratio: float, sto
     out_kv[0, 1, n_ctx:] = round_store(vq, store)
     if keep_exact:
         exact[0, 0, n_ctx:], exact[0, 1, n_ctx:] = kq, vq
+    keep_rows(0, pos[n_ctx:], kq, vq)
     o = attention(q, out_kv[0, 0].astype(np.float64), out_kv[0, 1].astype(np.float64), pos, pos, Hkv)
     h = m.finish(W, h, o)
     del W
@@ -331,6 +345,7 @@ def blend(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratio: float, sto
     out_kv[1, 1, A] = round_store(v_new[A], store)
     if keep_exact:
         exact[1, 0, A], exact[1, 1, A] = k_new[A], v_new[A]
+    keep_rows(1, A, k_new[A], v_new[A])
     o = attention(q[A], out_kv[1, 0].astype(np.float64), out_kv[1, 1].astype(np.float64), A, pos, Hkv)
     hA = m.finish(W, h[A], o)
     del W, h, q, k_new, v_new
@@ -343,12 +358,14 @@ def blend(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratio: float, sto
         out_kv[layer, 1, A] = round_store(v_a, store)
         if keep_exact:
             exact[layer, 0, A], exact[layer, 1, A] = k_a, v_a
+        keep_rows(layer, A, k_a, v_a)
         o = attention(q, out_kv[layer, 0].astype(np.float64), out_kv[layer, 1].astype(np.float64), A, pos, Hkv)
         hA = m.finish(W, hA, o)
         del W
 
     logits = m.logits(hA[-1])
-    return dict(out_kv=out_kv, out_kv_exact=exact, logits=logits, selected=sel, dev=dev, k=kk, rows=A)
+    return dict(out_kv=out_kv, out_kv_exact=exact, exact_rows=exact_rows, logits=logits, selected=sel, dev=dev, k=kk,
+                rows=A)
 
 
 def deviation_rows(cfg: dict, weights: dict, tokens, cached_kv, chunks, rows, store: str) -> np.ndarray:
@@ -445,10 +462,10 @@ def blend_gradual(cfg: dict, weights: dict, tokens, cached_kv, chunks, ratios, s
     kv_dtype = np.float64 if store == "f64" else np.float32
     out_kv = np.zeros((L, 2, N, Hkv, hd), kv_dtype)
     if n_ctx:
-        out_kv[:, :, :n_ctx] = rerope(cached_kv, chunks, m.theta, store)
+        rerope(cached_kv, chunks, m.theta, store, out=out_kv[:, :, :n_ctx])
     exact = np.zeros((L, 2, N, Hkv, hd), np.float64) if keep_exact else None
     if keep_exact and n_ctx:
-        exact[:, :, :n_ctx] = rerope(cached_kv, chunks, m.theta, "f64")
+        rerope(cached_kv, chunks, m.theta, "f64", out=exact[:, :, :n_ctx])
 
     def store_rows(layer, rows, k_new, v_new):
         out_kv[layer, 0, rows] = round_store(k_new, store)

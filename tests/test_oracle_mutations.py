@@ -85,8 +85,8 @@ def select_smallest(dev, k):
     return np.sort(np.argsort(np.asarray(dev), kind="stable")[:k])
 
 
-def rerope_wrong_direction(cached_kv, chunks, theta, store):
-    return _orig_rerope(cached_kv, [(dst, src, ln) for src, dst, ln in chunks], theta, store)
+def rerope_wrong_direction(cached_kv, chunks, theta, store, out=None):
+    return _orig_rerope(cached_kv, [(dst, src, ln) for src, dst, ln in chunks], theta, store, out=out)
 
 
 def round_truncates(x):
@@ -104,12 +104,14 @@ def gradual_counts_first_only(n_ctx, ratios):
     return [ks[0]] * len(ks)
 
 
-def rerope_rotates_v(cached_kv, chunks, theta, store):
+def rerope_rotates_v(cached_kv, chunks, theta, store, out=None):
     """V rotated by the position delta as well as K."""
-    out = _orig_rerope(cached_kv, chunks, theta, store)
+    res = _orig_rerope(cached_kv, chunks, theta, store)
     swapped = np.ascontiguousarray(np.asarray(cached_kv)[:, ::-1])
-    out[:, 1] = _orig_rerope(swapped, chunks, theta, store)[:, 0]
-    return out
+    res[:, 1] = _orig_rerope(swapped, chunks, theta, store)[:, 0]
+    if out is not None:
+        out[...] = res
+    return res
 
 
 def _mutated(fn, *edits):
