@@ -104,15 +104,17 @@ __global__ void static_rerope_kernel(T* kv, int64_t rows, int n_ctx, int W, int 
     const int64_t total = (int64_t)L * per_layer;
     for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
          it += (int64_t)gridDim.x * blockDim.x) {
-        const int layer = (int)(it / per_layer);
-        const int rem = (int)(it - (int64_t)layer * per_layer);
-        const int j = rem / W8, e = (rem - j * W8) * 8;
+        // 64-bit throughout: one layer of a large buffer can hold more than 2^31 vectors
+        const int64_t layer = it / per_layer;
+        const int64_t rem = it - layer * per_layer;
+        const int64_t j = rem / W8;
+        const int e = (int)(rem - j * W8) * 8;
         int lo = 0, hi = n_chunks - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (cdst[mid] <= j) lo = mid; else hi = mid - 1;
+            if ((int64_t)cdst[mid] <= j) lo = mid; else hi = mid - 1;
         }
-        T* p = kv + ((int64_t)layer * 2 * rows + j) * W + e;
+        T* p = kv + (layer * 2 * rows + j) * W + e;
         float f[8];
         load8<T>(p, f);
         const float2* t = cs + (size_t)lo * kMaxHalf + (e % hd) / 2;
@@ -125,7 +127,9 @@ __global__ void static_rerope_kernel(T* kv, int64_t rows, int n_ctx, int W, int 
     }
 }
 
-// Device address of the scratch on the current device, queried once per device.
+// Device address of the scratch on the current device, queried once per device and kept for the life
+// of the process: the library must not be used on a device after cudaDeviceReset there (the array's
+// address may change with the new context).
 cb_status scratch_on_current_device(unsigned char** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
@@ -155,6 +159,8 @@ cb_status cb_rerope_static(void* kv, int64_t n_rows, int32_t n_layers, int32_t n
     if (!kv) return fail(CB_ERR_INVALID_ARG, "cb_rerope_static: kv is NULL");
     if (n_layers < 1 || n_kv_heads < 1 || n_rows < 0) return fail(CB_ERR_INVALID_ARG, "cb_rerope_static: bad shape");
     if (head_dim != 64 && head_dim != 128) return fail(CB_ERR_UNSUPPORTED, "cb_rerope_static: head_dim must be 64 or 128");
+    if ((int64_t)n_kv_heads * head_dim > (int64_t)1 << 24)
+        return fail(CB_ERR_INVALID_ARG, "cb_rerope_static: n_kv_heads * head_dim exceeds 2^24");
     if (dtype != CB_F32 && dtype != CB_BF16) return fail(CB_ERR_INVALID_ARG, "cb_rerope_static: dtype must be CB_F32 or CB_BF16");
     if (!(rope_theta > 0)) return fail(CB_ERR_INVALID_ARG, "cb_rerope_static: rope_theta must be > 0");
     if (n_chunks < 0 || (n_chunks > 0 && !chunks)) return fail(CB_ERR_INVALID_ARG, "cb_rerope_static: bad chunk list");
@@ -178,6 +184,7 @@ cb_status cb_rerope_static(void* kv, int64_t n_rows, int32_t n_layers, int32_t n
         t.delta[i] = c.dst_pos - c.src_pos;
     }
     if (at > n_rows) return fail(CB_ERR_INVALID_ARG, "cb_rerope_static: chunks cover more rows than the buffer has");
+    if (at > INT32_MAX) return fail(CB_ERR_INVALID_ARG, "cb_rerope_static: chunks cover more than 2^31 - 1 rows");
     if (n_chunks == 0) return CB_OK;
     unsigned char* scratch = nullptr;
     cb_status st = scratch_on_current_device(&scratch);
