@@ -1,14 +1,30 @@
 """GPU parity at the full 8B-shape sizes, in the launch configuration bench.py times.
 
-The chunk caches here are drawn by the workload generator (i.i.d. normal at the K/V scale of the
-random-init model): a genuine per-chunk prefill at this shape costs the fp64 oracle ~8 TFLOP per
-chunk.  The smaller configurations use genuine per-chunk prefills."""
+What each configuration is checked against:
+  * 3K (r = 0.15, seed 2) and the 8K sweep's r = 0.05 (seed 3), r = 0.15 (seed 4) and r = 0.30 (seed 5):
+    the whole blend of the CPU oracle, run here: the selected set (1e-3 band), every row's K/V at every
+    layer, every context row's deviation and the logits.
+  * 32K r = 0.15 (seed 6): stored results of the same oracle (tests/golden/fullsize_*.npz, written by
+    tests/golden/make_fullsize_golden.py, which calls only the oracle and the input generator; this blend
+    takes the oracle about 20 CPU minutes): the selected set, every context row's deviation, all logits,
+    the K/V of 32 recomputed rows (the last query row among them) at layers 1, 2, 16 and 31, and every
+    unselected row at layers 1, 16 and 31 against the oracle's re-RoPE of the cache.
+  * the other six runs of the 8K sweep: the selection is the top-k of the GPU's own deviations, sampled
+    rows' deviations against the oracle, unselected rows against the re-RoPE'd cache.
+  * genuine per-chunk caches: two 512-token chunks prefilled alone by the oracle and placed six times
+    (3072 context rows); the GPU's prefill of one of them against the oracle's, then the whole blend.
+The other 8B-shape tests draw their chunk caches from the generator (i.i.d. normal at the K/V scale of
+the random-init model), which both sides read.
+"""
+import time
+
 import numpy as np
 import pytest
 
 import oracle
 import parity
 import workload
+from golden import make_fullsize_golden as golden
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 torch = pytest.importorskip("torch")
@@ -24,81 +40,135 @@ def cb():
     return cbm
 
 
-def test_llama8b_3k_full_blend(cb):
-    spec = workload.WORKLOADS["llama8b-3k"]
-    shape, seed, ratio = spec.shape, spec.seeds[0], spec.ratios[0]
-    w = workload.make_weights(shape, seed)
-    req = workload.make_request(spec, seed, ratio)
-    caches = workload.synthetic_cache(shape, seed, spec.n_ctx, workload.kv_std(shape))
-    model = cb.BlendModel(shape.as_dict(), w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks)
-    cached = torch.from_numpy(caches.view(np.int16)).cuda().view(torch.bfloat16)
-    out = model.blend(torch.from_numpy(req.tokens).cuda(), cached, req.chunks, ratio, want_dev=True)
-    torch.cuda.synchronize()
-    assert model.status() == 0
-    g_sel = out["selected"].cpu().numpy()
-    g_kv = parity.bf16_to_f64(out["out_kv"])
-    g_lg = parity.bf16_to_f64(out["logits"])
-    g_dev = out["dev"].cpu().numpy().astype(np.float64)
-    model.close()
-    del cached
-    ref = oracle.blend(shape.as_dict(), w, req.tokens, caches, req.chunks, ratio, "bf16", keep_exact=True)
-    diff = parity.assert_selection(g_sel, ref["selected"], ref["dev"], ref["k"])
+def _bf16_tensor(a):
+    """Values that are bfloat16 numbers (bit patterns as uint16, or float32 values) -> a bf16 tensor on the GPU."""
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda().to(torch.bfloat16)
+
+
+def _compare_full(spec, w, tokens, caches, chunks, ratio, res, label, cascade=None):
+    """The GPU result `res` against a whole oracle blend run now: selection, every row's K/V at every layer,
+    every context row's deviation, logits.  Prints the per-layer errors and the oracle's time.  `cascade`
+    names the stored oracle spread whose per-layer bounds replace 2e-2 where that spread exceeds it."""
+    cfg = spec.shape.as_dict()
+    t0 = time.time()
+    ref = oracle.blend(cfg, w, tokens, caches, chunks, ratio, "bf16", keep_exact=True)
+    secs = time.time() - t0
+    diff = parity.assert_selection(res["selected"], ref["selected"], ref["dev"], ref["k"])
+    dev_rel = parity.dev_error(res["dev"], ref["dev"], ref["k"])
     if diff:
-        ref = oracle.blend(shape.as_dict(), w, req.tokens, caches, req.chunks, ratio, "bf16", selected=g_sel,
-                           keep_exact=True)
+        ref = oracle.blend(cfg, w, tokens, caches, chunks, ratio, "bf16", selected=res["selected"], keep_exact=True)
+    g_kv = res["kv"]
     rows = ref["rows"]
-    for l in (0, 1, 2, shape.n_layers // 2, shape.n_layers - 1):
-        mx, n_over, n_nb = parity.kv_error(g_kv[l][:, rows], ref["out_kv_exact"][l][:, rows], "bf16")
-        print(f"layer {l}: max abs {mx:.4f}, beyond tol {n_over}, of which bf16 neighbours {n_nb}")
-    dev_rel = np.abs(g_dev - ref["dev"]) / ref["dev"]
-    print(f"selection differs in {len(diff)} rows; deviation rel err max {dev_rel.max():.2e}")
-    print(f"logits max abs {np.abs(g_lg - ref['logits']).max():.4f}")
-    parity.assert_kv(g_kv, ref["out_kv_exact"], "bf16")
-    parity.assert_logits(g_lg, ref["logits"], "bf16")
-
-
-_MODELS = {}
-
-
-def _model_for(cb, spec, seed):
-    """Weights and a model handle per (workload, seed), kept for the next test of the same seed (one at a
-    time: the 8B weights are 16 GB on each side)."""
-    key = (spec.name, seed)
-    if key not in _MODELS:
-        for k in list(_MODELS):
-            _MODELS.pop(k)[1].close()
-        w = workload.make_weights(spec.shape, seed)
-        _MODELS[key] = (w, cb.BlendModel(spec.shape.as_dict(), w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks))
-    return _MODELS[key]
-
-
-def _gpu_blend(cb, spec, seed, ratio, caches, want_dev=True, keep=False):
-    shape = spec.shape
-    req = workload.make_request(spec, seed, ratio)
-    if keep:
-        w, model = _model_for(cb, spec, seed)
+    L = spec.shape.n_layers
+    for l in (0, 1, 2, L // 2, L - 1):
+        mx, n_over, n_ex = parity.kv_error(g_kv[l][:, rows], ref["out_kv_exact"][l][:, rows], "bf16")
+        print(f"{label} layer {l} recomputed rows: max abs {mx:.4f}, {n_over} beyond 2e-2 (exempt, |x| >= 8: {n_ex})")
+    print(f"{label}: oracle {secs:.0f} s; selection differs in {len(diff)} rows (all in the band); "
+          f"deviation rel err max {dev_rel.max():.2e}; logits max abs {np.abs(res['logits'] - ref['logits']).max():.4f}")
+    assert dev_rel.max() < 2e-3, float(dev_rel.max())
+    if cascade is None:
+        parity.assert_kv(g_kv, ref["out_kv_exact"], "bf16", f"{label} K/V")
+        parity.assert_logits(res["logits"], ref["logits"], "bf16")
     else:
-        w = workload.make_weights(shape, seed)
-        model = cb.BlendModel(shape.as_dict(), w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks)
-    cached = torch.from_numpy(caches.view(np.int16)).cuda().view(torch.bfloat16)
-    out = model.blend(torch.from_numpy(req.tokens).cuda(), cached, req.chunks, ratio, want_dev=want_dev)
+        kv_max, kv_mean, lg_tol = parity.cascade_bounds(cascade)
+        for l in range(L):
+            parity.assert_kv(g_kv[l], ref["out_kv_exact"][l], "bf16", f"{label} layer {l} K/V", tol=kv_max[l])
+            m = float(np.mean(np.abs(g_kv[l][:, rows] - ref["out_kv_exact"][l][:, rows])))
+            assert m <= kv_mean[l], (l, m, kv_mean[l])
+        assert np.max(np.abs(res["logits"] - ref["logits"])) <= lg_tol
+        over = sum(int(np.sum(np.abs(g_kv[l] - ref["out_kv_exact"][l]) > 2e-2)) for l in range(L))
+        print(f"{label}: {over} elements beyond 2e-2 (the oracle's own spread under a rounding-sized "
+              f"perturbation reaches {max(kv_max) / 1.5:.4f})")
+    return ref
+
+
+def _gpu_blend(cb, model, tokens, cached, chunks, ratio):
+    out = model.blend(torch.from_numpy(np.asarray(tokens, np.int32)).cuda(), cached, chunks, ratio, want_dev=True)
     torch.cuda.synchronize()
     assert model.status() == 0
-    res = dict(selected=out["selected"].cpu().numpy(), logits=parity.bf16_to_f64(out["logits"]), k=out["k"])
-    if want_dev:
-        res["dev"] = out["dev"].cpu().numpy().astype(np.float64)
-    res["kv"] = out["out_kv"]          # stays on the device; sampled below
-    del cached
-    return w, req, res, model
+    return dict(selected=out["selected"].cpu().numpy(), logits=parity.bf16_to_f64(out["logits"]), k=out["k"],
+                dev=out["dev"].cpu().numpy().astype(np.float64), kv_dev=out["out_kv"])
 
 
-def _kv_rows(res, layer, kv, rows):
-    t = res["kv"][layer, kv, torch.as_tensor(rows, device=res["kv"].device)]
-    return parity.bf16_to_f64(t)
+FULL_ORACLE = [("llama8b-3k", 2, 0.15), ("llama8b-8k", 3, 0.05), ("llama8b-8k", 4, 0.15), ("llama8b-8k", 5, 0.30)]
 
 
-def _sampled_checks(spec, w, req, res, caches, ratio, rng, n_sample=48):
-    """Checks that need no full oracle blend: the selection is exactly the top-k of the GPU's own
+@pytest.mark.parametrize("name,seed,ratio", FULL_ORACLE)
+def test_fullsize_against_whole_oracle_blend(cb, name, seed, ratio):
+    """3K and 8K blends (16 shuffled chunks at 8K, r = 0.05, 0.15, 0.30) against the whole oracle blend."""
+    spec = workload.WORKLOADS[name]
+    w = workload.make_weights(spec.shape, seed)
+    req = workload.make_request(spec, seed, ratio)
+    caches = workload.synthetic_cache(spec.shape, seed, spec.n_ctx, workload.kv_std(spec.shape))
+    model = cb.BlendModel(spec.shape.as_dict(), w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks)
+    res = _gpu_blend(cb, model, req.tokens, _bf16_tensor(caches), req.chunks, ratio)
+    res["kv"] = parity.bf16_to_f64(res.pop("kv_dev"))
+    model.close()
+    _compare_full(spec, w, req.tokens, caches, req.chunks, ratio, res, f"{name} seed {seed} r={ratio}",
+                  cascade="blend-8k-r0.30" if (name, ratio) == ("llama8b-8k", 0.30) else None)
+
+
+STORED = [("llama8b-32k", 6, 0.15)]
+
+
+@pytest.mark.parametrize("name,seed,ratio", STORED)
+def test_fullsize_against_stored_oracle_results(cb, name, seed, ratio):
+    """32K r = 0.15 against the oracle's stored results for the same seeded inputs.  cb_blend's selection
+    and deviations are compared with the oracle's; the stored K/V and logits follow the oracle's own set,
+    so they are compared with cb_blend_hkvd given that set (bit-identical to cb_blend when the sets agree)."""
+    g = np.load(golden.golden_path(name, seed, ratio))
+    spec, w, req, caches = golden.make_inputs(name, seed, ratio)
+    assert np.array_equal(golden.fingerprint(spec, w, req, caches), g["fingerprint"]), \
+        "the input generator made other inputs here than where the stored oracle results were written"
+    k = int(g["k"])
+    ref_sel = np.flatnonzero(np.unpackbits(g["selected_mask"])[:spec.n_ctx]).astype(np.int32)
+    ref_dev = g["dev"].astype(np.float64)
+    model = cb.BlendModel(spec.shape.as_dict(), w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks)
+    cached = _bf16_tensor(caches)
+    res = _gpu_blend(cb, model, req.tokens, cached, req.chunks, ratio)
+    assert res["k"] == k
+    diff = parity.assert_selection(res["selected"], ref_sel, ref_dev, k)
+    dev_rel = parity.dev_error(res["dev"], ref_dev, k)
+    assert dev_rel.max() < 2e-3, float(dev_rel.max())
+    kv = res["kv_dev"]
+    if diff:   # follow the oracle's set
+        out = model.blend_hkvd(torch.from_numpy(req.tokens).cuda(), cached, req.chunks,
+                               torch.from_numpy(ref_sel).cuda(), out_kv=kv)
+        torch.cuda.synchronize()
+        assert model.status() == 0
+        logits = parity.bf16_to_f64(out["logits"])
+    else:
+        logits = res["logits"]
+    lg = parity.assert_logits(logits, g["logits"].astype(np.float64), "bf16")
+    # recomputed rows: the stored sample, at the stored layers
+    rows = torch.as_tensor(g["rows"].astype(np.int64), device=kv.device)
+    kv_max = 0.0
+    for li, layer in enumerate(g["kv_layers"]):
+        got = parity.bf16_to_f64(kv[int(layer)][:, rows])
+        kv_max = max(kv_max, parity.assert_kv(got, g["kv"][li].astype(np.float64), "bf16", f"layer {layer} K/V"))
+    # unselected context rows: the re-RoPE'd cache, every row, at three layers
+    L = spec.shape.n_layers
+    unsel = np.setdiff1d(np.arange(spec.n_ctx), ref_sel)
+    layers = [1, L // 2, L - 1]
+    placed = oracle.rerope(caches[layers], req.chunks, spec.shape.rope_theta, "bf16")
+    base = oracle.to_f64(caches[layers])
+    ut = torch.as_tensor(unsel, device=kv.device)
+    for li, layer in enumerate(layers):
+        got_k = parity.bf16_to_f64(kv[layer, 0][ut])
+        got_v = parity.bf16_to_f64(kv[layer, 1][ut])
+        assert np.all(np.abs(got_k - placed[li, 0, unsel]) <= parity.rotation_tol(base[li, 0, unsel], placed[li, 0, unsel]))
+        assert np.array_equal(got_v, base[li, 1, unsel])
+    model.close()
+    print(f"{name} seed {seed} r={ratio}: selection differs in {len(diff)} rows (all in the band"
+          f"{'; K/V and logits taken with the oracle set' if diff else ''}); deviation rel err max {dev_rel.max():.2e}; "
+          f"logits max abs {lg:.4f}; sampled recomputed K/V max abs {kv_max:.4f}; {len(unsel)} unselected rows at "
+          f"layers {layers} equal the re-RoPE'd cache")
+
+
+def _sampled_checks(spec, w, req, res, caches, rng, n_sample=48):
+    """Checks that need no whole oracle blend: the selection is exactly the top-k of the GPU's own
     deviations; the deviations of sampled context rows match the oracle's row-restricted deviation;
     unselected context rows hold the re-RoPE'd cache at every layer."""
     shape = spec.shape
@@ -112,75 +182,109 @@ def _sampled_checks(spec, w, req, res, caches, ratio, rng, n_sample=48):
     unsel = np.array([r for r in rows if r not in sel])
     layers = [0, 1, shape.n_layers // 2, shape.n_layers - 1]
     placed = oracle.rerope(caches[layers], req.chunks, shape.rope_theta, "bf16")
+    ut = torch.as_tensor(unsel, device=res["kv_dev"].device)
     for li, layer in enumerate(layers):
         for kv in (0, 1):
-            got = _kv_rows(res, layer, kv, unsel)
+            got = parity.bf16_to_f64(res["kv_dev"][layer, kv][ut])
             ref = placed[li, kv, unsel]
             ulp = np.ldexp(1.0, np.frexp(np.abs(ref))[1] - 8)
             assert np.all(np.abs(got - ref) <= ulp), (layer, kv)
     return rel.max()
 
 
-def test_llama8b_8k_r005_full_blend_seed3(cb):
-    """8K context, 16 shuffled chunks, r = 0.05: the whole blend against the oracle."""
-    spec = workload.WORKLOADS["llama8b-8k"]
-    seed, ratio = 3, 0.05
-    caches = workload.synthetic_cache(spec.shape, seed, spec.n_ctx, workload.kv_std(spec.shape))
-    w, req, res, model = _gpu_blend(cb, spec, seed, ratio, caches)
-    assert [c[1] for c in req.chunks] == [512 * i for i in range(16)]
-    g_kv = parity.bf16_to_f64(res["kv"])
-    model.close()
-    ref = oracle.blend(spec.shape.as_dict(), w, req.tokens, caches, req.chunks, ratio, "bf16", keep_exact=True)
-    diff = parity.assert_selection(res["selected"], ref["selected"], ref["dev"], ref["k"])
-    if diff:
-        ref = oracle.blend(spec.shape.as_dict(), w, req.tokens, caches, req.chunks, ratio, "bf16",
-                           selected=res["selected"], keep_exact=True)
-    print(f"8K r=0.05: {len(diff)} rows in the tie band; kv max {parity.kv_error(g_kv, ref['out_kv_exact'], 'bf16')[0]:.4f}")
-    parity.assert_kv(g_kv, ref["out_kv_exact"], "bf16")
-    parity.assert_logits(res["logits"], ref["logits"], "bf16")
+_MODELS = {}
 
 
-C4_RUNS = [(s, r) for s in (3, 4, 5) for r in (0.05, 0.15, 0.30) if (s, r) != (3, 0.05)]
+def _model_for(cb, spec, seed):
+    """Weights and a model handle per seed, kept for the next test of the same seed (one at a time: the 8B
+    weights are 16 GB on each side)."""
+    key = (spec.name, seed)
+    if key not in _MODELS:
+        for kk in list(_MODELS):
+            _MODELS.pop(kk)[1].close()
+        w = workload.make_weights(spec.shape, seed)
+        _MODELS[key] = (w, cb.BlendModel(spec.shape.as_dict(), w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks))
+    return _MODELS[key]
 
 
-@pytest.mark.parametrize("seed,ratio", C4_RUNS)
+C4_SAMPLED = [(s, r) for s in (3, 4, 5) for r in (0.05, 0.15, 0.30) if (s, r) not in ((3, 0.05), (4, 0.15), (5, 0.30))]
+
+
+@pytest.mark.parametrize("seed,ratio", C4_SAMPLED)
 def test_llama8b_8k_sampled(cb, seed, ratio):
-    """The 8K configuration's sweep (seeds 3-5, each with its own shuffled chunk order, r in {0.05, 0.15,
-    0.30}; seed 3 at r = 0.05 runs against the full oracle above): sampled checks on every other run."""
+    """The rest of the 8K sweep (seeds 3-5, each with its own shuffled chunk order, r in {0.05, 0.15, 0.30}):
+    sampled checks on every run the whole-blend tests above do not cover."""
     spec = workload.WORKLOADS["llama8b-8k"]
     caches = workload.synthetic_cache(spec.shape, seed, spec.n_ctx, workload.kv_std(spec.shape))
-    w, req, res, model = _gpu_blend(cb, spec, seed, ratio, caches, keep=True)
-    rel = _sampled_checks(spec, w, req, res, caches, ratio, np.random.default_rng(seed))
+    w, model = _model_for(cb, spec, seed)
+    req = workload.make_request(spec, seed, ratio)
+    res = _gpu_blend(cb, model, req.tokens, _bf16_tensor(caches), req.chunks, ratio)
+    rel = _sampled_checks(spec, w, req, res, caches, np.random.default_rng(seed))
     print(f"8K seed {seed} r={ratio}: sampled deviation rel err {rel:.2e}")
-    if (seed, ratio) == C4_RUNS[-1]:
-        for k in list(_MODELS):
-            _MODELS.pop(k)[1].close()
+    if (seed, ratio) == C4_SAMPLED[-1]:
+        for kk in list(_MODELS):
+            _MODELS.pop(kk)[1].close()
 
 
-def test_llama8b_32k_sampled(cb):
-    """32K context (64 chunks + 128 query tokens), r = 0.15: sampled checks at full size."""
-    spec = workload.WORKLOADS["llama8b-32k"]
-    seed, ratio = spec.seeds[0], spec.ratios[0]
-    caches = workload.synthetic_cache(spec.shape, seed, spec.n_ctx, workload.kv_std(spec.shape))
-    w, req, res, model = _gpu_blend(cb, spec, seed, ratio, caches)
-    rel = _sampled_checks(spec, w, req, res, caches, ratio, np.random.default_rng(seed), n_sample=32)
-    print(f"32K r=0.15: sampled deviation rel err {rel:.2e}")
+def check_prefill_layers(g_kv, exact, label):
+    """A plain prefill recomputes every row at every layer, and every layer's K/V is rounded to bf16 before
+    the next rows and layers read it.  Two implementations whose sums differ in the last float32 bits round a
+    small share of those values to the other bf16 neighbour, and each such difference perturbs the attention
+    of every later row a little, so the two drift apart with depth (a cascade of storage roundings, not of
+    arithmetic error).  The oracle shows the same drift against itself when its stored values move by 1e-5
+    (tests/golden/cascade_spread.json).  Layer 0, before any cascade, is held to the blend's bound (2e-2);
+    every layer to max(2e-2, 1.5 x the oracle's own spread) max-abs and 1.5 x its spread mean-abs."""
+    kv_max, kv_mean, _ = parity.cascade_bounds("prefill-8b")
+    parity.assert_kv(g_kv[0], exact[0], "bf16", f"{label} layer 0 K/V")
+    for l in range(g_kv.shape[0]):
+        err = np.abs(g_kv[l] - exact[l])
+        print(f"{label} layer {l}: max abs {err.max():.4f} (bound {kv_max[l]:.4f}), mean {err.mean():.2e} "
+              f"(bound {kv_mean[l]:.2e})")
+        parity.assert_kv(g_kv[l], exact[l], "bf16", f"{label} layer {l} K/V", tol=kv_max[l])
+        assert err.mean() <= kv_mean[l], (l, float(err.mean()), kv_mean[l])
+
+
+def test_llama8b_genuine_chunk_caches(cb):
+    """Chunk caches that are genuine per-chunk prefills at the 8B shape: two 512-token chunks A and B, each
+    prefilled alone at positions 0..511 by the oracle, placed as A B A B A B (3072 context rows) before a
+    64-token query, r = 0.15.  First the GPU's own prefill of A (cb_blend with no chunks, the caller's
+    fallback and the bench's cache maker) against the oracle's: K/V of every layer and the logits.  Then the
+    blend against the whole oracle blend.  The first chunk sits where it was prefilled, so its rows deviate
+    only by the cache's bf16 rounding (the causal prefix): none of them may be selected."""
+    spec = workload.WORKLOADS["llama8b-3k"]
+    shape, seed, ratio = spec.shape, spec.seeds[0], spec.ratios[0]
+    cfg = shape.as_dict()
+    w = workload.make_weights(shape, seed)
+    req = workload.make_request(spec, seed, ratio)
+    A, B = req.chunk_tokens[0], req.chunk_tokens[1]
+    t0 = time.time()
+    pre_a = oracle.blend(cfg, w, A, None, [], 0.0, "bf16", keep_exact=True)
+    pre_b = oracle.prefill(cfg, w, B, "bf16")
+    t_pre = time.time() - t0
+    model = cb.BlendModel(cfg, w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks)
+    out = model.blend(torch.from_numpy(A).cuda(), None, [], 0.0)
+    torch.cuda.synchronize()
+    assert model.status() == 0
+    g_pre = parity.bf16_to_f64(out["out_kv"])
+    pre_lg = float(np.max(np.abs(parity.bf16_to_f64(out["logits"]) - pre_a["logits"])))
+    assert pre_lg <= parity.cascade_bounds("prefill-8b")[2], pre_lg
+    check_prefill_layers(g_pre, pre_a["out_kv_exact"], "8B 512-token prefill")
+    print(f"8B 512-token prefill: oracle {t_pre:.0f} s for two chunks; logits max abs {pre_lg:.4f}")
+
+    order = [pre_a, pre_b] * 3
+    toks = [A, B] * 3
+    caches = np.concatenate([p["out_kv"] for p in order], axis=2).astype(np.float32)   # bf16 values
+    chunks = [(0, 512 * i, 512) for i in range(6)]
+    tokens = np.concatenate(toks + [req.query]).astype(np.int32)
+    res = _gpu_blend(cb, model, tokens, _bf16_tensor(caches), chunks, ratio)
+    res["kv"] = parity.bf16_to_f64(res.pop("kv_dev"))
     model.close()
-
-
-def test_llama8b_32k_full_reuse(cb):
-    """32K context at r = 0 (full KV reuse): the query rows' K/V at every layer and the logits
-    against the oracle; every context row is the re-RoPE'd cache."""
-    spec = workload.WORKLOADS["llama8b-32k"]
-    seed = spec.seeds[0]
-    caches = workload.synthetic_cache(spec.shape, seed, spec.n_ctx, workload.kv_std(spec.shape))
-    w, req, res, model = _gpu_blend(cb, spec, seed, 0.0, caches, want_dev=False)
-    q_rows = np.arange(spec.n_ctx, spec.n_tokens)
-    g_q = np.stack([np.stack([_kv_rows(res, l, kv, q_rows) for kv in (0, 1)]) for l in range(spec.shape.n_layers)])
-    model.close()
-    ref = oracle.blend(spec.shape.as_dict(), w, req.tokens, caches, req.chunks, 0.0, "bf16", keep_exact=True)
-    parity.assert_kv(g_q, ref["out_kv_exact"][:, :, spec.n_ctx:], "bf16", "query-row K/V")
-    parity.assert_logits(res["logits"], ref["logits"], "bf16")
+    ref = _compare_full(spec, w, tokens, caches, chunks, ratio, res, "8B genuine caches")
+    thr = parity.threshold(ref["dev"], ref["k"])
+    print(f"first chunk: oracle deviation max {ref['dev'][:512].max():.3e}, GPU {res['dev'][:512].max():.3e}; "
+          f"threshold {thr:.3e}; other chunks' median {np.median(ref['dev'][512:]):.3e}")
+    assert ref["dev"][:512].max() < 1e-3 * thr and res["dev"][:512].max() < 1e-3 * thr
+    assert not np.any(res["selected"] < 512)
 
 
 def test_llama8b_3k_gradual(cb):
@@ -200,8 +304,8 @@ def test_llama8b_3k_gradual(cb):
 
 def test_llama8b_3k_streamed_matches_device_resident(cb):
     """The 8B-shape 3K blend with its chunk caches streamed from pinned host memory layer by layer: K/V
-    and logits within the parity tolerances of the device-resident blend (the residual GEMMs add split-K
-    partial sums in a run-dependent order), and the copied-back K/V equal to the device K/V."""
+    and logits equal, bit for bit, to the device-resident blend's, and the copied-back K/V equal to the
+    device K/V."""
     spec = workload.WORKLOADS["llama8b-3k"]
     shape, seed, ratio = spec.shape, spec.seeds[0], spec.ratios[0]
     w = workload.make_weights(shape, seed)
@@ -217,8 +321,7 @@ def test_llama8b_3k_streamed_matches_device_resident(cb):
     assert model.status() == 0
     assert torch.equal(kv_host, b["out_kv"].cpu())
     ka, kb = parity.bf16_to_f64(a["out_kv"]), parity.bf16_to_f64(b["out_kv"])
-    # 2e-2, or one bf16 step at the value (two roundings of sums taken in different orders)
-    ulp = np.ldexp(1.0, np.frexp(np.maximum(np.abs(ka), 1e-30))[1] - 8)
-    assert np.all(np.abs(ka - kb) <= np.maximum(2e-2, ulp))
-    assert np.max(np.abs(parity.bf16_to_f64(a["logits"]) - parity.bf16_to_f64(b["logits"]))) <= 3e-2
+    # the same kernels on the same values, every reduction in a fixed order: the same bits
+    assert np.array_equal(ka, kb)
+    assert torch.equal(a["logits"], b["logits"])
     model.close()
