@@ -27,7 +27,8 @@ EXPORTED = ("cb_model_create", "cb_model_destroy", "cb_rerope", "cb_blend", "cb_
             "cb_rerope_static", "cb_model_diag", "cb_load_time", "cb_controller_ratio", "cb_pick_storage",
             "cb_blend_paged", "cb_kv_gather_pages", "cb_kv_scatter_pages", "cb_pages_create", "cb_pages_destroy",
             "cb_pages_alloc", "cb_pages_retain", "cb_pages_release", "cb_pages_plan_write", "cb_pages_count",
-            "cb_pages_free", "cb_index_create", "cb_index_destroy", "cb_index_size", "cb_index_match")
+            "cb_pages_free", "cb_index_create", "cb_index_destroy", "cb_index_size", "cb_index_match",
+            "cb_select_hkvd", "cb_blend_hkvd")
 CB_STATIC_MAX_CHUNKS = 256
 CB_STATUS_BAD_TOKEN, CB_STATUS_WAIT_TIMEOUT, CB_STATUS_BAD_ROW = 1, 2, 4
 
@@ -153,6 +154,11 @@ def lib() -> ctypes.CDLL:
         L.cb_index_match.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, vp, vp]
         L.cb_selected_count.restype = i32
         L.cb_selected_count.argtypes = [i32, ctypes.c_double]
+        L.cb_select_hkvd.restype = ctypes.c_int
+        L.cb_select_hkvd.argtypes = [vp, i32, i32, vp, vp]
+        L.cb_blend_hkvd.restype = ctypes.c_int
+        L.cb_blend_hkvd.argtypes = [vp, vp, i32, vp, ctypes.POINTER(CbChunk), i32, vp, i32, vp, vp,
+                                    ctypes.POINTER(CbStats), vp]
         L.cb_profile_enable.restype = ctypes.c_int
         L.cb_profile_enable.argtypes = [vp, i32, i32]
         L.cb_profile_read.restype = i32
@@ -180,6 +186,11 @@ def _check(code: int):
 
 def cb_selected_count(n_ctx: int, ratio: float) -> int:
     return int(lib().cb_selected_count(n_ctx, ratio))
+
+
+def cb_select_hkvd(dev, n: int, k: int, out_rows, stream=None) -> None:
+    """The k rows of largest dev[0..n) (ties to the lower row), ascending, into out_rows (device tensors)."""
+    _check(lib().cb_select_hkvd(_ptr(dev), n, k, _ptr(out_rows), _stream(stream)))
 
 
 def _chunks(chunks):
@@ -245,6 +256,18 @@ def cb_blend(handle: int, tokens, n_tokens: int, cached_kv, chunks, ratio: float
     _check(lib().cb_blend(handle, _ptr(tokens), int(n_tokens), _ptr(cached_kv), _chunks(chunks), len(chunks),
                           float(ratio), _ptr(out_kv), _ptr(out_logits), _ptr(out_selected), _ptr(out_dev),
                           ctypes.byref(st) if stats else None, _stream(stream)))
+    if stats:
+        return {f: getattr(st, f) for f, _ in CbStats._fields_}
+    return None
+
+
+def cb_blend_hkvd(handle: int, tokens, n_tokens: int, cached_kv, chunks, hkvd, k: int, out_kv, out_logits,
+                  stream=None, stats: bool = False):
+    """A blend whose recomputed context rows are the caller's (device int32 [k], ascending)."""
+    st = CbStats()
+    _check(lib().cb_blend_hkvd(handle, _ptr(tokens), int(n_tokens), _ptr(cached_kv), _chunks(chunks), len(chunks),
+                               _ptr(hkvd), int(k), _ptr(out_kv), _ptr(out_logits), ctypes.byref(st) if stats else None,
+                               _stream(stream)))
     if stats:
         return {f: getattr(st, f) for f, _ in CbStats._fields_}
     return None
@@ -512,6 +535,17 @@ class BlendModel:
         if stats:
             out["stats"] = st
         return out
+
+    def blend_hkvd(self, tokens, cached_kv, chunks, hkvd, out_kv=None, stream=None):
+        """Run cb_blend_hkvd with the given recomputed context rows (device int32, ascending); returns
+        dict(out_kv, logits).  Asynchronous on `stream`."""
+        import torch
+        n = int(tokens.shape[0])
+        if out_kv is None:
+            out_kv = self.kv_buffer(n)
+        logits = torch.empty(self.shape["vocab"], dtype=torch.float32, device=self.device)
+        cb_blend_hkvd(self.handle, tokens, n, cached_kv, chunks, hkvd, int(hkvd.numel()), out_kv, logits, stream)
+        return dict(out_kv=out_kv, logits=logits)
 
     def blend_gradual(self, tokens, cached_kv, chunks, ratios, out_kv=None, stream=None, want_dev=False,
                       stats=False):

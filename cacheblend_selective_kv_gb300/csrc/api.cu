@@ -38,7 +38,8 @@ cb_status fail(cb_status code, const char* fmt, ...) {
 size_t act_size(const Model& m) { return m.bf16 ? 2 : 4; }
 
 void free_ws(Model& m) {
-    void* ptrs[] = {m.h, m.hA, m.x, m.xA, m.q, m.attn, m.act, m.kf, m.vf, m.dev, m.rows, m.rows2, m.sel_local, m.iota,
+    void* ptrs[] = {m.h, m.hA, m.x, m.xA, m.q, m.attn, m.act, m.kf, m.vf, m.dev, m.dev_part, m.part_h, m.rows, m.rows2,
+                    m.sel_local, m.iota,
                     m.rope, m.inv_freq, m.delta_cs, m.chunk_dst, m.chunk_delta, m.xfinal, m.status,
                     m.x_lo, m.xA_lo, m.attn_lo, m.act_lo, m.q_lo, m.part_o, m.part_ml, m.attn_sched};
     for (void* p : ptrs)
@@ -77,6 +78,7 @@ cb_status cb_model_create(const cb_config* cfg, const cb_weights* w, cb_model** 
     if (c.n_heads % c.n_kv_heads != 0) return fail(CB_ERR_INVALID_ARG, "n_heads must be a multiple of n_kv_heads");
     if (c.head_dim != 64 && c.head_dim != 128) return fail(CB_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
     if (c.d_model % 64 || c.ffn_hidden % 64) return fail(CB_ERR_UNSUPPORTED, "d_model and ffn_hidden must be multiples of 64");
+    if (c.d_model > 8192) return fail(CB_ERR_UNSUPPORTED, "d_model above 8192");
     if (c.n_heads / c.n_kv_heads > 8) return fail(CB_ERR_UNSUPPORTED, "at most 8 query heads per KV head");
     if (c.dtype != CB_F32 && c.dtype != CB_BF16) return fail(CB_ERR_INVALID_ARG, "dtype must be CB_F32 or CB_BF16");
     if (c.precision != CB_PREC_SPLIT && c.precision != CB_PREC_BF16)
@@ -119,7 +121,11 @@ cb_status cb_model_create(const cb_config* cfg, const cb_weights* w, cb_model** 
     m->w_up.assign(w->w_up, w->w_up + c.n_layers);
     m->w_down.assign(w->w_down, w->w_down + c.n_layers);
     m->h = m->hA = nullptr; m->x = m->xA = m->q = m->attn = m->act = nullptr;
-    m->kf = m->vf = m->dev = nullptr; m->rows = m->rows2 = m->sel_local = m->iota = nullptr; m->rope = nullptr;
+    m->kf = m->vf = m->dev = m->dev_part = m->part_h = nullptr;
+    m->rows = m->rows2 = m->sel_local = m->iota = nullptr; m->rope = nullptr;
+    // split-K partial-sum slots of the residual GEMMs: splits x rows must fit in part_rows rows of d
+    m->part_rows = m->bf16 ? 12288 : 0;
+    m->dev_parts = 2 * c.n_kv_heads * c.head_dim / 32;
     m->inv_freq = nullptr;
     m->delta_cs = nullptr; m->chunk_dst = m->chunk_delta = nullptr; m->xfinal = nullptr; m->status = nullptr;
     m->tc = nullptr;
@@ -131,7 +137,9 @@ cb_status cb_model_create(const cb_config* cfg, const cb_weights* w, cb_model** 
     struct { void** p; size_t bytes; } allocs[] = {
         {(void**)&m->h, T * d * 4}, {(void**)&m->hA, T * d * 4}, {&m->x, T * d * as}, {&m->xA, T * d * as},
         {&m->q, T * nq * as}, {&m->attn, T * nq * as}, {&m->act, T * F * as}, {(void**)&m->kf, T * nkv * 4},
-        {(void**)&m->vf, T * nkv * 4}, {(void**)&m->dev, T * 4}, {(void**)&m->rows, T * 4},
+        {(void**)&m->vf, T * nkv * 4}, {(void**)&m->dev, T * 4},
+        {(void**)&m->dev_part, m->bf16 ? T * (size_t)m->dev_parts * 4 : 0},
+        {(void**)&m->part_h, (size_t)m->part_rows * d * 4}, {(void**)&m->rows, T * 4},
         {(void**)&m->rows2, T * 4}, {(void**)&m->sel_local, T * 4},
         {(void**)&m->iota, T * 4}, {(void**)&m->rope, T * half * sizeof(float2)},
         {(void**)&m->inv_freq, half * sizeof(double)}, {(void**)&m->delta_cs, mc * half * sizeof(float2)},
@@ -238,7 +246,7 @@ cb_status check_chunks(const cb_chunk* chunks, int32_t n_chunks, int max_chunks,
 
 const char* const kClassName[K_NCLASS] = {"rerope", "embed", "rmsnorm", "gemm_q", "gemm_kv", "gemm_qkv", "gemm_o",
                                          "gemm_gateup", "gemm_down", "attention", "deviation", "topk",
-                                         "gather_scatter", "logits", "delta_table", "refilter", "pages"};
+                                         "gather", "logits", "delta_table", "refilter", "pages"};
 
 // Enqueues launches on one stream; counts them and, when profiling is on, brackets each with events.
 struct Sched {
@@ -246,6 +254,7 @@ struct Sched {
     cudaStream_t s;
     int launches = 0;
     double gemm_flops = 0;
+    int last_splits = 1;     // K ranges of the last residual GEMM (S > 1: S partial-sum slots pending)
     cudaError_t err = cudaSuccess;
 
     template <typename F>
@@ -289,9 +298,10 @@ struct Sched {
         const double f = 2.0 * M * (double)N * K * (e.kind == EPI_SWIGLU ? 2 : 1);
         const double wbytes = (double)N * K * es * (e.kind == EPI_SWIGLU ? 2 : 1);
         gemm_flops += f;
+        last_splits = 1;
         if (m.tc) {
             int n = 1;
-            k(cls, f, wbytes, [&] { return launch_gemm_tc(m, xb, row0, M, K, w, N, e, s, &n); });
+            k(cls, f, wbytes, [&] { return launch_gemm_tc(m, xb, row0, M, K, w, N, e, s, &n, &last_splits); });
         } else {
             const char* base = (const char*)xbuf(xb) + (size_t)row0 * K * act_size(m);
             const char* lo = m.split ? (const char*)xbuf_lo(xb) + (size_t)row0 * K * act_size(m) : nullptr;
@@ -322,6 +332,8 @@ GemmW wsel(const Model& m, int layer, int which) {
 EpiParams epi_base(const Model& m, int kind, int M) {
     EpiParams e;
     memset(&e, 0, sizeof e);
+    e.part = m.part_h;
+    e.part_rows = m.part_rows;
     e.q_out_lo = m.q_lo;
     e.kind = kind;
     e.M = M;
@@ -368,7 +380,8 @@ namespace {
 cb_status blend_impl(Model& m, const int32_t* tokens, int32_t n_tokens, const void* cached_kv, const ChunkTable& t,
                      int n_chunks, int n_ctx, const std::vector<int>& ks, void* out_kv, float* out_logits,
                      int32_t* out_selected, float* out_dev, cb_stats* stats, cudaStream_t s,
-                     const cb_layer_io* io = nullptr, const cb_paged_kv* pg = nullptr, int page_shift = 0) {
+                     const cb_layer_io* io = nullptr, const cb_paged_kv* pg = nullptr, int page_shift = 0,
+                     const int32_t* given = nullptr) {
     const cb_config& c = m.cfg;
     const size_t es = act_size(m);
     const int L = c.n_layers, d = c.d_model, nq = c.n_heads * c.head_dim, nkv = c.n_kv_heads * c.head_dim;
@@ -450,9 +463,15 @@ cb_status blend_impl(Model& m, const int32_t* tokens, int32_t n_tokens, const vo
         S.launches += n - 1;
         if (m.prof.on) m.prof.launches[K_ATTENTION] += n - 1;
     };
-    auto norm = [&](const float* h, const void* g, void* out, int n) {
+    // partial-sum slots the last residual GEMM left for the next norm (or the logits) to add
+    int pend = 0;
+    auto resid_done = [&] { pend = S.last_splits > 1 ? S.last_splits : 0; };
+    auto norm = [&](float* h, const void* g, void* out, int n) {
         void* lo = !m.split ? nullptr : (out == m.x ? m.x_lo : m.xA_lo);
-        S.k(K_RMSNORM, 0, (double)n * d * (4 + es), [&] { return launch_rmsnorm(m, h, g, out, lo, n, s); });
+        const int parts = pend;
+        pend = 0;
+        const double bytes = (double)n * d * (4.0 + (parts ? 4.0 * parts + 4.0 : 0.0) + es * (lo ? 2 : 1));
+        S.k(K_RMSNORM, 0, bytes, [&] { return launch_rmsnorm(m, h, m.part_h, parts, g, out, lo, n, s); });
     };
 
     // ---- layer 0: every row's hidden state; context K/V reused, query K/V fresh --------------
@@ -475,6 +494,7 @@ cb_status blend_impl(Model& m, const int32_t* tokens, int32_t n_tokens, const vo
         er.h = m.h;
         er.ldh = d;
         S.gemm(K_GEMM_O, XBUF_ATTN, 0, N, nq, wsel(m, 0, WSEL_O), d, er);
+        resid_done();
         norm(m.h, m.mlp_norm[0], m.x, N);
         EpiParams eg = epi_base(m, EPI_SWIGLU, N);
         eg.act = m.act;
@@ -482,26 +502,67 @@ cb_status blend_impl(Model& m, const int32_t* tokens, int32_t n_tokens, const vo
         eg.ld_act = F;
         S.gemm(K_GEMM_GATEUP, XBUF_X, 0, N, d, wsel(m, 0, WSEL_GATEUP), F, eg);
         S.gemm(K_GEMM_DOWN, XBUF_ACT, 0, N, F, wsel(m, 0, WSEL_DOWN), d, er);
+        resid_done();
     }
 
     // ---- check layer 1: fresh K/V of every row, deviation, top-k, then the chosen rows --------
+    // With the tensor cores the comparing GEMM's epilogue keeps the fresh K/V as rows of the storage type and
+    // compares them with the cache itself (per-warp partial sums, added by the top-k kernel in a fixed
+    // order); on the CUDA-core path the GEMM keeps fp32 rows and a separate kernel compares them.
+    const bool fused_dev = m.tc != nullptr;
     float* devp = out_dev ? out_dev : m.dev;
+    // fresh K/V of `rows` GEMM rows of input buffer `xb` (positions `pos`, NULL: 0..), the first `ncmp` of them
+    // compared with the re-RoPE'd cache of layer l: deviations into devd, then the top `kk` of them
+    auto compare = [&](int l, int xb, int rows, int ncmp, const int* pos, float* devd, int kk, int* sel_rows,
+                       int* sel_out) {
+        if (rows > 0) {
+            EpiParams ekv = epi_base(m, EPI_QKV, rows);
+            ekv.qkv_base = nq;
+            ekv.pos = pos;
+            ekv.k_dst = m.kf;
+            ekv.v_dst = m.vf;
+            if (fused_dev) {
+                ekv.kv_fresh = 2;
+                ekv.cmp_k = layer_kv(l);
+                ekv.cmp_v = layer_v(l);
+                ekv.dev_part = m.dev_part;
+                ekv.dev_parts = m.dev_parts;
+                ekv.dev_rows = ncmp;
+            } else {
+                ekv.kv_fresh = 1;
+            }
+            S.gemm(K_GEMM_KV, xb, 0, rows, d, wsel(m, l, WSEL_KV), 2 * nkv, ekv);
+            if (!fused_dev && ncmp > 0)
+                S.k(K_DEVIATION, 0, (double)ncmp * 2 * nkv * (4 + es),
+                    [&] { return launch_deviation(m, m.kf, m.vf, layer_kv(l), N, pos, ncmp, devd, s); });
+        }
+        const double tk_bytes = (double)ncmp * 4 * (fused_dev ? m.dev_parts + 1 : 1);
+        S.k(K_TOPK, 0, tk_bytes, [&] {
+            return launch_topk(m.pdl, fused_dev ? nullptr : devd, m.dev_part, m.dev_parts, devd, ncmp, kk, Q, sel_rows,
+                               sel_out, s);
+        });
+    };
+    const double kvrow_bytes = 2.0 * nkv * ((fused_dev ? es : 4.0) + es);   // one row's fresh K/V read, stored
     {
         norm(m.h, m.attn_norm[1], m.x, N);
-        EpiParams ekv = epi_base(m, EPI_QKV, N);
-        ekv.qkv_base = nq;
-        ekv.kv_fresh = 1;
-        ekv.k_dst = m.kf;
-        ekv.v_dst = m.vf;
-        S.gemm(K_GEMM_KV, XBUF_X, 0, N, d, wsel(m, 1, WSEL_KV), 2 * nkv, ekv);
-        layer_in(1);
-        if (n_ctx > 0)
-            S.k(K_DEVIATION, 0, (double)n_ctx * 2 * nkv * (4 + es),
-                [&] { return launch_deviation(m, m.kf, m.vf, layer_kv(1), N, nullptr, n_ctx, devp, s); });
-        S.k(K_TOPK, 0, (double)n_ctx * 4, [&] { return launch_topk(m, devp, n_ctx, k, Q, m.rows, out_selected, s); });
-        S.k(K_GATHER, 0, (double)M * (8.0 * d + 2.0 * d * es + 2.0 * nkv * (4 + es)),
-            [&] { return launch_gather_scatter(m, m.rows, M, m.h, m.hA, m.x, m.xA, m.x_lo, m.xA_lo, m.kf, m.vf,
-                                               layer_kv(1), N, s); });
+        layer_in(1);                                 // the comparison reads the re-RoPE'd cache of layer 1
+        if (given) {                                 // the caller's set: no comparison at the check layer
+            EpiParams ekv = epi_base(m, EPI_QKV, N);
+            ekv.qkv_base = nq;
+            ekv.k_dst = m.kf;
+            ekv.v_dst = m.vf;
+            ekv.kv_fresh = fused_dev ? 2 : 1;        // fresh K/V rows only (nothing to compare: dev_rows 0)
+            ekv.dev_part = m.dev_part;
+            ekv.dev_parts = m.dev_parts;
+            S.gemm(K_GEMM_KV, XBUF_X, 0, N, d, wsel(m, 1, WSEL_KV), 2 * nkv, ekv);
+            S.k(K_TOPK, 0, (double)k * 4,
+                [&] { return launch_given_rows(m.pdl, given, k, n_ctx, Q, m.rows, out_selected, m.status, s); });
+        } else {
+            compare(1, XBUF_X, N, n_ctx, nullptr, devp, k, m.rows, out_selected);
+        }
+        S.k(K_GATHER, 0, (double)M * (8.0 * d + 2.0 * d * es * (m.split ? 2 : 1) + kvrow_bytes),
+            [&] { return launch_gather(m, m.rows, M, m.h, m.hA, m.x, m.xA, m.x_lo, m.xA_lo, m.kf, m.vf, !fused_dev,
+                                       layer_kv(1), N, s); });
         EpiParams e = epi_base(m, EPI_QKV, M);
         e.qkv_base = 0;
         e.pos = m.rows;
@@ -525,31 +586,22 @@ cb_status blend_impl(Model& m, const int32_t* tokens, int32_t n_tokens, const vo
         void* xcp = xc == XBUF_X ? m.x : m.xA;
         if (l >= 2) layer_in(l);
         if (l >= 2 && kl < k_prev) {
-            // shrinking layer (Figure 9): fresh K/V of the candidates, their deviation against the
-            // re-RoPE'd cache of this layer, the top kl of them, compaction, then Q of the kept rows
+            // shrinking layer (Figure 9): fresh K/V of the candidates (and the query), the candidates compared
+            // with the re-RoPE'd cache of this layer, the top kl of them, compaction with the kept rows' K/V
+            // stored, then Q of the kept rows
             norm(hc, m.attn_norm[l], xcp, Mp);
-            EpiParams ekv = epi_base(m, EPI_QKV, Mp);
-            ekv.qkv_base = nq;
-            ekv.kv_fresh = 1;
-            ekv.pos = rows_c;
-            ekv.k_dst = m.kf;
-            ekv.v_dst = m.vf;
-            S.gemm(K_GEMM_KV, xc, 0, Mp, d, wsel(m, l, WSEL_KV), 2 * nkv, ekv);
             float* devl = (out_dev ? out_dev : m.dev) + dev_at;
-            S.k(K_DEVIATION, 0, (double)k_prev * 2 * nkv * (4 + es),
-                [&] { return launch_deviation(m, m.kf, m.vf, layer_kv(l), N, rows_c, k_prev, devl, s); });
-            S.k(K_TOPK, 0, (double)k_prev * 4,
-                [&] { return launch_topk(m, devl, k_prev, kl, Q, m.sel_local, nullptr, s); });
+            compare(l, xc, Mp, k_prev, rows_c, devl, kl, m.sel_local, nullptr);
             float* hn = hc == m.hA ? m.h : m.hA;
             const int xn = xc == XBUF_XA ? XBUF_X : XBUF_XA;
             void* xnp = xn == XBUF_X ? m.x : m.xA;
             int* rows_n = rows_c == m.rows ? m.rows2 : m.rows;
             int* sel_out = out_selected ? out_selected + sel_at : nullptr;
-            S.k(K_REFILTER, 0, (double)Ml * (8.0 * d + 2.0 * d * es * (m.split ? 2 : 1) + 2.0 * nkv * (4 + es)),
+            S.k(K_REFILTER, 0, (double)Ml * (8.0 * d + 2.0 * d * es * (m.split ? 2 : 1) + kvrow_bytes),
                 [&] { return launch_refilter(m, m.sel_local, rows_c, rows_n, Ml, kl, sel_out, hc, hn, xcp, xnp,
                                              m.split ? (xc == XBUF_X ? m.x_lo : m.xA_lo) : nullptr,
                                              m.split ? (xn == XBUF_X ? m.x_lo : m.xA_lo) : nullptr, m.kf, m.vf,
-                                             layer_kv(l), N, s); });
+                                             !fused_dev, layer_kv(l), N, s); });
             EpiParams e = epi_base(m, EPI_QKV, Ml);
             e.qkv_base = 0;
             e.pos = rows_n;
@@ -578,6 +630,7 @@ cb_status blend_impl(Model& m, const int32_t* tokens, int32_t n_tokens, const vo
         er.h = hc;
         er.ldh = d;
         S.gemm(K_GEMM_O, XBUF_ATTN, 0, Ml, nq, wsel(m, l, WSEL_O), d, er);
+        resid_done();
         norm(hc, m.mlp_norm[l], xcp, Ml);
         EpiParams eg = epi_base(m, EPI_SWIGLU, Ml);
         eg.act = m.act;
@@ -585,13 +638,16 @@ cb_status blend_impl(Model& m, const int32_t* tokens, int32_t n_tokens, const vo
         eg.ld_act = F;
         S.gemm(K_GEMM_GATEUP, xc, 0, Ml, d, wsel(m, l, WSEL_GATEUP), F, eg);
         S.gemm(K_GEMM_DOWN, XBUF_ACT, 0, Ml, F, wsel(m, l, WSEL_DOWN), d, er);
+        resid_done();
         k_prev = kl;
     }
 
     // ---- logits of the last row --------------------------------------------------------------
-    const float* h_last = hc + (size_t)(k_prev + Q - 1) * d;
+    const int M_last = k_prev + Q;
+    const float* h_last = hc + (size_t)(M_last - 1) * d;
+    const float* p_last = m.part_h + (size_t)(M_last - 1) * d;
     S.k(K_LOGITS, 2.0 * d * c.vocab, (double)c.vocab * d * es,
-        [&] { return launch_logits(m, h_last, out_logits, s); });
+        [&] { return launch_logits(m, h_last, p_last, pend, (size_t)M_last * d, out_logits, s); });
 
     if (pg) {   // every row of the blended K/V into its destination page (a copy-on-write page when shared)
         S.k(K_PAGES, 0, 4.0 * L * N * row,
@@ -620,7 +676,7 @@ cb_status blend_impl(Model& m, const int32_t* tokens, int32_t n_tokens, const vo
         double scat = 0;
         for (int l = 1; l < L; ++l) scat += (double)(ks[l] + Q) * 2 * row;
         stats->kv_bytes_moved = (n_chunks ? (inplace ? 2.0 * L * n_ctx * row : 4.0 * L * n_ctx * row) : 0) +
-                                (double)n_ctx * 2 * nkv * (4 + es) + scat;
+                                (double)n_ctx * 2 * nkv * (fused_dev ? es : 4 + es) + scat;
     }
     return CB_OK;
 }
@@ -666,6 +722,24 @@ cb_status cb_blend(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const 
     std::vector<int> ks(m.cfg.n_layers, cb_selected_count(n_ctx, ratio));
     return blend_impl(m, tokens, n_tokens, cached_kv, t, n_chunks, n_ctx, ks, out_kv, out_logits, out_selected,
                       out_dev, stats, (cudaStream_t)stream);
+}
+
+cb_status cb_blend_hkvd(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const void* cached_kv,
+                        const cb_chunk* chunks, int32_t n_chunks, const int32_t* hkvd, int32_t k, void* out_kv,
+                        float* out_logits, cb_stats* stats, void* stream) {
+    g_err[0] = 0;
+    if (!mp) return fail(CB_ERR_INVALID_ARG, "cb_blend_hkvd: null model");
+    Model& m = *mp;
+    ChunkTable t;
+    int n_ctx = 0;
+    cb_status st = check_blend(m, tokens, n_tokens, cached_kv, chunks, n_chunks, out_kv, out_logits, t, n_ctx);
+    if (st != CB_OK) return st;
+    if (k < 0 || k > n_ctx) return fail(CB_ERR_INVALID_ARG, "cb_blend_hkvd: k %d outside [0, n_ctx = %d]", k, n_ctx);
+    if (k > 0 && !hkvd) return fail(CB_ERR_INVALID_ARG, "cb_blend_hkvd: null hkvd with k > 0");
+    std::vector<int> ks(m.cfg.n_layers, k);
+    // with k = 0 the set is empty and never read; any device pointer marks the given-set path
+    return blend_impl(m, tokens, n_tokens, cached_kv, t, n_chunks, n_ctx, ks, out_kv, out_logits, nullptr, nullptr,
+                      stats, (cudaStream_t)stream, nullptr, nullptr, 0, k > 0 ? hkvd : m.rows);
 }
 
 cb_status cb_blend_streamed(cb_model* mp, const int32_t* tokens, int32_t n_tokens, const cb_layer_io* io,
@@ -805,6 +879,15 @@ cb_status cb_blend_gradual(cb_model* mp, const int32_t* tokens, int32_t n_tokens
     ks[0] = ks[1];
     return blend_impl(m, tokens, n_tokens, cached_kv, t, n_chunks, n_ctx, ks, out_kv, out_logits, out_selected,
                       out_dev, stats, (cudaStream_t)stream);
+}
+
+cb_status cb_select_hkvd(const float* dev, int32_t n, int32_t k, int32_t* out_rows, void* stream) {
+    g_err[0] = 0;
+    if (n < 0 || k < 0 || k > n) return fail(CB_ERR_INVALID_ARG, "cb_select_hkvd: need 0 <= k <= n (n %d, k %d)", n, k);
+    if (k == 0) return CB_OK;
+    if (!dev || !out_rows) return fail(CB_ERR_INVALID_ARG, "cb_select_hkvd: null dev or out_rows");
+    const cudaError_t e = launch_topk(false, dev, nullptr, 0, nullptr, n, k, 0, out_rows, nullptr, (cudaStream_t)stream);
+    return e == cudaSuccess ? CB_OK : fail(CB_ERR_CUDA, "cb_select_hkvd: %s", cudaGetErrorString(e));
 }
 
 double cb_load_time(double per_token_kv_bytes, int64_t n_tokens, double throughput_bytes_per_s) {

@@ -92,14 +92,26 @@ struct EpiParams {
     void* q_out;           // [M][nq] activation type
     void* act_lo;          // EPI_SWIGLU, split precision: low bf16 part of act (NULL otherwise)
     void* q_out_lo;        // EPI_QKV, split precision: low bf16 part of q (NULL otherwise)
-    void* k_dst;           // K rows: storage type at row pos(r) (kv_fresh == 0) or fp32 at row r
+    void* k_dst;           // K rows: storage type at row pos(r) (kv_fresh 0), fp32 at row r (1), storage type at row r (2)
     void* v_dst;
-    int kv_fresh;
+    int kv_fresh;          // 0: store K/V into the cache; 1: fp32 rows; 2 (tensor cores): compare, see below
+    // kv_fresh == 2: the fresh K/V go to k_dst / v_dst at row r (storage type), and each epilogue warp also
+    // compares its 32 features of every token row r < dev_rows with the stored cache row pos(r) of cmp_k /
+    // cmp_v and writes the sum of squared differences to dev_part[r][slot], slot = (K: 0, V: nkv / 32) +
+    // first feature / 32 (KV deviation, CacheBlend page "核心思想"); dev_parts = 2 * nkv / 32 per row.
+    const void* cmp_k;
+    const void* cmp_v;
+    float* dev_part;
+    int dev_parts;
+    int dev_rows;
     const float2* rope;    // (cos, sin) [position][head_dim/2]
-    // EPI_RESID: h[r][c] += y  (fp32; atomic when the K range is split)
+    // EPI_RESID: h[r][c] += y (fp32).  With the K range split over S > 1 units, unit s stores its sum to
+    // part + s * M * ldh instead, and the next RMSNorm adds the S slots to h in slot order.
     float* h;
     int ldh;
     int atomic;
+    float* part;           // partial-sum slots (tensor-core path)
+    int part_rows;         // capacity of `part` in rows of ldh floats: S * M must not exceed it
     // EPI_SWIGLU: act[r][f] = silu(gate) * up
     void* act;
     int ld_act;
@@ -155,6 +167,10 @@ struct Model {
     float* kf;            // [max_tokens][nkv] fresh K at the check layer (fp32)
     float* vf;            // [max_tokens][nkv] fresh V at the check layer (fp32)
     float* dev;           // [max_tokens] deviations
+    float* part_h;        // [part_rows][d] split-K partial sums of the residual GEMMs (tensor-core path)
+    int part_rows;
+    float* dev_part;      // [max_tokens][2 * nkv / 32] per-warp deviation partials of the GEMM epilogue (bf16)
+    int dev_parts;        // 2 * nkv / 32
     int* rows;            // [max_tokens] recomputed-row positions (selected ascending, then query)
     int* rows2;           // [max_tokens] the other rows buffer of gradual filtering (sets alternate)
     int* sel_local;       // [max_tokens] kept rows of a shrinking layer, as indices into the previous set
@@ -194,30 +210,43 @@ cudaError_t launch_rerope(const Model& m, const void* src, void* dst, int64_t sr
 cudaError_t launch_page_copy(const Model& m, const void* src, int64_t src_rows, const int* src_pages, void* dst,
                              int64_t dst_rows, const int* dst_pages, int page_shift, int n_rows, cudaStream_t s);
 cudaError_t launch_embed(const Model& m, const int* tokens, int n, float* h, cudaStream_t s);
-cudaError_t launch_rmsnorm(const Model& m, const float* h, const void* g, void* out, void* out_lo, int n,
-                           cudaStream_t s);
+// out = RMSNorm(h) for n rows; when parts > 0, h is first completed as h + part[0] + ... + part[parts-1]
+// (slots of n rows each, added in slot order) and written back
+cudaError_t launch_rmsnorm(const Model& m, float* h, const float* part, int parts, const void* g, void* out,
+                           void* out_lo, int n, cudaStream_t s);
 cudaError_t launch_deviation(const Model& m, const float* kf, const float* vf, const void* kv_layer, int64_t kv_rows,
                              const int* crow, int n_ctx, float* dev, cudaStream_t s);
 cudaError_t launch_refilter(const Model& m, const int* local, const int* rows_old, int* rows_new, int M_new, int k_new,
                             int* out_sel, const float* h_old, float* h_new, const void* x_old, void* x_new,
-                            const void* xlo_old, void* xlo_new, const float* kf, const float* vf, void* kv_layer,
-                            int64_t kv_rows, cudaStream_t s);
-cudaError_t launch_topk(const Model& m, const float* dev, int n_ctx, int k, int n_query, int* rows, int* out_sel,
-                        cudaStream_t s);
-cudaError_t launch_gather_scatter(const Model& m, const int* rows, int M, const float* h, float* hA, const void* x,
-                                  void* xA, const void* x_lo, void* xA_lo, const float* kf, const float* vf,
-                                  void* kv_layer, int64_t kv_rows, cudaStream_t s);
+                            const void* xlo_old, void* xlo_new, const void* kf, const void* vf, bool kv_f32,
+                            void* kv_layer, int64_t kv_rows, cudaStream_t s);
+// top-k of the deviations dev_in[n_ctx], or (dev_in NULL) of the sums of dev_part[n_ctx][parts], which are
+// then written to dev; rows receives the selected rows ascending, then the query rows n_ctx .. n_ctx+n_query-1
+cudaError_t launch_topk(bool pdl, const float* dev_in, const float* dev_part, int parts, float* dev, int n_ctx, int k,
+                        int n_query, int* rows, int* out_sel, cudaStream_t s);
+// rows = sel[0..k) (validated: ascending, in [0, n)) then the query rows n .. n+n_query-1
+cudaError_t launch_given_rows(bool pdl, const int* sel, int k, int n, int n_query, int* rows, int* out_sel,
+                              unsigned* status, cudaStream_t s);
+// hA/xA <- rows of h/x; with kf (fresh K/V rows, fp32 when kv_f32 else the storage type) also the K/V of those
+// rows into the blended cache block kv_layer at their positions
+cudaError_t launch_gather(const Model& m, const int* rows, int M, const float* h, float* hA, const void* x, void* xA,
+                          const void* x_lo, void* xA_lo, const void* kf, const void* vf, bool kv_f32, void* kv_layer,
+                          int64_t kv_rows, cudaStream_t s);
 cudaError_t launch_attention(const Model& m, const void* q, const void* q_lo, const int* qpos, int M,
                              const void* kv_layer, int64_t kv_rows, int n_keys, void* out, void* out_lo, cudaStream_t s);
-cudaError_t launch_logits(const Model& m, const float* h_last, float* logits, cudaStream_t s);
+// logits of h_last (+ the pending partial sums part[0 .. parts-1] of that row, slot stride part_stride floats)
+cudaError_t launch_logits(const Model& m, const float* h_last, const float* part, int parts, size_t part_stride,
+                          float* logits, cudaStream_t s);
 cudaError_t launch_gemm_simt(const Model& m, const void* X, const void* X_lo, int M, int K, const GemmW& w, int N,
                              const EpiParams& e, cudaStream_t s);
 
 // tensor-core path (gemm_tc.cu)
 bool tc_init(Model& m, std::string& err);
 void tc_destroy(Model& m);
+// *splits (optional) receives the number of K ranges of a residual GEMM (1: h holds the final sum; S > 1:
+// S partial-sum slots are pending)
 cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, const GemmW& w, int N,
-                           const EpiParams& e, cudaStream_t s, int* launches);
+                           const EpiParams& e, cudaStream_t s, int* launches, int* splits = nullptr);
 enum { XBUF_X = 0, XBUF_XA = 1, XBUF_ATTN = 2, XBUF_ACT = 3 };
 
 // Raise kernel `k`'s dynamic shared-memory limit to `bytes` on the current device, once per device (CUDA

@@ -57,7 +57,7 @@ struct TcArgs {
 };
 
 struct Unit {
-    int seg, lt, t, kb0, kb1;
+    int seg, lt, t, kb0, kb1, s;   // s: index of the unit's K range (split-K)
 };
 
 __device__ __forceinline__ Unit decode_unit(const TcArgs& a, int u) {
@@ -72,6 +72,7 @@ __device__ __forceinline__ Unit decode_unit(const TcArgs& a, int u) {
         ++r.seg;
     }
     r.lt = mt;
+    r.s = s;
     r.kb0 = (int)((long long)a.kb_total * s / a.splits);
     r.kb1 = (int)((long long)a.kb_total * (s + 1) / a.splits);
     return r;
@@ -151,7 +152,47 @@ __device__ __forceinline__ void qkv_tile(const TcArgs& a, const Unit& w, int row
             r1[j] = rot ? x * cs[j].y + y * cs[j].x : y;
         }
         if (fv) {
-            if (e.kv_fresh && reg > 0) {
+            if (e.kv_fresh == 2 && reg > 0) {
+                // compare with the stored cache: stage [16 tokens][32 features] fp32, feature f of token j at
+                // column f ^ j (reads below are then free of bank conflicts); lane = (token lane & 15, half
+                // lane >> 4) sums its 16 squared differences in feature order, the two halves are added and
+                // the warp's partial for the token is written once
+                float* st = reinterpret_cast<float*>(stg);
+                if (even) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        *reinterpret_cast<float2*>(st + j * 32 + ((lane ^ j) & ~1)) =
+                            (j & 1) ? make_float2(r1[j], r0[j]) : make_float2(r0[j], r1[j]);
+                }
+                __syncwarp();
+                const int t = lane & 15, hs = lane >> 4;
+                const int r = tok0 + base + t;
+                float acc = 0.f;
+                if (t < nt && r < e.dev_rows) {
+                    const bf16* cp = reinterpret_cast<const bf16*>(reg == 1 ? e.cmp_k : e.cmp_v) +
+                                     (size_t)wpos[base + t] * e.nkv + off0 + hs * 16;
+                    const uint4 u0 = *reinterpret_cast<const uint4*>(cp);
+                    const uint4 u1 = *reinterpret_cast<const uint4*>(cp + 8);
+                    const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&u0);
+                    const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&u1);
+                    float c[16];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 a0 = __bfloat1622float2(h0[i]), a1 = __bfloat1622float2(h1[i]);
+                        c[2 * i] = a0.x; c[2 * i + 1] = a0.y; c[8 + 2 * i] = a1.x; c[8 + 2 * i + 1] = a1.y;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float dd = st[t * 32 + ((hs * 16 + i) ^ t)] - c[i];
+                        acc = fmaf(dd, dd, acc);
+                    }
+                }
+                acc += __shfl_xor_sync(0xffffffffu, acc, 16);
+                if (hs == 0 && t < nt && r < e.dev_rows)
+                    e.dev_part[(size_t)r * e.dev_parts + (reg - 1) * (e.nkv >> 5) + (off0 >> 5)] = acc;
+                __syncwarp();
+            }
+            if (e.kv_fresh == 1 && reg > 0) {
                 // fp32 rows: stage [16 tokens][32 features], write 8 x 16 bytes per token
                 float* st = reinterpret_cast<float*>(stg);
                 if (even) {
@@ -187,11 +228,12 @@ __device__ __forceinline__ void qkv_tile(const TcArgs& a, const Unit& w, int row
                 bf16* hi_base = reinterpret_cast<bf16*>(reg == 0 ? e.q_out : (reg == 1 ? e.k_dst : e.v_dst)) + off0;
                 bf16* lo_base = lo ? reinterpret_cast<bf16*>(e.q_out_lo) + off0 : nullptr;
                 const int ld = reg == 0 ? e.nq : e.nkv;
+                const bool by_pos = reg > 0 && e.kv_fresh == 0;      // K/V into the cache at the position
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     const int t = (lane >> 2) + 8 * k, sg = lane & 3;
                     if (t < nt) {
-                        const size_t r = reg == 0 ? (size_t)(tok0 + base + t) : (size_t)wpos[base + t];
+                        const size_t r = by_pos ? (size_t)wpos[base + t] : (size_t)(tok0 + base + t);
                         *reinterpret_cast<uint4*>(hi_base + r * ld + sg * 8) =
                             *reinterpret_cast<const uint4*>(stg + t * 16 + sg * 4);
                         if (lo)
@@ -233,9 +275,12 @@ __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, 
                  : "memory");
 }
 
-// Residual epilogue: h[token][feature] += y.  The warp's 32 features x 16 tokens are transposed
-// through shared memory so each lane adds four consecutive features of a token with one 16-byte
-// vector reduction (the K range may be split across CTAs, hence the atomic adds).
+// Residual epilogue.  The warp's 32 features x 16 tokens are transposed through shared memory so each
+// lane handles four consecutive features of a token with 16-byte accesses.  With one K range the unit
+// adds its sum into the residual stream with a vector reduction (h[token][feature] += y; the only writer
+// of those elements, so the result is fixed).  With the K range split over S units, unit s stores its sum
+// to partial slot s ([M][ldh] each) and the next RMSNorm adds the slots to h in slot order, so the result
+// does not depend on which CTA finished first.
 __device__ __forceinline__ void epi_resid(const TcArgs& a, const Unit& w, int row, int lane, int tok0, const float* v,
                                           float* wst) {
     const EpiParams& e = a.e;
@@ -246,16 +291,29 @@ __device__ __forceinline__ void epi_resid(const TcArgs& a, const Unit& w, int ro
     __syncwarp();
     const int nf = a.seg_rows[w.seg] - feat0;                 // valid features in this warp (may be < 32)
     const int fq = (lane & 7) * 4;                            // 4 features
+    const bool slots = a.splits > 1;
+    float* dst = slots ? e.part + (size_t)w.s * a.M * e.ldh : e.h;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int j = (lane >> 3) + 4 * i;                    // token within the chunk
         const int tok = tok0 + j;
         if (tok < a.M && fq < nf) {
-            float* hp = e.h + (size_t)tok * e.ldh + col0 + fq;
-            if (fq + 3 < nf)
-                red_add_v4(hp, wst[fq * 17 + j], wst[(fq + 1) * 17 + j], wst[(fq + 2) * 17 + j], wst[(fq + 3) * 17 + j]);
-            else
-                for (int t = 0; fq + t < nf; ++t) atomicAdd(hp + t, wst[(fq + t) * 17 + j]);
+            float* hp = dst + (size_t)tok * e.ldh + col0 + fq;
+            const float y0 = wst[fq * 17 + j], y1 = wst[(fq + 1) * 17 + j], y2 = wst[(fq + 2) * 17 + j],
+                        y3 = wst[(fq + 3) * 17 + j];
+            if (fq + 3 < nf) {
+                if (slots)
+                    *reinterpret_cast<float4*>(hp) = make_float4(y0, y1, y2, y3);
+                else
+                    red_add_v4(hp, y0, y1, y2, y3);
+            } else {
+#pragma unroll
+                for (int t = 0; t < 3; ++t) {               // at most three features left in this warp
+                    if (fq + t >= nf) break;
+                    const float yt = t == 0 ? y0 : (t == 1 ? y1 : y2);
+                    if (slots) hp[t] = yt; else atomicAdd(hp + t, yt);
+                }
+            }
         }
     }
     __syncwarp();
@@ -845,7 +903,7 @@ void tc_destroy(Model& m) {
 }
 
 cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, const GemmW& w, int N,
-                           const EpiParams& e, cudaStream_t s, int* launches) {
+                           const EpiParams& e, cudaStream_t s, int* launches, int* splits) {
     (void)N;
     TcMaps& t = *m.tc;
     const int l = w.layer;
@@ -929,9 +987,10 @@ cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, c
     if (e.kind == EPI_RESID) {
         double best = 1e30;
         int smax = 8;
-        if (const char* v = getenv("CB_TUNE_SPLITK")) smax = std::max(1, atoi(v));
+        if (const char* v = getenv("CB_TUNE_SPLITK")) smax = std::min(8, std::max(1, atoi(v)));   // 8 slots at most
         for (int S = 1; S <= smax; ++S) {
             if (a.kb_total / S < 4) break;
+            if (S > 1 && (!e.part || (long long)S * M > e.part_rows)) break;   // the partial slots must fit
             const long long units = (long long)mtiles * a.ttiles * S;
             const long long waves = (units + workers - 1) / workers;
             const double cost = waves * ((double)a.kb_total / S + 2.0);
@@ -939,6 +998,7 @@ cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, c
         }
     }
     a.units = mtiles * a.ttiles * a.splits;
+    if (splits) *splits = a.splits;
     a.prefetch = 0;
     if (!pair)
         if (const char* v = getenv("CB_TUNE_PF")) a.prefetch = std::max(0, atoi(v));

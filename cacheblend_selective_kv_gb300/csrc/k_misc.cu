@@ -189,84 +189,131 @@ cudaError_t launch_embed(const Model& m, const int* tokens, int n, float* h, cud
 }
 
 // ------------------------------------------------------------------------------------------------
-// RMSNorm: out[r] = g * h[r] / sqrt(mean(h[r]^2) + eps), stored in the activation type
+// RMSNorm: out[r] = g * h[r] / sqrt(mean(h[r]^2) + eps), stored in the activation type (in split
+// precision also lo = rn(v - rn(v))).  One CTA per row; a thread keeps its RC chunks of 8 values in
+// registers between the sum of squares and the scaled write, so the row is read once.  When the residual
+// GEMM before it split its K range, h[r] is first completed with that GEMM's partial sums, added in slot
+// order (all slots' loads in flight together) and written back, which makes the residual stream
+// independent of which CTA finished first.
 // ------------------------------------------------------------------------------------------------
-template <typename T>
-__global__ void rmsnorm_kernel(const float* __restrict__ h, const T* __restrict__ g, T* __restrict__ out,
-                               T* __restrict__ out_lo, int d, float eps) {
+constexpr int NORM_THREADS = 256;
+constexpr int NORM_MAX_PARTS = 8;
+
+// P > 0: the number of partial-sum slots, known at compile time for the common counts so that every
+// slot's loads are issued before the first addition (P = NORM_MAX_PARTS: any count up to it, predicated)
+template <typename T, int RC, int P>
+__global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(float* __restrict__ h, const float* __restrict__ part,
+                                                               int parts, const T* __restrict__ g, T* __restrict__ out,
+                                                               T* __restrict__ out_lo, int n, int d, float eps) {
     grid_dep_launch();
     grid_dep_wait();
-    // one CTA per row; the first RC eight-element chunks of each thread stay in registers between the
-    // sum of squares and the scaled write, so a row of up to RC * 8 * blockDim.x elements is read once
-    constexpr int RC = 4;
-    const int r = blockIdx.x, bd = blockDim.x, tid = threadIdx.x;
-    const float* row = h + (size_t)r * d;
-    __shared__ float red[32];
+    __shared__ float red[NORM_THREADS / 32];
+    const int r = blockIdx.x, tid = threadIdx.x;
+    float* row = h + (size_t)r * d;
+    const size_t pstride = (size_t)n * d;
     float f[RC][8];
+#pragma unroll
+    for (int c = 0; c < RC; ++c) {
+        const int e = (tid + c * NORM_THREADS) * 8;
+        if (e < d) Vec8<float>::load(row + e, f[c]);
+    }
+    if (P > 0 && parts > 0) {
+#pragma unroll
+        for (int c = 0; c < RC; ++c) {
+            const int e = (tid + c * NORM_THREADS) * 8;
+            if (e < d) {
+                float t[P > 0 ? P : 1][8];
+#pragma unroll
+                for (int p = 0; p < P; ++p)
+                    if (p < parts) Vec8<float>::load(part + p * pstride + (size_t)r * d + e, t[p]);
+#pragma unroll
+                for (int p = 0; p < P; ++p)
+                    if (p < parts) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) f[c][i] += t[p][i];
+                    }
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < RC; ++c) {
+            const int e = (tid + c * NORM_THREADS) * 8;
+            if (e < d) Vec8<float>::store(row + e, f[c]);
+        }
+    }
     float ss = 0.f;
 #pragma unroll
     for (int c = 0; c < RC; ++c) {
-        const int e = (tid + c * bd) * 8;
+        const int e = (tid + c * NORM_THREADS) * 8;
         if (e < d) {
-            Vec8<float>::load(row + e, f[c]);
 #pragma unroll
             for (int i = 0; i < 8; ++i) ss += f[c][i] * f[c][i];
         }
     }
-    for (int e = (tid + RC * bd) * 8; e < d; e += bd * 8) {
-        float t[8];
-        Vec8<float>::load(row + e, t);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) ss += t[i] * t[i];
-    }
     ss = warp_sum(ss);
     if ((tid & 31) == 0) red[tid >> 5] = ss;
     __syncthreads();
-    if (tid < 32) {
-        float v = tid < (bd >> 5) ? red[tid] : 0.f;
-        v = warp_sum(v);
-        if (tid == 0) red[0] = v;
-    }
-    __syncthreads();
-    const float scale = 1.0f / sqrtf(red[0] / (float)d + eps);
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < NORM_THREADS / 32; ++w) tot += red[w];
+    const float scale = 1.0f / sqrtf(tot / (float)d + eps);
     T* o = out + (size_t)r * d;
     T* ol = out_lo ? out_lo + (size_t)r * d : nullptr;
-    auto emit = [&](int e, float* v) {
-        float gg[8];
-        Vec8<T>::load(g + e, gg);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = v[i] * scale * gg[i];
-        Vec8<T>::store(o + e, v);
-        if (ol) {                // remainder after rounding to T (split precision)
-            float hi[8];
-            round_to<T>(v, hi);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) hi[i] = v[i] - hi[i];
-            Vec8<T>::store(ol + e, hi);
-        }
-    };
 #pragma unroll
     for (int c = 0; c < RC; ++c) {
-        const int e = (tid + c * bd) * 8;
-        if (e < d) emit(e, f[c]);
-    }
-    for (int e = (tid + RC * bd) * 8; e < d; e += bd * 8) {
-        float t[8];
-        Vec8<float>::load(row + e, t);
-        emit(e, t);
+        const int e = (tid + c * NORM_THREADS) * 8;
+        if (e < d) {
+            float gg[8], v[8];
+            Vec8<T>::load(g + e, gg);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = f[c][i] * scale * gg[i];
+            Vec8<T>::store(o + e, v);
+            if (ol) {            // remainder after rounding to T (split precision)
+                float hi[8];
+                round_to<T>(v, hi);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) hi[i] = v[i] - hi[i];
+                Vec8<T>::store(ol + e, hi);
+            }
+        }
     }
 }
 
-cudaError_t launch_rmsnorm(const Model& m, const float* h, const void* g, void* out, void* out_lo, int n,
-                           cudaStream_t s) {
+template <typename T, int RC, int P>
+cudaError_t launch_norm_p(const Model& m, float* h, const float* part, int parts, const void* g, void* out,
+                          void* out_lo, int n, cudaStream_t s) {
+    return launch_ex(m.pdl, rmsnorm_kernel<T, RC, P>, dim3(n), dim3(NORM_THREADS), 0, s, h, part, parts, (const T*)g,
+                     (T*)out, (T*)out_lo, n, m.cfg.d_model, m.cfg.rms_eps);
+}
+
+template <typename T, int RC>
+cudaError_t launch_norm_t(const Model& m, float* h, const float* part, int parts, const void* g, void* out,
+                          void* out_lo, int n, cudaStream_t s) {
+    switch (parts) {
+        case 0: return launch_norm_p<T, RC, 0>(m, h, part, parts, g, out, out_lo, n, s);
+        case 2: return launch_norm_p<T, RC, 2>(m, h, part, parts, g, out, out_lo, n, s);
+        case 3: return launch_norm_p<T, RC, 3>(m, h, part, parts, g, out, out_lo, n, s);
+        case 4: return launch_norm_p<T, RC, 4>(m, h, part, parts, g, out, out_lo, n, s);
+        default: return launch_norm_p<T, RC, NORM_MAX_PARTS>(m, h, part, parts, g, out, out_lo, n, s);
+    }
+}
+
+template <typename T>
+cudaError_t launch_norm_d(const Model& m, float* h, const float* part, int parts, const void* g, void* out,
+                          void* out_lo, int n, cudaStream_t s) {
+    const int d = m.cfg.d_model;
+    if (parts > NORM_MAX_PARTS) return cudaErrorInvalidValue;
+    if (d <= 8 * NORM_THREADS) return launch_norm_t<T, 1>(m, h, part, parts, g, out, out_lo, n, s);
+    if (d <= 16 * NORM_THREADS) return launch_norm_t<T, 2>(m, h, part, parts, g, out, out_lo, n, s);
+    if (d <= 32 * NORM_THREADS) return launch_norm_t<T, 4>(m, h, part, parts, g, out, out_lo, n, s);
+    if (d <= 64 * NORM_THREADS) return launch_norm_t<T, 8>(m, h, part, parts, g, out, out_lo, n, s);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_rmsnorm(const Model& m, float* h, const float* part, int parts, const void* g, void* out,
+                           void* out_lo, int n, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
-    if (m.bf16)
-        rmsnorm_kernel<bf16><<<n, 256, 0, s>>>(h, (const bf16*)g, (bf16*)out, (bf16*)out_lo, m.cfg.d_model,
-                                               m.cfg.rms_eps);
-    else
-        rmsnorm_kernel<float><<<n, 256, 0, s>>>(h, (const float*)g, (float*)out, nullptr, m.cfg.d_model,
-                                                m.cfg.rms_eps);
-    return cudaGetLastError();
+    if (m.bf16) return launch_norm_d<bf16>(m, h, part, parts, g, out, out_lo, n, s);
+    return launch_norm_d<float>(m, h, part, parts, g, out, nullptr, n, s);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -318,65 +365,58 @@ cudaError_t launch_deviation(const Model& m, const float* kf, const float* vf, c
 }
 
 // ------------------------------------------------------------------------------------------------
-// Recomputed rows at the check layer: compact their hidden state and normalised input, and store
-// their fresh K/V into the blended cache before attention (Figure 5: assemble the complete K/V).
+// Rows of the next recomputed set: their hidden state and normalised input are compacted, and their
+// fresh K/V (kept by the comparing GEMM as rows of the storage type, or fp32 rows on the CUDA-core path)
+// are stored into the blended cache at their positions before attention (Figure 5: assemble the complete
+// K/V, then attend).  src[i] is the row of h/x/K/V that becomes compact row i; dst_pos[i] its position.
 // ------------------------------------------------------------------------------------------------
+template <typename T, typename S>
+__device__ __forceinline__ void copy_kv_row(const S* kf, const S* vf, int src, T* kv_layer, int64_t kv_rows, int pos,
+                                            int W) {
+    for (int e = threadIdx.x * 8; e < W; e += blockDim.x * 8) {
+        float f[8];
+        Vec8<S>::load(kf + (size_t)src * W + e, f);
+        Vec8<T>::store(kv_layer + (int64_t)pos * W + e, f);
+        Vec8<S>::load(vf + (size_t)src * W + e, f);
+        Vec8<T>::store(kv_layer + (kv_rows + pos) * (int64_t)W + e, f);
+    }
+}
+
 template <typename T>
-__global__ void gather_scatter_kernel(const int* __restrict__ rows, const float* __restrict__ h, float* __restrict__ hA,
-                                      const T* __restrict__ x, T* __restrict__ xA, const T* __restrict__ x_lo,
-                                      T* __restrict__ xA_lo, const float* __restrict__ kf,
-                                      const float* __restrict__ vf, T* kv_layer, int64_t kv_rows, int d, int W) {
+__device__ __forceinline__ void copy_state_row(const float* h, float* hn, const T* x, T* xn, const T* xl, T* xln,
+                                               int src, int i, int d) {
+    for (int e = threadIdx.x * 4; e < d; e += blockDim.x * 4)
+        *reinterpret_cast<float4*>(hn + (size_t)i * d + e) = *reinterpret_cast<const float4*>(h + (size_t)src * d + e);
+    for (int e = threadIdx.x * 8; e < d; e += blockDim.x * 8) {
+        float f[8];
+        Vec8<T>::load(x + (size_t)src * d + e, f);
+        Vec8<T>::store(xn + (size_t)i * d + e, f);
+        if (xl) {
+            Vec8<T>::load(xl + (size_t)src * d + e, f);
+            Vec8<T>::store(xln + (size_t)i * d + e, f);
+        }
+    }
+}
+
+template <typename T, typename S>
+__global__ void gather_kernel(const int* __restrict__ rows, const float* __restrict__ h, float* __restrict__ hA,
+                              const T* __restrict__ x, T* __restrict__ xA, const T* __restrict__ x_lo,
+                              T* __restrict__ xA_lo, const S* __restrict__ kf, const S* __restrict__ vf, T* kv_layer,
+                              int64_t kv_rows, int d, int W) {
     grid_dep_launch();
     grid_dep_wait();
     const int i = blockIdx.x;
     const int r = rows[i];
-    for (int e = threadIdx.x * 4; e < d; e += blockDim.x * 4)
-        *reinterpret_cast<float4*>(hA + (size_t)i * d + e) = *reinterpret_cast<const float4*>(h + (size_t)r * d + e);
-    for (int e = threadIdx.x * 8; e < d; e += blockDim.x * 8) {
-        float f[8];
-        Vec8<T>::load(x + (size_t)r * d + e, f);
-        Vec8<T>::store(xA + (size_t)i * d + e, f);
-        if (x_lo) {
-            Vec8<T>::load(x_lo + (size_t)r * d + e, f);
-            Vec8<T>::store(xA_lo + (size_t)i * d + e, f);
-        }
-    }
-    for (int e = threadIdx.x * 8; e < W; e += blockDim.x * 8) {
-        float f[8];
-        Vec8<float>::load(kf + (size_t)r * W + e, f);
-        Vec8<T>::store(kv_layer + (int64_t)r * W + e, f);
-        Vec8<float>::load(vf + (size_t)r * W + e, f);
-        Vec8<T>::store(kv_layer + (kv_rows + r) * (int64_t)W + e, f);
-    }
+    copy_state_row<T>(h, hA, x, xA, x_lo, xA_lo, r, i, d);
+    if (kf) copy_kv_row<T, S>(kf, vf, r, kv_layer, kv_rows, r, W);
 }
 
-cudaError_t launch_gather_scatter(const Model& m, const int* rows, int M, const float* h, float* hA, const void* x,
-                                  void* xA, const void* x_lo, void* xA_lo, const float* kf, const float* vf,
-                                  void* kv_layer, int64_t kv_rows, cudaStream_t s) {
-    const int d = m.cfg.d_model, W = m.cfg.n_kv_heads * m.cfg.head_dim;
-    if (m.bf16)
-        gather_scatter_kernel<bf16><<<M, 256, 0, s>>>(rows, h, hA, (const bf16*)x, (bf16*)xA, (const bf16*)x_lo,
-                                                      (bf16*)xA_lo, kf, vf, (bf16*)kv_layer, kv_rows, d, W);
-    else
-        gather_scatter_kernel<float><<<M, 256, 0, s>>>(rows, h, hA, (const float*)x, (float*)xA, nullptr, nullptr, kf,
-                                                       vf, (float*)kv_layer, kv_rows, d, W);
-    return cudaGetLastError();
-}
-
-// ------------------------------------------------------------------------------------------------
-// A shrinking layer of gradual filtering (Figure 9 funnel): the kept rows are local[i] (indices into
-// the previous layer's compact rows; the kept context rows ascending, then the query rows).  Row i of
-// the new compact set takes the hidden state and normalised input of row local[i] (into the other
-// buffer of each pair: compaction in place would race), its position, and its fresh K/V is stored
-// into the blended cache at that position before attention.  out_sel (optional) receives the kept
-// context rows' positions.
-// ------------------------------------------------------------------------------------------------
-template <typename T>
+template <typename T, typename S>
 __global__ void refilter_kernel(const int* __restrict__ local, const int* __restrict__ rows_old, int* __restrict__ rows_new,
-                                int k_new, int* __restrict__ out_sel, const float* __restrict__ h_old, float* __restrict__ h_new,
-                                const T* __restrict__ x_old, T* __restrict__ x_new, const T* __restrict__ xlo_old,
-                                T* __restrict__ xlo_new, const float* __restrict__ kf, const float* __restrict__ vf,
-                                T* kv_layer, int64_t kv_rows, int d, int W) {
+                                int k_new, int* __restrict__ out_sel, const float* __restrict__ h_old,
+                                float* __restrict__ h_new, const T* __restrict__ x_old, T* __restrict__ x_new,
+                                const T* __restrict__ xlo_old, T* __restrict__ xlo_new, const S* __restrict__ kf,
+                                const S* __restrict__ vf, T* kv_layer, int64_t kv_rows, int d, int W) {
     grid_dep_launch();
     grid_dep_wait();
     const int i = blockIdx.x;
@@ -386,40 +426,50 @@ __global__ void refilter_kernel(const int* __restrict__ local, const int* __rest
         rows_new[i] = r;
         if (out_sel && i < k_new) out_sel[i] = r;
     }
-    for (int e = threadIdx.x * 4; e < d; e += blockDim.x * 4)
-        *reinterpret_cast<float4*>(h_new + (size_t)i * d + e) = *reinterpret_cast<const float4*>(h_old + (size_t)src * d + e);
-    for (int e = threadIdx.x * 8; e < d; e += blockDim.x * 8) {
-        float f[8];
-        Vec8<T>::load(x_old + (size_t)src * d + e, f);
-        Vec8<T>::store(x_new + (size_t)i * d + e, f);
-        if (xlo_old) {
-            Vec8<T>::load(xlo_old + (size_t)src * d + e, f);
-            Vec8<T>::store(xlo_new + (size_t)i * d + e, f);
-        }
-    }
-    for (int e = threadIdx.x * 8; e < W; e += blockDim.x * 8) {
-        float f[8];
-        Vec8<float>::load(kf + (size_t)src * W + e, f);
-        Vec8<T>::store(kv_layer + (int64_t)r * W + e, f);
-        Vec8<float>::load(vf + (size_t)src * W + e, f);
-        Vec8<T>::store(kv_layer + (kv_rows + r) * (int64_t)W + e, f);
-    }
+    copy_state_row<T>(h_old, h_new, x_old, x_new, xlo_old, xlo_new, src, i, d);
+    copy_kv_row<T, S>(kf, vf, src, kv_layer, kv_rows, r, W);
+}
+
+cudaError_t launch_gather(const Model& m, const int* rows, int M, const float* h, float* hA, const void* x, void* xA,
+                          const void* x_lo, void* xA_lo, const void* kf, const void* vf, bool kv_f32, void* kv_layer,
+                          int64_t kv_rows, cudaStream_t s) {
+    if (M <= 0) return cudaSuccess;
+    const int d = m.cfg.d_model, W = m.cfg.n_kv_heads * m.cfg.head_dim;
+    if (!m.bf16)
+        gather_kernel<float, float><<<M, 256, 0, s>>>(rows, h, hA, (const float*)x, (float*)xA, nullptr, nullptr,
+                                                      (const float*)kf, (const float*)vf, (float*)kv_layer, kv_rows, d, W);
+    else if (kv_f32)
+        gather_kernel<bf16, float><<<M, 256, 0, s>>>(rows, h, hA, (const bf16*)x, (bf16*)xA, (const bf16*)x_lo,
+                                                     (bf16*)xA_lo, (const float*)kf, (const float*)vf, (bf16*)kv_layer,
+                                                     kv_rows, d, W);
+    else
+        gather_kernel<bf16, bf16><<<M, 256, 0, s>>>(rows, h, hA, (const bf16*)x, (bf16*)xA, (const bf16*)x_lo,
+                                                    (bf16*)xA_lo, (const bf16*)kf, (const bf16*)vf, (bf16*)kv_layer,
+                                                    kv_rows, d, W);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_refilter(const Model& m, const int* local, const int* rows_old, int* rows_new, int M_new, int k_new,
                             int* out_sel, const float* h_old, float* h_new, const void* x_old, void* x_new,
-                            const void* xlo_old, void* xlo_new, const float* kf, const float* vf, void* kv_layer,
-                            int64_t kv_rows, cudaStream_t s) {
+                            const void* xlo_old, void* xlo_new, const void* kf, const void* vf, bool kv_f32,
+                            void* kv_layer, int64_t kv_rows, cudaStream_t s) {
     if (M_new <= 0) return cudaSuccess;
     const int d = m.cfg.d_model, W = m.cfg.n_kv_heads * m.cfg.head_dim;
-    if (m.bf16)
-        refilter_kernel<bf16><<<M_new, 256, 0, s>>>(local, rows_old, rows_new, k_new, out_sel, h_old, h_new,
-                                                    (const bf16*)x_old, (bf16*)x_new, (const bf16*)xlo_old,
-                                                    (bf16*)xlo_new, kf, vf, (bf16*)kv_layer, kv_rows, d, W);
+    if (!m.bf16)
+        refilter_kernel<float, float><<<M_new, 256, 0, s>>>(local, rows_old, rows_new, k_new, out_sel, h_old, h_new,
+                                                            (const float*)x_old, (float*)x_new, nullptr, nullptr,
+                                                            (const float*)kf, (const float*)vf, (float*)kv_layer,
+                                                            kv_rows, d, W);
+    else if (kv_f32)
+        refilter_kernel<bf16, float><<<M_new, 256, 0, s>>>(local, rows_old, rows_new, k_new, out_sel, h_old, h_new,
+                                                           (const bf16*)x_old, (bf16*)x_new, (const bf16*)xlo_old,
+                                                           (bf16*)xlo_new, (const float*)kf, (const float*)vf,
+                                                           (bf16*)kv_layer, kv_rows, d, W);
     else
-        refilter_kernel<float><<<M_new, 256, 0, s>>>(local, rows_old, rows_new, k_new, out_sel, h_old, h_new,
-                                                     (const float*)x_old, (float*)x_new, nullptr, nullptr, kf, vf,
-                                                     (float*)kv_layer, kv_rows, d, W);
+        refilter_kernel<bf16, bf16><<<M_new, 256, 0, s>>>(local, rows_old, rows_new, k_new, out_sel, h_old, h_new,
+                                                          (const bf16*)x_old, (bf16*)x_new, (const bf16*)xlo_old,
+                                                          (bf16*)xlo_new, (const bf16*)kf, (const bf16*)vf,
+                                                          (bf16*)kv_layer, kv_rows, d, W);
     return cudaGetLastError();
 }
 
@@ -428,14 +478,22 @@ cudaError_t launch_refilter(const Model& m, const int* local, const int* rows_ol
 // vocabulary; one warp per vocabulary row, 16-byte loads.  HBM-bound on the LM-head read.
 // ------------------------------------------------------------------------------------------------
 template <typename T>
-__global__ void logits_kernel(const float* __restrict__ hl, const T* __restrict__ g, const T* __restrict__ Wh,
-                              int d, int vocab, float eps, float* __restrict__ out) {
+__global__ void logits_kernel(const float* __restrict__ hl, const float* __restrict__ part, int parts, size_t pstride,
+                              const T* __restrict__ g, const T* __restrict__ Wh, int d, int vocab, float eps,
+                              float* __restrict__ out) {
     grid_dep_launch();
     grid_dep_wait();
     extern __shared__ float xs[];
     __shared__ float red[32];
+    // the last row, completed with the partial sums its residual GEMM left (slot order), kept in shared memory
+    for (int e = threadIdx.x; e < d; e += blockDim.x) {
+        float v = hl[e];
+        for (int p = 0; p < parts; ++p) v += part[p * pstride + e];
+        xs[e] = v;
+    }
+    __syncthreads();
     float ss = 0.f;
-    for (int e = threadIdx.x; e < d; e += blockDim.x) { float v = hl[e]; ss += v * v; }
+    for (int e = threadIdx.x; e < d; e += blockDim.x) { float v = xs[e]; ss += v * v; }
     ss = warp_sum(ss);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
     __syncthreads();
@@ -446,7 +504,7 @@ __global__ void logits_kernel(const float* __restrict__ hl, const T* __restrict_
     }
     __syncthreads();
     const float scale = 1.0f / sqrtf(red[0] / (float)d + eps);
-    for (int e = threadIdx.x; e < d; e += blockDim.x) xs[e] = hl[e] * scale * to_f(g[e]);
+    for (int e = threadIdx.x; e < d; e += blockDim.x) xs[e] = xs[e] * scale * to_f(g[e]);
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const int warps = (gridDim.x * blockDim.x) >> 5;
@@ -464,17 +522,18 @@ __global__ void logits_kernel(const float* __restrict__ hl, const T* __restrict_
     }
 }
 
-cudaError_t launch_logits(const Model& m, const float* h_last, float* logits, cudaStream_t s) {
+cudaError_t launch_logits(const Model& m, const float* h_last, const float* part, int parts, size_t part_stride,
+                          float* logits, cudaStream_t s) {
     const int d = m.cfg.d_model;
     const int grid = m.num_sms * 4;
     if (m.bf16)
-        logits_kernel<bf16><<<grid, 256, d * sizeof(float), s>>>(h_last, (const bf16*)m.final_norm,
-                                                                 (const bf16*)m.lm_head, d, m.cfg.vocab,
-                                                                 m.cfg.rms_eps, logits);
+        logits_kernel<bf16><<<grid, 256, d * sizeof(float), s>>>(h_last, part, parts, part_stride,
+                                                                 (const bf16*)m.final_norm, (const bf16*)m.lm_head, d,
+                                                                 m.cfg.vocab, m.cfg.rms_eps, logits);
     else
-        logits_kernel<float><<<grid, 256, d * sizeof(float), s>>>(h_last, (const float*)m.final_norm,
-                                                                  (const float*)m.lm_head, d, m.cfg.vocab,
-                                                                  m.cfg.rms_eps, logits);
+        logits_kernel<float><<<grid, 256, d * sizeof(float), s>>>(h_last, part, parts, part_stride,
+                                                                  (const float*)m.final_norm, (const float*)m.lm_head,
+                                                                  d, m.cfg.vocab, m.cfg.rms_eps, logits);
     return cudaGetLastError();
 }
 

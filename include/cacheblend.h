@@ -42,7 +42,7 @@ typedef enum {
 typedef enum { CB_F32 = 0, CB_BF16 = 1 } cb_dtype;
 
 /* Llama-style pre-norm decoder shape.  Supported: head_dim in {64, 128},
- * n_heads % n_kv_heads == 0, n_layers >= 2, d_model and ffn_hidden multiples of 64. */
+ * n_heads % n_kv_heads == 0, n_layers >= 2, d_model and ffn_hidden multiples of 64, d_model <= 8192. */
 typedef struct {
     int32_t n_layers;
     int32_t d_model;
@@ -159,6 +159,18 @@ cb_status cb_rerope(cb_model* model, void* kv, int64_t n_rows, const cb_chunk* c
 cb_status cb_blend(cb_model* model, const int32_t* tokens, int32_t n_tokens, const void* cached_kv,
                    const cb_chunk* chunks, int32_t n_chunks, double ratio, void* out_kv, float* out_logits,
                    int32_t* out_selected, float* out_dev, cb_stats* stats, void* stream);
+
+/* One blend whose recomputed set is given by the caller (the page's interface passes the HKVD indices
+ * between layers and switches the comparison off with check_flag; section "读源码时的几个观察点"): the
+ * check layer compares nothing and every later layer recomputes exactly the k given context rows and the
+ * query.  Everything else is cb_blend's.
+ *   hkvd  device int32 [k]: context rows, strictly ascending, in [0, n_ctx).  A row out of range or out of
+ *         order is replaced by a valid one and recorded as CB_STATUS_BAD_ROW (read with cb_model_status).
+ * With the set cb_blend chose for the same inputs the result is bit-identical to cb_blend's.
+ * Errors: those of cb_blend, plus CB_ERR_INVALID_ARG for k outside [0, n_ctx] or a NULL hkvd with k > 0. */
+cb_status cb_blend_hkvd(cb_model* model, const int32_t* tokens, int32_t n_tokens, const void* cached_kv,
+                        const cb_chunk* chunks, int32_t n_chunks, const int32_t* hkvd, int32_t k, void* out_kv,
+                        float* out_logits, cb_stats* stats, void* stream);
 
 /* One blend with gradual filtering (section "核心思想", the layer-by-layer funnel of Figure 9): the set
  * of context rows recomputed shrinks from layer to layer, each set nested in the previous one.
@@ -318,7 +330,7 @@ cb_status cb_model_diag(cb_model* model, uint32_t* words);
  * launch is bracketed by CUDA events recorded on the call's stream (this serialises nothing that was
  * not already serial on that stream, but adds event records between kernels).  Classes: "rerope",
  * "embed", "rmsnorm", "gemm_q", "gemm_kv", "gemm_qkv", "gemm_o", "gemm_gateup", "gemm_down",
- * "attention", "deviation", "topk", "gather_scatter", "logits", "delta_table", "refilter", "pages". */
+ * "attention", "deviation", "topk", "gather", "logits", "delta_table", "refilter", "pages". */
 typedef struct {
     char name[24];
     int32_t launches;        /* launches recorded since the last read */
@@ -349,13 +361,26 @@ int32_t cb_profile_read(cb_model* model, cb_kernel_profile* out, int32_t max_ent
  *   128), rope_theta and dtype (cb_dtype) describe the buffer [n_layers][2][n_rows][n_kv_heads][head_dim].
  *   More than CB_STATIC_MAX_CHUNKS chunks -> CB_ERR_INVALID_ARG, with nothing enqueued.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress, with that
- * device current); make that first call before any stream capture.  No call allocates or frees device
+ * device current) and keeps it for the life of the process; make that first call before any stream
+ * capture, and do not call this entry point on a device after cudaDeviceReset there (the new context
+ * may place the array elsewhere).  n_kv_heads * head_dim above 2^24, or chunks covering more than
+ * 2^31 - 1 rows -> CB_ERR_INVALID_ARG.  No call allocates or frees device
  * memory.  All calls share the one array; each call writes every entry it reads before reading it, so
  * nothing needs clearing, but calls whose GPU work may overlap (other streams, other threads) race on
  * it and must be serialised by the caller.  Errors are reported through cb_last_error(). */
 #define CB_STATIC_MAX_CHUNKS 256
 cb_status cb_rerope_static(void* kv, int64_t n_rows, int32_t n_layers, int32_t n_kv_heads, int32_t head_dim,
                            double rope_theta, int32_t dtype, const cb_chunk* chunks, int32_t n_chunks, void* stream);
+
+/* HKVD selection on its own (section "选 token:HKVD、逐层过滤与 15% 这个经验值": keep the tokens of largest
+ * KV deviation): the k rows of largest dev[0..n-1], ties to the lower row, written ascending to out_rows.
+ * This is the select step cb_blend runs after its check layer, for callers that compute deviations
+ * themselves.  A value that is not positive (including -0 and NaN) ranks as 0.
+ *   dev       device float32 [n]
+ *   out_rows  device int32 [k]
+ * Requires 0 <= k <= n (else CB_ERR_INVALID_ARG); k = 0 enqueues nothing.  Async on `stream`; no allocation;
+ * concurrent calls are independent. */
+cb_status cb_select_hkvd(const float* dev, int32_t n, int32_t k, int32_t* out_rows, void* stream);
 
 /* Loading controller (section "位置恢复、KV 存储与加载流水线", Figure 11).  Host arithmetic only.
  * cb_load_time: T_load = per_token_kv_bytes * n_tokens / throughput (seconds); -1 for a non-positive

@@ -126,6 +126,23 @@ def test_tiny_prefill_matches_oracle(cb):
     model.close()
 
 
+def test_small_bf16_prefill_matches_oracle(cb):
+    """cb_blend with no cached chunks is a plain causal prefill (the chunk precompute, and the caller's
+    fallback): on the small bf16 configuration, the whole request's 2080 tokens through the tensor-core
+    path, every layer's K/V and the last row's logits against the oracle's prefill."""
+    spec, w, req, _, _ = setup_case("small-bf16")
+    shape = spec.shape.as_dict()
+    model = cb.BlendModel(shape, w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks)
+    out = model.blend(torch.from_numpy(req.tokens).cuda(), None, [], 0.0)
+    torch.cuda.synchronize()
+    assert model.status() == 0
+    ref = oracle.blend(shape, w, req.tokens, None, [], 0.0, "bf16", keep_exact=True)
+    kv_err = parity.assert_kv(parity.bf16_to_f64(out["out_kv"]), ref["out_kv_exact"], "bf16", "prefill K/V")
+    lg_err = parity.assert_logits(parity.bf16_to_f64(out["logits"]), ref["logits"], "bf16")
+    print(f"small bf16 prefill of {len(req.tokens)} tokens: K/V max abs {kv_err:.4f}, logits {lg_err:.4f}")
+    model.close()
+
+
 def test_inplace_blend_equals_out_of_place(cb):
     spec, w, req, caches, ratio = setup_case("small-bf16")
     shape = spec.shape.as_dict()
@@ -137,21 +154,62 @@ def test_inplace_blend_equals_out_of_place(cb):
     buf[:, :, :spec.n_ctx] = cached
     b = model.blend(tokens, buf, req.chunks, ratio, out_kv=buf)
     torch.cuda.synchronize()
-    # the residual GEMMs add split-K partial sums with fp32 atomics, so two runs agree up to the
-    # order of those additions, not bit for bit
+    # every reduction of the blend runs in a fixed order, so the two placements give the same bits
     assert torch.equal(a["selected"], b["selected"])
-    assert (a["out_kv"].float() - b["out_kv"].float()).abs().max().item() <= parity.KV_TOL["bf16"]
-    assert (a["logits"] - b["logits"]).abs().max().item() <= parity.LOGIT_TOL["bf16"]
+    assert torch.equal(a["out_kv"], b["out_kv"])
+    assert torch.equal(a["logits"], b["logits"])
     model.close()
 
 
-def rotation_tol(base_k, ref_k):
-    """Bound on |GPU - oracle| for a K rotated in fp32 with fp32 (cos, sin) and rounded once to bf16:
-    one bf16 ulp of the result, plus the fp32 rounding of the products, a few 2^-24 of the rotated
-    pair's magnitude |x0| + |x1| (it dominates where the result cancels to near zero)."""
-    ulp = np.ldexp(1.0, np.frexp(np.abs(ref_k))[1] - 8)
-    pair = np.abs(base_k.reshape(base_k.shape[:-1] + (-1, 2))).sum(-1)
-    return ulp + np.ldexp(np.repeat(pair, 2, axis=-1), -20)
+@pytest.mark.parametrize("name", ["tiny-fp32", "small-bf16"])
+def test_blend_with_given_set_equals_blend(cb, name):
+    """cb_blend_hkvd with the set cb_blend chose gives cb_blend's K/V and logits bit for bit; with another
+    set (the oracle's top-k of a perturbed ratio) it matches the oracle following that set."""
+    spec, w, req, caches, ratio = setup_case(name)
+    shape = spec.shape.as_dict()
+    store = spec.shape.dtype
+    model = cb.BlendModel(shape, w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks)
+    tokens = torch.from_numpy(req.tokens).cuda()
+    cached = cached_tensor(caches, store)
+    a = model.blend(tokens, cached, req.chunks, ratio)
+    b = model.blend_hkvd(tokens, cached, req.chunks, a["selected"].clone())
+    torch.cuda.synchronize()
+    assert torch.equal(a["out_kv"], b["out_kv"]) and torch.equal(a["logits"], b["logits"])
+    # a set that is not the top-k: every other context row
+    sel = np.arange(0, spec.n_ctx, 2, dtype=np.int32)
+    c = model.blend_hkvd(tokens, cached, req.chunks, torch.from_numpy(sel).cuda())
+    torch.cuda.synchronize()
+    assert model.status() == 0
+    ref = oracle.blend(shape, w, req.tokens, caches, req.chunks, len(sel) / spec.n_ctx, store, selected=sel,
+                       keep_exact=True)
+    parity.assert_kv(parity.bf16_to_f64(c["out_kv"]), ref["out_kv_exact"], store)
+    parity.assert_logits(parity.bf16_to_f64(c["logits"]), ref["logits"], store)
+    # a set out of order is recorded, not faulted
+    bad = torch.from_numpy(np.array([5, 3, spec.n_ctx + 7], np.int32)).cuda()
+    model.blend_hkvd(tokens, cached, req.chunks, bad)
+    torch.cuda.synchronize()
+    assert model.status(clear=True) & cb.CB_STATUS_BAD_ROW
+    model.close()
+
+
+@pytest.mark.parametrize("name", ["tiny-fp32", "small-bf16"])
+def test_blend_is_deterministic(cb, name):
+    """Three blends of the same inputs give the same bits: the split-K partial sums of the residual GEMMs
+    are added by the next RMSNorm in slot order, the deviation partials by the top-k kernel in a fixed
+    order, and attention merges its key-range parts in part order, so no result depends on which CTA
+    finished first."""
+    spec, w, req, caches, ratio = setup_case(name)
+    shape = spec.shape.as_dict()
+    model = cb.BlendModel(shape, w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks)
+    tokens = torch.from_numpy(req.tokens).cuda()
+    cached = cached_tensor(caches, spec.shape.dtype)
+    outs = [model.blend(tokens, cached, req.chunks, ratio, want_dev=True) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert model.status() == 0
+    for o in outs[1:]:
+        for key in ("out_kv", "logits", "selected", "dev"):
+            assert torch.equal(o[key], outs[0][key]), key
+    model.close()
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -176,7 +234,7 @@ def test_rerope_in_place(cb, dtype):
     tol = 1e-5 if dtype == "f32" else 0.0
     err = np.abs(got[:, 0, :n_ctx] - ref[:, 0, :n_ctx])
     if dtype == "bf16":
-        assert np.all(err <= rotation_tol(base[:, 0, :n_ctx], ref[:, 0, :n_ctx])), float(err.max())
+        assert np.all(err <= parity.rotation_tol(base[:, 0, :n_ctx], ref[:, 0, :n_ctx])), float(err.max())
     else:
         assert err.max() <= tol, float(err.max())
     model.close()
@@ -204,7 +262,7 @@ def test_rerope_in_place_many_slabs(cb):
     assert np.array_equal(got[:, 1], base[:, 1]), "V changed"
     assert np.array_equal(got[:, :, n_ctx:], base[:, :, n_ctx:]), "rows past the chunks changed"
     err = np.abs(got[:, 0, :n_ctx] - ref[:, 0, :n_ctx])
-    assert np.all(err <= rotation_tol(base[:, 0, :n_ctx], ref[:, 0, :n_ctx])), float(err.max())
+    assert np.all(err <= parity.rotation_tol(base[:, 0, :n_ctx], ref[:, 0, :n_ctx])), float(err.max())
     model.close()
 
 
@@ -220,6 +278,28 @@ def test_diag_words_after_a_clean_blend(cb):
     assert words[0] == 0 and words[1] == 0, words[:8]
     assert model.status() == 0
     model.close()
+
+
+@pytest.mark.parametrize("n", [1, 5, 8, 9, 100, 3072, 8192, 32768, 100003])
+def test_select_hkvd_equals_stable_sort(cb, n):
+    """The cluster radix select (cb_select_hkvd, the select step of every blend) against the oracle's
+    top-k (a stable sort by decreasing deviation): bit for bit, with many exact ties (values drawn from a
+    small set, so ties straddle every CTA's row range and the threshold), zeros, and k from 0 to n."""
+    rng = np.random.default_rng(n)
+    for trial, pool in enumerate((4, 97, None)):
+        if pool is None:
+            dev = rng.exponential(1.0, n).astype(np.float32)
+        else:
+            dev = rng.choice(np.linspace(0.0, 3.0, pool, dtype=np.float32), n)
+        d = torch.from_numpy(dev).cuda()
+        for k in sorted({0, 1, n // 3, n // 2, n - 1, n} - {-1}):
+            if k < 0:
+                continue
+            out = torch.full((max(k, 1),), -1, dtype=torch.int32, device="cuda")
+            cb.cb_select_hkvd(d, n, k, out)
+            torch.cuda.synchronize()
+            ref = oracle.select_hkvd(dev.astype(np.float64), k)
+            assert np.array_equal(out[:k].cpu().numpy(), ref), (n, trial, k)
 
 
 def test_topk_is_exact_on_gpu_deviations(cb):

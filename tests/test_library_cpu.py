@@ -99,6 +99,17 @@ def test_calls_reject_null_model(lib):
     assert lib.cb_model_destroy(None) == cb.CB_OK
 
 
+def test_select_hkvd_validation_enqueues_nothing(lib):
+    """cb_select_hkvd rejects k outside [0, n] and null buffers on the host; k = 0 is a no-op."""
+    for n, k in ((10, 11), (10, -1), (-1, 0)):
+        with pytest.raises(cb.CacheBlendError) as ei:
+            cb.cb_select_hkvd(4096, n, k, 4096, stream=0)
+        assert ei.value.code == cb.CB_ERR_INVALID_ARG
+    with pytest.raises(cb.CacheBlendError):
+        cb.cb_select_hkvd(0, 10, 3, 4096, stream=0)
+    cb.cb_select_hkvd(0, 10, 0, 0, stream=0)
+
+
 def test_loading_controller_matches_oracle(lib):
     """The library's loading-controller arithmetic against the oracle's (host code, no GPU)."""
     from oracle import accounting
