@@ -7,7 +7,9 @@
 //                   to the requester's namespace, then the token-by-token verification
 //   assign_kernel   one CTA: the verified windows in position order; the t-th verified window of a content
 //                   takes that content's t-th occupant in the requester's namespace (each occupant matches
-//                   at most once, at its first place); then leftmost-greedy non-overlap
+//                   at most once, at its first place), ranks counted per block of 1024 windows with a
+//                   running count per content; then leftmost-greedy non-overlap as a successor chain
+//                   (binary search per match, one walk over the kept matches)
 #include <algorithm>
 #include <cstring>
 #include <new>
@@ -29,6 +31,9 @@ struct cb_index {
     int* hits = nullptr;                   // scratch [max_tokens]: verified content per probe, or -1
     int* list = nullptr;                   // scratch [2 * max_tokens]: (probe, content) of verified probes
     int* matches = nullptr;                // scratch [3 * max_tokens]
+    int* seen = nullptr;                   // scratch [n_contents]: verified probes of each content so far
+    int* vidx = nullptr;                   // scratch [max_tokens]: matches that took an occupant
+    int* nxt = nullptr;                    // scratch [max_tokens]: leftmost-greedy successor of each
     int n_indexed = 0;
 };
 
@@ -96,13 +101,17 @@ __device__ __forceinline__ int block_count(bool flag, int* warp_tot, int& total)
 __global__ void __launch_bounds__(kAssignThreads)
     assign_kernel(const int* __restrict__ hits, int n_probe, int stride, int C, const int* __restrict__ occ_begin,
                   const int* __restrict__ occ_id, const int* __restrict__ occ_old, const int* __restrict__ occ_ns,
-                  int ns, int greedy, int* __restrict__ list, int* __restrict__ matches, int32_t* __restrict__ out,
+                  int n_contents, int ns, int greedy, int* __restrict__ list, int* __restrict__ matches,
+                  int* __restrict__ seen, int* __restrict__ vidx, int* __restrict__ nxt, int32_t* __restrict__ out,
                   int max_out, int32_t* __restrict__ out_count) {
     __shared__ int warp_tot[33];
+    __shared__ int blk_c[kAssignThreads];
+    const int tid = threadIdx.x;
+    for (int c = tid; c < n_contents; c += kAssignThreads) seen[c] = 0;
     // verified probes in position order: list[2i] = probe, list[2i+1] = content
     int n = 0;
     for (int t0 = 0; t0 < n_probe; t0 += kAssignThreads) {
-        const int p = t0 + (int)threadIdx.x;
+        const int p = t0 + tid;
         const int c = p < n_probe ? hits[p] : -1;
         int tot;
         const int at = block_count(c >= 0, warp_tot, tot);
@@ -113,32 +122,75 @@ __global__ void __launch_bounds__(kAssignThreads)
         n += tot;
     }
     __syncthreads();
-    // the rank of each verified probe among the earlier ones of its content -> that occupant
-    for (int i = threadIdx.x; i < n; i += kAssignThreads) {
-        const int c = list[2 * i + 1];
-        int rank = 0;
-        for (int j = 0; j < i; ++j) rank += list[2 * j + 1] == c;
-        int pick = -1;
-        for (int o = occ_begin[c]; o < occ_begin[c + 1]; ++o)
-            if (occ_ns[o] == ns && rank-- == 0) { pick = o; break; }
-        matches[3 * i] = pick >= 0 ? occ_id[pick] : -1;
-        matches[3 * i + 1] = pick >= 0 ? occ_old[pick] : 0;
-        matches[3 * i + 2] = list[2 * i] * stride;
+    // the rank of each verified probe among the earlier ones of its content -> that occupant.  Blocks of
+    // probes in position order: within a block the rank counts the earlier probes of the block with the
+    // same content; seen[c] carries the count of content c over the earlier blocks
+    for (int b0 = 0; b0 < n; b0 += kAssignThreads) {
+        const int i = b0 + tid, nb = min(kAssignThreads, n - b0);
+        const int c = i < n ? list[2 * i + 1] : -1;
+        blk_c[tid] = c;
+        __syncthreads();
+        int rank = 0, pick = -1;
+        bool last = true;
+        if (i < n) {
+            for (int j = 0; j < tid; ++j) rank += blk_c[j] == c;
+            for (int j = tid + 1; j < nb && last; ++j) last = blk_c[j] != c;
+            rank += seen[c];
+            int r = rank;
+            for (int o = occ_begin[c]; o < occ_begin[c + 1]; ++o)
+                if (occ_ns[o] == ns && r-- == 0) { pick = o; break; }
+            matches[3 * i] = pick >= 0 ? occ_id[pick] : -1;
+            matches[3 * i + 1] = pick >= 0 ? occ_old[pick] : 0;
+            matches[3 * i + 2] = list[2 * i] * stride;
+        }
+        __syncthreads();                               // every rank of this block read seen[] first
+        if (i < n && last) seen[c] = rank + 1;         // the block's last probe of c carries its count on
+        __syncthreads();
+    }
+    // matches that took an occupant, in position order
+    int m = 0;
+    for (int t0 = 0; t0 < n; t0 += kAssignThreads) {
+        const int i = t0 + tid;
+        const bool ok = i < n && matches[3 * i] >= 0;
+        int tot;
+        const int at = block_count(ok, warp_tot, tot);
+        if (ok) vidx[m + at] = i;
+        m += tot;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int k = 0, end = -1;
-        for (int i = 0; i < n; ++i) {
-            if (matches[3 * i] < 0) continue;
-            const int cur = matches[3 * i + 2];
-            if (greedy && cur < end) continue;
+    if (!greedy) {
+        for (int v = tid; v < m && v < max_out; v += kAssignThreads) {
+            const int i = vidx[v];
+            out[3 * v] = matches[3 * i];
+            out[3 * v + 1] = matches[3 * i + 1];
+            out[3 * v + 2] = matches[3 * i + 2];
+        }
+        if (tid == 0) *out_count = m;
+        return;
+    }
+    // leftmost-greedy: after a kept match at cur, the next kept one is the first that starts at or after
+    // cur + C.  nxt[v] (binary search over the ascending starts) links each match to that successor; the
+    // kept matches are the chain from the first one (at most n_tokens / C links)
+    for (int v = tid; v < m; v += kAssignThreads) {
+        const int want = matches[3 * vidx[v] + 2] + C;
+        int lo = v + 1, hi = m;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (matches[3 * vidx[mid] + 2] < want) lo = mid + 1; else hi = mid;
+        }
+        nxt[v] = lo;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int k = 0;
+        for (int v = 0; v < m; v = nxt[v]) {
+            const int i = vidx[v];
             if (k < max_out) {
                 out[3 * k] = matches[3 * i];
                 out[3 * k + 1] = matches[3 * i + 1];
-                out[3 * k + 2] = cur;
+                out[3 * k + 2] = matches[3 * i + 2];
             }
             ++k;
-            end = cur + C;
         }
         *out_count = k;
     }
@@ -152,7 +204,7 @@ unsigned long long host_fingerprint(const uint32_t* t, int C) {
 
 void free_index(cb_index* x) {
     void* ptrs[] = {x->fps, x->tokens, x->occ_begin, x->occ_id, x->occ_old, x->occ_ns, x->slots, x->hits,
-                    x->list, x->matches};
+                    x->list, x->matches, x->seen, x->vidx, x->nxt};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     delete x;
@@ -232,7 +284,10 @@ cb_status cb_index_create(int32_t chunk_size, const uint32_t* tokens, const int3
         {(void**)&x->slots, slots.size(), slots.data(), slots.size()},
         {(void**)&x->hits, (size_t)max_tokens * 4, nullptr, 0},
         {(void**)&x->list, (size_t)2 * max_tokens * 4, nullptr, 0},
-        {(void**)&x->matches, (size_t)3 * max_tokens * 4, nullptr, 0}};
+        {(void**)&x->matches, (size_t)3 * max_tokens * 4, nullptr, 0},
+        {(void**)&x->seen, ncs * 4, nullptr, 0},
+        {(void**)&x->vidx, (size_t)max_tokens * 4, nullptr, 0},
+        {(void**)&x->nxt, (size_t)max_tokens * 4, nullptr, 0}};
     for (auto& e : a) {
         if (cudaMalloc(e.p, e.bytes) != cudaSuccess ||
             (e.n && cudaMemcpy(*e.p, e.src, e.n, cudaMemcpyHostToDevice) != cudaSuccess)) {
@@ -284,8 +339,8 @@ cb_status cb_index_match(cb_index* x, const int32_t* tokens, int32_t n_tokens, i
                                                             x->tokens, x->occ_begin, x->occ_ns, x->slots,
                                                             (1ull << x->filter_bits) - 1, ns, x->hits);
     assign_kernel<<<1, kAssignThreads, 0, s>>>(x->hits, n_probe, probe_stride, C, x->occ_begin, x->occ_id, x->occ_old,
-                                               x->occ_ns, ns, leftmost_greedy ? 1 : 0, x->list, x->matches, out,
-                                               max_out, out_count);
+                                               x->occ_ns, x->n_contents, ns, leftmost_greedy ? 1 : 0, x->list,
+                                               x->matches, x->seen, x->vidx, x->nxt, out, max_out, out_count);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_last_error(cudaGetErrorString(e));

@@ -100,3 +100,27 @@ def test_matcher_edges(cb):
     assert empty.match(t, 1) == []
     index.close()
     empty.close()
+
+
+@pytest.mark.parametrize("stride,greedy", [(1, True), (1, False), (3, True)])
+def test_matcher_low_entropy_request(cb, stride, greedy):
+    """A low-entropy request: a run of one repeated token, where every window verifies against the indexed
+    chunk of that token (thousands of verified windows of one content).  Its occupants (three in the
+    requester's namespace, one in another) are taken in position order and leftmost-greedy keeps windows
+    a chunk apart; two more contents of mixed tokens are planted after the run."""
+    n_tokens = 12288
+    run = np.full((1, C), 77, np.uint32)
+    mixed = np.stack([workload.tokens(3, 500 + i, C, VOCAB) for i in range(2)]).astype(np.uint32)
+    all_t = np.concatenate([run, run, run, run, mixed])        # the run's content under four occupants
+    all_o = np.array([1, 2, 3, 4, 5, 6], np.int32)
+    all_s = np.array([0, 512, 1024, 0, 256, 768], np.int32)
+    all_n = np.array([1, 1, 1, 2, 1, 1], np.int32)
+    req = np.full(n_tokens, 77, np.int32)
+    req[9000:9000 + C] = mixed[0]
+    req[9400:9400 + C] = mixed[1]
+    index = cb.FragmentIndex(C, all_t, all_o, all_s, all_n, max_tokens=n_tokens)
+    got = index.match(torch.from_numpy(req).cuda(), 1, stride, greedy)
+    want = oracle_matches(all_t, all_o, all_s, all_n, req, 1, stride, greedy)
+    assert len(want) >= 2
+    assert got == [tuple(int(v) for v in w) for w in want]
+    index.close()
