@@ -158,6 +158,11 @@ def oracle_sample(spec: workload.WorkloadSpec, seed: int, ratio: float, sample_l
     return dt, scale, desc
 
 
+def oracle_k(spec: workload.WorkloadSpec, ratio: float) -> int:
+    import oracle
+    return oracle.selected_count(spec.n_ctx, ratio)
+
+
 def cpu_cores():
     n = os.cpu_count() or 1
     for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
@@ -211,15 +216,23 @@ def run_reference(args, spec, ws, rank):
     times, scale, desc = [], 1.0, ""
     for _ in range(args.steps):
         dt, scale, desc = oracle_sample(spec, seed, ratio)
-        times.append(dt * scale)
+        times.append(dt)
+    # One step is one timed sample (the blend's first layers); ms_per_step is its measured time.  The
+    # sample does 1/scale of a whole blend's FLOPs, so it blends n_ctx/scale context tokens' worth of work.
     t = float(np.sum(times))
-    value = spec.n_ctx * args.steps / t
+    value = spec.n_ctx / scale * args.steps / t
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
-            "latency_ms": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": spec.name, "n_ctx": spec.n_ctx, "n_query": spec.n_query, "ratio": ratio,
-                       "seed": seed, "parallelism": "cpu"},
+            "latency_ms": 1e3 * t * scale / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded random-init weights, uniform random "
+                                                          "tokens, generator chunk caches)",
+            "config": {"workload": spec.name, "n_layers": spec.shape.n_layers, "d_model": spec.shape.d_model,
+                       "n_ctx": spec.n_ctx, "n_query": spec.n_query, "n_chunks": spec.n_chunks,
+                       "chunk_len": spec.chunk_len, "ratio": ratio, "k": oracle_k(spec, ratio),
+                       "recomputed_rows": oracle_k(spec, ratio) + spec.n_query, "seed": seed, "parallelism": "cpu",
+                       "step": f"one timed oracle sample ({desc}); ms_per_step is the sample's measured time, "
+                               f"latency_ms the whole blend's (sample time x {scale:.2f})",
+                       "blend_fraction_per_step": 1.0 / scale},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -240,6 +253,8 @@ def main():
                     help="keep the chunk caches and the blended K/V in a paged pool of P-row pages (shuffled block table)")
     ap.add_argument("--matcher", action="store_true",
                     help="time the GPU fragment matcher instead (32K-token request, 4096 indexed 256-token chunks)")
+    ap.add_argument("--low-entropy", action="store_true",
+                    help="with --matcher: a request of one repeated token, so every window verifies")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-profile", action="store_true")
@@ -524,8 +539,13 @@ def run_matcher(args, cb, ws, rank, local):
     chunks = np.stack([workload.tokens(seed, 1000 + i, C, V) for i in range(n_idx)]).astype(np.uint32)
     req = workload.tokens(seed, 1, n_tok, V)
     rng = np.random.default_rng(seed)
-    for slot, i in enumerate(rng.permutation(n_idx)[: n_tok // C]):
-        req[slot * C:(slot + 1) * C] = chunks[i]
+    if args.low_entropy:
+        # one repeated token: every one of the 32513 windows verifies against chunk 0 (made of that token)
+        chunks[0] = 77
+        req[:] = 77
+    else:
+        for slot, i in enumerate(rng.permutation(n_idx)[: n_tok // C]):
+            req[slot * C:(slot + 1) * C] = chunks[i]
     index = cb.FragmentIndex(C, chunks, np.arange(n_idx), np.zeros(n_idx, np.int32), np.ones(n_idx, np.int32), n_tok)
     dev = torch.device("cuda", local)
     t = torch.from_numpy(req).to(dev)
@@ -550,8 +570,8 @@ def run_matcher(args, cb, ws, rank, local):
     line = {"metric": "fragment match: request tokens/s (GPU matcher)", "value": n_tok / (ms / 1e3),
             "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "dtype": "u64", "data": "synthetic (seeded tokens)",
-            "config": {"workload": f"{n_tok}-token request, {n_idx} indexed {C}-token chunks, stride 1, "
-                                   "leftmost-greedy", "matches": n_match,
+            "config": {"workload": f"{n_tok}-token request{' of one repeated token' if args.low_entropy else ''}, "
+                                   f"{n_idx} indexed {C}-token chunks, stride 1, leftmost-greedy", "matches": n_match,
                        "window_hash_macs": windows * C}}
     if rank == 0:
         print(json.dumps(line), flush=True)
