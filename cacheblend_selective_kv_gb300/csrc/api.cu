@@ -38,7 +38,8 @@ cb_status fail(cb_status code, const char* fmt, ...) {
 size_t act_size(const Model& m) { return m.bf16 ? 2 : 4; }
 
 void free_ws(Model& m) {
-    void* ptrs[] = {m.h, m.hA, m.x, m.xA, m.q, m.attn, m.act, m.kf, m.vf, m.dev, m.dev_part, m.part_h, m.rows, m.rows2,
+    void* ptrs[] = {m.h, m.hA, m.x, m.xA, m.q, m.attn, m.act, m.kf, m.vf, m.dev, m.dev_part, m.part_h, m.tail_part,
+                    m.tail_flag, m.rows, m.rows2,
                     m.sel_local, m.iota,
                     m.rope, m.inv_freq, m.delta_cs, m.chunk_dst, m.chunk_delta, m.xfinal, m.status,
                     m.x_lo, m.xA_lo, m.attn_lo, m.act_lo, m.q_lo, m.part_o, m.part_ml, m.attn_sched};
@@ -121,7 +122,9 @@ cb_status cb_model_create(const cb_config* cfg, const cb_weights* w, cb_model** 
     m->w_up.assign(w->w_up, w->w_up + c.n_layers);
     m->w_down.assign(w->w_down, w->w_down + c.n_layers);
     m->h = m->hA = nullptr; m->x = m->xA = m->q = m->attn = m->act = nullptr;
-    m->kf = m->vf = m->dev = m->dev_part = m->part_h = nullptr;
+    m->kf = m->vf = m->dev = m->dev_part = m->part_h = m->tail_part = nullptr;
+    m->tail_flag = nullptr;
+    m->tail_units = m->bf16 ? (m->num_sms + 1) / 2 : 0;    // at most one unit per CTA pair
     m->rows = m->rows2 = m->sel_local = m->iota = nullptr; m->rope = nullptr;
     // split-K partial-sum slots of the residual GEMMs: splits x rows must fit in part_rows rows of d
     m->part_rows = m->bf16 ? 12288 : 0;
@@ -139,7 +142,9 @@ cb_status cb_model_create(const cb_config* cfg, const cb_weights* w, cb_model** 
         {&m->q, T * nq * as}, {&m->attn, T * nq * as}, {&m->act, T * F * as}, {(void**)&m->kf, T * nkv * 4},
         {(void**)&m->vf, T * nkv * 4}, {(void**)&m->dev, T * 4},
         {(void**)&m->dev_part, m->bf16 ? T * (size_t)m->dev_parts * 4 : 0},
-        {(void**)&m->part_h, (size_t)m->part_rows * d * 4}, {(void**)&m->rows, T * 4},
+        {(void**)&m->part_h, (size_t)m->part_rows * d * 4},
+        {(void**)&m->tail_part, (size_t)m->tail_units * 2 * 128 * 256 * 4},
+        {(void**)&m->tail_flag, (size_t)m->tail_units * 2 * 4}, {(void**)&m->rows, T * 4},
         {(void**)&m->rows2, T * 4}, {(void**)&m->sel_local, T * 4},
         {(void**)&m->iota, T * 4}, {(void**)&m->rope, T * half * sizeof(float2)},
         {(void**)&m->inv_freq, half * sizeof(double)}, {(void**)&m->delta_cs, mc * half * sizeof(float2)},

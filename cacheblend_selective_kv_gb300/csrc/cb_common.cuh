@@ -167,6 +167,9 @@ struct Model {
     float* kf;            // [max_tokens][nkv] fresh K at the check layer (fp32)
     float* vf;            // [max_tokens][nkv] fresh V at the check layer (fp32)
     float* dev;           // [max_tokens] deviations
+    float* tail_part;     // SwiGLU last-wave split: [tail_units][2][128][256] first-half accumulators
+    unsigned* tail_flag;  // [tail_units][2] (zero between launches)
+    int tail_units;
     float* part_h;        // [part_rows][d] split-K partial sums of the residual GEMMs (tensor-core path)
     int part_rows;
     float* dev_part;      // [max_tokens][2 * nkv / 32] per-warp deviation partials of the GEMM epilogue (bf16)

@@ -17,6 +17,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <cstdlib>
 #include <map>
 
@@ -29,7 +30,7 @@ struct TcMaps {
     std::vector<CUtensorMap> wq, wk, wv, wo, wg, wu, wd;   // per layer, box {64, 128}
     std::vector<CUtensorMap> wg64, wu64;                    // per layer, box {64, 64} (paired SwiGLU)
     bool pair = true;                                       // CTA-pair kernel usable
-    int pair_clusters[2][3] = {};                           // co-resident clusters per (SPLIT, EPI), 0 = unknown
+    int pair_clusters[2][4] = {};                           // co-resident clusters per (SPLIT, EPI), 0 = unknown
     const void* xptr[4];                                    // activation buffers (hi) and their row widths
     const void* xptr_lo[4];                                 // low parts (split precision) or NULL
     int xcols[4];
@@ -41,6 +42,9 @@ struct TcMaps {
 namespace {
 
 constexpr int BM = 128, BK = 64, TMEM_COLS = 512, NUM_THREADS = 192;
+// kernel instance of a QKV-epilogue GEMM in comparing mode (EpiParams::kv_fresh == 2), kept apart so the plain
+// QKV instance carries none of its code
+constexpr int EPI_KVCMP = 3;
 constexpr int A_BYTES = BM * BK * 2;        // 16 KB per weight tile
 constexpr int MAX_STAGES = 8;
 constexpr int EPI_POS_INTS = 32 * 17;           // per epilogue warp: token positions (QKV) / transposes
@@ -54,14 +58,39 @@ struct TcArgs {
     uint32_t idesc;
     EpiParams e;
     unsigned* status;
+    // SwiGLU last-wave split: the last `tail` whole units (those of a partial last wave) run as two K halves
+    // each, work items full_units + j (first half) and full_units + tail + j (second half)
+    int full_units, tail;
+    float* tail_part;        // [tail][2 CTAs][128 rows][BN] first-half accumulators
+    unsigned* tail_flag;     // [tail][2 CTAs]: 1 once the first half's accumulators are stored; reset to 0 after use
 };
 
 struct Unit {
-    int seg, lt, t, kb0, kb1, s;   // s: index of the unit's K range (split-K)
+    int seg, lt, t, kb0, kb1, s;   // s: index of the unit's K range (split-K, or the half of a tail unit)
+    int tail, j;                    // a K half of tail unit j
 };
 
+__device__ __forceinline__ Unit decode_whole(const TcArgs& a, int u);
+
 __device__ __forceinline__ Unit decode_unit(const TcArgs& a, int u) {
+    if (u >= a.full_units) {
+        const int p = u - a.full_units, h = p >= a.tail ? 1 : 0, j = p - h * a.tail;
+        Unit r = decode_whole(a, a.full_units + j);
+        const int mid = a.kb_total / 2;
+        r.kb0 = h ? mid : 0;
+        r.kb1 = h ? a.kb_total : mid;
+        r.s = h;
+        r.tail = 1;
+        r.j = j;
+        return r;
+    }
+    return decode_whole(a, u);
+}
+
+__device__ __forceinline__ Unit decode_whole(const TcArgs& a, int u) {
     Unit r;
+    r.tail = 0;
+    r.j = 0;
     r.t = u % a.ttiles;
     const int rest = u / a.ttiles;
     const int s = rest % a.splits;
@@ -92,13 +121,14 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, unsign
 // ---- epilogues: one thread = one feature (TMEM lane), 16 consecutive token rows -------------------
 
 // QKV epilogue of one tile: RoPE of q/k pairs (partner feature = lane ^ 1), q as bf16 (hi and, in split
-// precision, lo), k/v either into the blended cache at each token's position or as fp32 rows.  A warp's 32
+// precision, lo), k/v into the blended cache at each token's position -- or, comparing (CMP), as bf16 rows at
+// the GEMM row, each warp also writing the squared difference of its features from the cached row.  A warp's 32
 // features are consecutive and lie in one region (regions and segments are multiples of 64 wide), so each
 // 16-token chunk is transposed through the warp's shared-memory staging area and written as 16-byte
 // vectors along the features of each token row.  Positions come from a per-warp shared-memory copy; the
 // (cos, sin) loads run DEEP ? two : one chunk of 16 tokens ahead (the shallow form saves 32 registers
 // for kernels with twice the epilogue warps, whose extra warps hide the latency instead).
-template <bool DEEP>
+template <bool DEEP, bool CMP>
 __device__ __forceinline__ void qkv_tile(const TcArgs& a, const Unit& w, int row, int lane, int tok0, int ntok,
                                          uint32_t tbase, const int* wpos, uint32_t* stg) {
     const EpiParams& e = a.e;
@@ -152,7 +182,7 @@ __device__ __forceinline__ void qkv_tile(const TcArgs& a, const Unit& w, int row
             r1[j] = rot ? x * cs[j].y + y * cs[j].x : y;
         }
         if (fv) {
-            if (e.kv_fresh == 2 && reg > 0) {
+            if (CMP && reg > 0) {
                 // compare with the stored cache: stage [16 tokens][32 features] fp32, feature f of token j at
                 // column f ^ j (reads below are then free of bank conflicts); lane = (token lane & 15, half
                 // lane >> 4) sums its 16 squared differences in feature order, the two halves are added and
@@ -192,25 +222,7 @@ __device__ __forceinline__ void qkv_tile(const TcArgs& a, const Unit& w, int row
                     e.dev_part[(size_t)r * e.dev_parts + (reg - 1) * (e.nkv >> 5) + (off0 >> 5)] = acc;
                 __syncwarp();
             }
-            if (e.kv_fresh == 1 && reg > 0) {
-                // fp32 rows: stage [16 tokens][32 features], write 8 x 16 bytes per token
-                float* st = reinterpret_cast<float*>(stg);
-                if (even) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        *reinterpret_cast<float2*>(st + j * 32 + lane) = make_float2(r0[j], r1[j]);
-                }
-                __syncwarp();
-                float* dst = reinterpret_cast<float*>(reg == 1 ? e.k_dst : e.v_dst) + off0;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int t = (lane >> 3) + 4 * k, sg = lane & 7;
-                    if (t < nt)
-                        *reinterpret_cast<float4*>(dst + (size_t)(tok0 + base + t) * e.nkv + sg * 4) =
-                            *reinterpret_cast<const float4*>(st + t * 32 + sg * 4);
-                }
-                __syncwarp();
-            } else {
+            {
                 // bf16 rows: stage [16 tokens][16 pairs] (hi, then lo for split q), write 4 x 16 bytes per token
                 const bool lo = reg == 0 && e.q_out_lo != nullptr;
                 if (even) {
@@ -228,7 +240,7 @@ __device__ __forceinline__ void qkv_tile(const TcArgs& a, const Unit& w, int row
                 bf16* hi_base = reinterpret_cast<bf16*>(reg == 0 ? e.q_out : (reg == 1 ? e.k_dst : e.v_dst)) + off0;
                 bf16* lo_base = lo ? reinterpret_cast<bf16*>(e.q_out_lo) + off0 : nullptr;
                 const int ld = reg == 0 ? e.nq : e.nkv;
-                const bool by_pos = reg > 0 && e.kv_fresh == 0;      // K/V into the cache at the position
+                const bool by_pos = reg > 0 && !CMP;                 // K/V into the cache at the position
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     const int t = (lane >> 2) + 8 * k, sg = lane & 3;
@@ -344,6 +356,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                    const __grid_constant__ CUtensorMap mw0, const __grid_constant__ CUtensorMap mw1,
                    const __grid_constant__ CUtensorMap mw2, const TcArgs a) {
     constexpr bool SWIGLU = EPI == EPI_SWIGLU;
+    constexpr bool IS_QKV = EPI == EPI_QKV || EPI == EPI_KVCMP;
     constexpr int A_STAGE = SWIGLU ? 2 * A_BYTES : A_BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -500,16 +513,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int tok0 = w.t * a.BN;
             const int ntok = min(a.BN, a.M - tok0);
             int* wpos = spos + (warp - 2) * EPI_POS_INTS;
-            if (EPI == EPI_QKV) qkv_prefetch(a, w, row, lane, tok0, ntok, wpos);
+            if (IS_QKV) qkv_prefetch(a, w, row, lane, tok0, ntok, wpos);
             if (!ptx::mbar_wait(ptx::smem_u32(tfull + acc), acc_phase, abort, a.status)) break;
             ptx::tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256;
-            if (EPI == EPI_QKV) {
-                qkv_tile<true>(a, w, row, lane, tok0, ntok, tbase, wpos,
+            if (IS_QKV) {
+                qkv_tile<true, EPI == EPI_KVCMP>(a, w, row, lane, tok0, ntok, tbase, wpos,
                                reinterpret_cast<uint32_t*>(spos + 4 * EPI_POS_INTS) + (warp - 2) * EPI_STG_WORDS);
                 __syncwarp();
             }
-            for (int c = 0; EPI != EPI_QKV && c * 16 < ntok; ++c) {
+            for (int c = 0; !IS_QKV && c * 16 < ntok; ++c) {
                 float v[16];
                 ptx::tmem_ld16(tbase + c * 16, v);
                 if (EPI == EPI_RESID) {
@@ -594,6 +607,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
                      const __grid_constant__ CUtensorMap mw0, const __grid_constant__ CUtensorMap mw1,
                      const __grid_constant__ CUtensorMap mw2, const TcArgs a) {
     constexpr bool SWIGLU = EPI == EPI_SWIGLU;
+    constexpr bool IS_QKV = EPI == EPI_QKV || EPI == EPI_KVCMP;
     constexpr int EW = pair_epi_warps(EPI);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -740,13 +754,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
                 tb = hs ? ntok : mid;
             }
             int* wpos = spos + ew * EPI_POS_INTS;
-            if (EPI == EPI_QKV && tb > ta) qkv_prefetch(a, w, row, lane, tok0 + ta, tb - ta, wpos);
+            if (IS_QKV && tb > ta) qkv_prefetch(a, w, row, lane, tok0 + ta, tb - ta, wpos);
             if (!ptx::mbar_wait(ptx::smem_u32(tfull + acc), acc_phase, abort, a.status)) break;
             ptx::tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256;
-            if (EPI == EPI_QKV) {
+            if (IS_QKV) {
                 if (tb > ta)
-                    qkv_tile<EW == 4>(a, w, row, lane, tok0 + ta, tb - ta, tbase + ta, wpos,
+                    qkv_tile<EW == 4, EPI == EPI_KVCMP>(a, w, row, lane, tok0 + ta, tb - ta, tbase + ta, wpos,
                                       reinterpret_cast<uint32_t*>(spos + EW * EPI_POS_INTS) + ew * EPI_STG_WORDS);
                 __syncwarp();
             } else if (EPI == EPI_RESID) {
@@ -758,11 +772,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
             } else {
                 const int feat = w.lt * 128 + (int)rank * 64 + (q & 1) * 32 + lane;
                 const bool fv = feat < a.seg_rows[0];
-                for (int c = 0; c * 16 < ntok; ++c, ++gc) {
-                    float v[16];
-                    __syncwarp();
-                    ptx::tmem_ld16(tbase + c * 16, v);
-                    epi_swiglu_pair(a, feat, fv, q, lane, tok0 + c * 16, min(16, ntok - c * 16), gc & 1, v, sepi);
+                // a K half of a tail unit: the first half stores its accumulator rows ([lane][token] per CTA) and
+                // raises the unit's flag; the second half waits for the flag (bounded), adds the stored rows to
+                // its own in a fixed order, and only then forms silu(g) * u
+                float* tp = w.tail ? a.tail_part + (((size_t)w.j * 2 + rank) * 128 + q * 32 + lane) * a.BN : nullptr;
+                unsigned* tf = w.tail ? a.tail_flag + w.j * 2 + rank : nullptr;
+                if (w.tail && w.s == 0) {
+                    for (int c = 0; c * 16 < ntok; ++c) {
+                        float v[16];
+                        ptx::tmem_ld16(tbase + c * 16, v);
+#pragma unroll
+                        for (int i = 0; i < 16; i += 4)
+                            *reinterpret_cast<float4*>(tp + c * 16 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                    }
+                    ptx::named_bar_sync(3, 128);                      // every epilogue warp's rows are stored
+                    if (ew == 0 && lane == 0) {
+                        __threadfence();
+                        asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(tf), "r"(1u) : "memory");
+                    }
+                } else {
+                    if (w.tail) {
+                        if (ew == 0 && lane == 0) {
+                            const uint64_t t0 = ptx::global_ns();
+                            unsigned f = 0;
+                            for (;;) {
+                                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(f) : "l"(tf) : "memory");
+                                if (f) break;
+                                if (ptx::global_ns() - t0 > ptx::kWaitLimitNs) {
+                                    atomicOr(a.status, ST_WAIT_TIMEOUT);
+                                    break;
+                                }
+                            }
+                            *tf = 0u;                                    // ready for the next launch
+                        }
+                        ptx::named_bar_sync(3, 128);
+                    }
+                    for (int c = 0; c * 16 < ntok; ++c, ++gc) {
+                        float v[16];
+                        __syncwarp();
+                        ptx::tmem_ld16(tbase + c * 16, v);
+                        if (w.tail) {
+#pragma unroll
+                            for (int i = 0; i < 16; i += 4) {
+                                const float4 f = *reinterpret_cast<const float4*>(tp + c * 16 + i);
+                                v[i] += f.x; v[i + 1] += f.y; v[i + 2] += f.z; v[i + 3] += f.w;
+                            }
+                        }
+                        epi_swiglu_pair(a, feat, fv, q, lane, tok0 + c * 16, min(16, ntok - c * 16), gc & 1, v, sepi);
+                    }
                 }
             }
             ptx::tc_fence_before();
@@ -908,6 +965,8 @@ cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, c
     TcMaps& t = *m.tc;
     const int l = w.layer;
     const bool swiglu = e.kind == EPI_SWIGLU;
+    const int kind = (e.kind == EPI_QKV && e.kv_fresh == 2) ? EPI_KVCMP : e.kind;   // kernel instance
+    if (e.kind == EPI_QKV && e.kv_fresh == 1) return cudaErrorInvalidValue;          // fp32 rows: CUDA-core path only
     const bool split = m.split;
     const bool pair = t.pair;
     TcArgs a;
@@ -967,10 +1026,13 @@ cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, c
     // co-resident workers: SMs, or clusters of two
     int workers = m.num_sms;
     if (pair) {
-        int& cap = t.pair_clusters[split ? 1 : 0][e.kind];
+        int& cap = t.pair_clusters[split ? 1 : 0][kind];
         if (cap == 0) {
-            switch (e.kind) {
+            switch (kind) {
                 case EPI_QKV: cap = split ? pair_capacity<EPI_QKV, true>(smem) : pair_capacity<EPI_QKV, false>(smem); break;
+                case EPI_KVCMP:
+                    cap = split ? pair_capacity<EPI_KVCMP, true>(smem) : pair_capacity<EPI_KVCMP, false>(smem);
+                    break;
                 case EPI_RESID:
                     cap = split ? pair_capacity<EPI_RESID, true>(smem) : pair_capacity<EPI_RESID, false>(smem);
                     break;
@@ -999,11 +1061,31 @@ cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, c
     }
     a.units = mtiles * a.ttiles * a.splits;
     if (splits) *splits = a.splits;
+    // SwiGLU on CTA pairs: a partial last wave of T whole units runs as 2T K halves when they fit in one wave
+    // (the idle clusters take the second halves); the tail pieces keep weight-tile order, so the token tiles of
+    // a weight tile still stream the same weight k-blocks together
+    a.full_units = a.units;
+    a.tail = 0;
+    if (swiglu && pair && m.tail_part && a.kb_total >= 8) {
+        const char* tv = getenv("CB_SWIGLU_TAIL");
+        const int T = a.units % workers;
+        if (!(tv && tv[0] == '0') && T > 0 && 2 * T <= workers && T <= m.tail_units && a.BN <= 256) {
+            a.tail = T;
+            a.full_units = a.units - T;
+            a.units = a.full_units + 2 * T;
+            a.tail_part = m.tail_part;
+            a.tail_flag = m.tail_flag;
+        }
+    }
     a.prefetch = 0;
     if (!pair)
         if (const char* v = getenv("CB_TUNE_PF")) a.prefetch = std::max(0, atoi(v));
     a.idesc = ptx::idesc_bf16(pair ? 256 : BM, a.BN);
     const int grid = pair ? 2 * std::min(a.units, workers) : std::min(a.units, workers);
+    if (getenv("CB_DEBUG_LAUNCH"))
+        fprintf(stderr, "cb gemm: epi %d rows %d K %d N %d | BN %d token tiles %d weight tiles %d splits %d units %d "
+                        "(tail %d) workers %d grid %d stages %d\n", e.kind, M, K, N, a.BN, a.ttiles, mtiles, a.splits,
+                a.units, a.tail, workers, grid, a.stages);
     if (launches) *launches = 1;
     auto tile_map = [&](std::map<int, CUtensorMap>& cache, const void* ptr, CUtensorMap** out) -> bool {
         auto it = cache.find(b_rows);
@@ -1024,14 +1106,16 @@ cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, c
 #define CB_GEMM_DISPATCH(LAUNCH)                                                                     \
     do {                                                                                             \
         if (split) {                                                                                 \
-            switch (e.kind) {                                                                        \
+            switch (kind) {                                                                          \
                 case EPI_QKV: return LAUNCH<EPI_QKV, true>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s, m.pdl);     \
+                case EPI_KVCMP: return LAUNCH<EPI_KVCMP, true>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s, m.pdl); \
                 case EPI_RESID: return LAUNCH<EPI_RESID, true>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s, m.pdl); \
                 default: return LAUNCH<EPI_SWIGLU, true>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s, m.pdl);       \
             }                                                                                        \
         }                                                                                            \
-        switch (e.kind) {                                                                            \
+        switch (kind) {                                                                              \
             case EPI_QKV: return LAUNCH<EPI_QKV, false>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s, m.pdl);        \
+            case EPI_KVCMP: return LAUNCH<EPI_KVCMP, false>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s, m.pdl);    \
             case EPI_RESID: return LAUNCH<EPI_RESID, false>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s, m.pdl);    \
             default: return LAUNCH<EPI_SWIGLU, false>(mx, mxl, wm[0], wm[1], wm[2], a, grid, smem, s, m.pdl);          \
         }                                                                                            \

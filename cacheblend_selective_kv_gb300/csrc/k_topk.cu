@@ -50,9 +50,11 @@ __device__ __forceinline__ int block_excl_count(bool flag, int* warp_tot, int& t
     return warp_tot[warp] + in_warp;
 }
 
+// a load from another CTA's shared memory (distributed shared memory); callers order it after a cluster
+// barrier, itself a compiler barrier
 __device__ __forceinline__ unsigned ld_cluster_u32(uint32_t caddr) {
     unsigned v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(caddr) : "memory");
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(caddr));
     return v;
 }
 
@@ -70,6 +72,7 @@ __global__ void __cluster_dims__(TK_CTAS, 1, 1) __launch_bounds__(TK_THREADS) to
     grid_dep_launch();
     grid_dep_wait();
     __shared__ unsigned hist[2][256];
+    __shared__ unsigned tot[256];                      // cluster-wide count of each digit
     __shared__ int warp_tot[33];
     __shared__ unsigned cnt[2];                        // this CTA's rows above / equal to the threshold
     __shared__ unsigned s_digit;
@@ -82,21 +85,28 @@ __global__ void __cluster_dims__(TK_CTAS, 1, 1) __launch_bounds__(TK_THREADS) to
     if (rank == 0)   // the query rows always follow the k selected rows
         for (int i = tid; i < a.n_query; i += TK_THREADS) a.rows[a.k + i] = a.n + i;
 
-    // 1. deviations of this CTA's rows: one thread per row adds the row's partials in slot order (the
-    //    same order on every run), four at a time
+    // 1. deviations of this CTA's rows: a warp adds a row's partials (lane i takes slots i, i + 32, ...)
+    //    and reduces them by a fixed butterfly, so the order is the same on every run; eight rows per warp
+    //    at a time keep their loads in flight together
     const float* dev = a.dev_in;
     if (!dev) {
-        for (int r = lo + tid; r < hi; r += TK_THREADS) {
-            const float* p = a.dev_part + (size_t)r * a.parts;
-            float v = 0.f;
-            int i = 0;
-            if ((a.parts & 3) == 0)
-                for (; i < a.parts; i += 4) {
-                    const float4 q = *reinterpret_cast<const float4*>(p + i);
-                    v += q.x; v += q.y; v += q.z; v += q.w;
+        constexpr int RW = 8;
+        constexpr int NW = TK_THREADS / 32;
+        for (int r0 = lo + warp * RW; r0 < hi; r0 += NW * RW) {
+            float v[RW];
+#pragma unroll
+            for (int j = 0; j < RW; ++j) {
+                v[j] = 0.f;
+                if (r0 + j < hi) {
+                    const float* p = a.dev_part + (size_t)(r0 + j) * a.parts;
+                    for (int i = lane; i < a.parts; i += 32) v[j] += p[i];
                 }
-            for (; i < a.parts; ++i) v += p[i];
-            a.dev[r] = v;
+            }
+#pragma unroll
+            for (int j = 0; j < RW; ++j) {
+                const float t = warp_sum(v[j]);
+                if (lane == 0 && r0 + j < hi) a.dev[r0 + j] = t;
+            }
         }
         __syncthreads();                               // this CTA's own writes, read back below
         dev = a.dev;
@@ -110,21 +120,35 @@ __global__ void __cluster_dims__(TK_CTAS, 1, 1) __launch_bounds__(TK_THREADS) to
         unsigned* h = hist[pass & 1];
         for (int b = tid; b < 256; b += TK_THREADS) h[b] = 0;
         __syncthreads();
-        for (int j = lo + tid; j < hi; j += TK_THREADS) {
-            const unsigned key = dev_key(dev[j]);
-            if ((key & mask) == prefix) atomicAdd(&h[(key >> shift) & 255u], 1u);
+        // warp-aggregated counting: the lanes of a warp that fall into the same digit add once (the leading
+        // digits of nearby deviations coincide, so plain per-lane atomics would serialise on a few bins)
+        for (int j0 = lo + (tid & ~31); j0 < hi; j0 += TK_THREADS) {
+            const int j = j0 + lane;
+            const unsigned key = j < hi ? dev_key(dev[j]) : 0u;
+            const bool in = j < hi && (key & mask) == prefix;
+            const unsigned bin = in ? (key >> shift) & 255u : 256u + lane;   // lanes out of the pass stay alone
+            const unsigned same = __match_any_sync(0xffffffffu, bin);
+            if (in && lane == __ffs(same) - 1) atomicAdd(&h[bin], (unsigned)__popc(same));
         }
         ptx::cluster_sync();                           // every CTA's histogram of this pass is complete
+        if (tid < 256) {                               // digit tid over the cluster, added in rank order
+            uint32_t src[TK_CTAS];
+            unsigned v[TK_CTAS];
+#pragma unroll
+            for (int q = 0; q < TK_CTAS; ++q) src[q] = ptx::map_to_rank(ptx::smem_u32(h + tid), (uint32_t)q);
+#pragma unroll
+            for (int q = 0; q < TK_CTAS; ++q) v[q] = ld_cluster_u32(src[q]);
+            unsigned c = 0;
+#pragma unroll
+            for (int q = 0; q < TK_CTAS; ++q) c += v[q];
+            tot[tid] = c;
+        }
+        __syncthreads();
         if (warp == 0) {
-            // lane l owns digits 8l .. 8l+7; the cluster-wide count of each, added in rank order
+            // lane l owns digits 8l .. 8l+7
             unsigned c[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) c[i] = 0;
-            for (int q = 0; q < TK_CTAS; ++q) {
-                const uint32_t base = ptx::map_to_rank(ptx::smem_u32(h), (uint32_t)q);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) c[i] += ld_cluster_u32(base + 4u * (8 * lane + i));
-            }
+            for (int i = 0; i < 8; ++i) c[i] = tot[8 * lane + i];
             unsigned own = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) own += c[i];
