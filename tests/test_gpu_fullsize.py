@@ -47,17 +47,22 @@ def _bf16_tensor(a):
     return torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda().to(torch.bfloat16)
 
 
-def _compare_full(spec, w, tokens, caches, chunks, ratio, res, label, cascade=None):
+def _compare_full(spec, w, tokens, caches, chunks, ratio, res, label, cascade=None, follow=None):
     """The GPU result `res` against a whole oracle blend run now: selection, every row's K/V at every layer,
     every context row's deviation, logits.  Prints the per-layer errors and the oracle's time.  `cascade`
-    names the stored oracle spread whose per-layer bounds replace 2e-2 where that spread exceeds it."""
+    names the stored oracle spread whose per-layer bounds replace 2e-2 where that spread exceeds it.  Where
+    the two selections differ (rows tied within the band), `follow(selected)` re-runs the GPU blend with the
+    oracle's set (cb_blend_hkvd) and returns its (K/V, logits); without it the oracle re-runs with the GPU's."""
     cfg = spec.shape.as_dict()
     t0 = time.time()
     ref = oracle.blend(cfg, w, tokens, caches, chunks, ratio, "bf16", keep_exact=True)
     secs = time.time() - t0
     diff = parity.assert_selection(res["selected"], ref["selected"], ref["dev"], ref["k"])
     dev_rel = parity.dev_error(res["dev"], ref["dev"], ref["k"])
-    if diff:
+    if diff and follow is not None:
+        res = dict(res)
+        res["kv"], res["logits"] = follow(ref["selected"])
+    elif diff:
         ref = oracle.blend(cfg, w, tokens, caches, chunks, ratio, "bf16", selected=res["selected"], keep_exact=True)
     g_kv = res["kv"]
     rows = ref["rows"]
@@ -65,7 +70,8 @@ def _compare_full(spec, w, tokens, caches, chunks, ratio, res, label, cascade=No
     for l in (0, 1, 2, L // 2, L - 1):
         mx, n_over, n_ex = parity.kv_error(g_kv[l][:, rows], ref["out_kv_exact"][l][:, rows], "bf16")
         print(f"{label} layer {l} recomputed rows: max abs {mx:.4f}, {n_over} beyond 2e-2 (exempt, |x| >= 8: {n_ex})")
-    print(f"{label}: oracle {secs:.0f} s; selection differs in {len(diff)} rows (all in the band); "
+    print(f"{label}: oracle {secs:.0f} s; selection differs in {len(diff)} rows (all in the band"
+          f"{'; K/V and logits taken with the oracle set' if diff and follow is not None else ''}); "
           f"deviation rel err max {dev_rel.max():.2e}; logits max abs {np.abs(res['logits'] - ref['logits']).max():.4f}")
     assert dev_rel.max() < 2e-3, float(dev_rel.max())
     if cascade is None:
@@ -82,6 +88,17 @@ def _compare_full(spec, w, tokens, caches, chunks, ratio, res, label, cascade=No
         print(f"{label}: {over} elements beyond 2e-2 (the oracle's own spread under a rounding-sized "
               f"perturbation reaches {max(kv_max) / 1.5:.4f})")
     return ref
+
+
+def _follower(model, tokens, cached, chunks):
+    """A `follow` for _compare_full: the GPU blend with a given recomputed set (cb_blend_hkvd)."""
+    def follow(selected):
+        out = model.blend_hkvd(torch.from_numpy(np.asarray(tokens, np.int32)).cuda(), cached, chunks,
+                               torch.from_numpy(np.asarray(selected, np.int32)).cuda())
+        torch.cuda.synchronize()
+        assert model.status() == 0
+        return parity.bf16_to_f64(out["out_kv"]), parity.bf16_to_f64(out["logits"])
+    return follow
 
 
 def _gpu_blend(cb, model, tokens, cached, chunks, ratio):
@@ -103,11 +120,15 @@ def test_fullsize_against_whole_oracle_blend(cb, name, seed, ratio):
     req = workload.make_request(spec, seed, ratio)
     caches = workload.synthetic_cache(spec.shape, seed, spec.n_ctx, workload.kv_std(spec.shape))
     model = cb.BlendModel(spec.shape.as_dict(), w, max_tokens=spec.n_tokens, max_chunks=spec.n_chunks)
-    res = _gpu_blend(cb, model, req.tokens, _bf16_tensor(caches), req.chunks, ratio)
+    cached = _bf16_tensor(caches)
+    res = _gpu_blend(cb, model, req.tokens, cached, req.chunks, ratio)
     res["kv"] = parity.bf16_to_f64(res.pop("kv_dev"))
-    model.close()
-    _compare_full(spec, w, req.tokens, caches, req.chunks, ratio, res, f"{name} seed {seed} r={ratio}",
-                  cascade="blend-8k-r0.30" if (name, ratio) == ("llama8b-8k", 0.30) else None)
+    try:
+        _compare_full(spec, w, req.tokens, caches, req.chunks, ratio, res, f"{name} seed {seed} r={ratio}",
+                      cascade="blend-8k-r0.30" if (name, ratio) == ("llama8b-8k", 0.30) else None,
+                      follow=_follower(model, req.tokens, cached, req.chunks))
+    finally:
+        model.close()
 
 
 STORED = [("llama8b-32k", 6, 0.15)]
@@ -276,10 +297,14 @@ def test_llama8b_genuine_chunk_caches(cb):
     caches = np.concatenate([p["out_kv"] for p in order], axis=2).astype(np.float32)   # bf16 values
     chunks = [(0, 512 * i, 512) for i in range(6)]
     tokens = np.concatenate(toks + [req.query]).astype(np.int32)
-    res = _gpu_blend(cb, model, tokens, _bf16_tensor(caches), chunks, ratio)
+    cached = _bf16_tensor(caches)
+    res = _gpu_blend(cb, model, tokens, cached, chunks, ratio)
     res["kv"] = parity.bf16_to_f64(res.pop("kv_dev"))
-    model.close()
-    ref = _compare_full(spec, w, tokens, caches, chunks, ratio, res, "8B genuine caches")
+    try:
+        ref = _compare_full(spec, w, tokens, caches, chunks, ratio, res, "8B genuine caches",
+                            follow=_follower(model, tokens, cached, chunks))
+    finally:
+        model.close()
     thr = parity.threshold(ref["dev"], ref["k"])
     print(f"first chunk: oracle deviation max {ref['dev'][:512].max():.3e}, GPU {res['dev'][:512].max():.3e}; "
           f"threshold {thr:.3e}; other chunks' median {np.median(ref['dev'][512:]):.3e}")
