@@ -8,7 +8,8 @@
 // position).
 //   warp 0      TMA producer of the Q tile (4-D box) and the K blocks (3-stage ring)
 //   warp 10     TMA producer of the V blocks (2-stage ring)
-//   warp 1      MMA issuer: S = Q K^T into a TMEM buffer; O_h += P_h V_h with P read from TMEM
+//   warp 1      S issuer: S = Q K^T into a TMEM buffer
+//   warp 11     PV issuer: O_h += P_h V_h with P read from TMEM
 //   warps 2..9  softmax, two warps per TMEM lane quarter: the warps of half h own keys 64h..64h+63
 //               of every block, keep their own running max and sum, and overwrite their S columns
 //               with P_h (bf16; in split precision a hi and a lo part), which the PV MMA reads as its
@@ -17,7 +18,12 @@
 // At the end of a unit the half-1 warps combine both halves: O = (O_0 2^(m_0-M) + O_1 2^(m_1-M)) / l.
 // S/P is double buffered in TMEM; a buffer is reused for S once the PV MMAs that read its P are done.
 // K blocks are released as soon as their S MMAs complete and V blocks once their PV MMAs do, so the
-// K loads run up to three blocks ahead.  V is consumed as an MN-major operand from its [key][dim]
+// K loads run up to three blocks ahead.
+// At N = 128 one tcgen05.mma executes in about as many cycles as one thread needs to issue it, so the
+// S and PV MMAs come from two threads (each one's waits and commits overlap the other's issue) and both
+// keep their per-block bookkeeping small: one wait for P (both halves' warps arrive on one barrier), no
+// barrier of their own for V stages or for O (the V producer and the softmax warps wait on the S/P
+// buffer's free barrier, which completes at the same point), and descriptors formed once per block.  V is consumed as an MN-major operand from its [key][dim]
 // layout.  The persistent CTAs claim units at run time (longest query tiles first) from a counter in
 // global memory; long key ranges are cut into parts merged by attn_combine_kernel.
 #include <cudaTypedefs.h>
@@ -34,11 +40,12 @@ namespace {
 constexpr int BKV = 128;                 // keys per block
 constexpr int HK = 64;                   // keys per softmax half
 constexpr int ROWS = 128;                // TMEM lanes per unit
-constexpr int NUM_THREADS = 352;         // K producer, MMA, 8 softmax warps, V producer
+constexpr int NUM_THREADS = 384;         // K producer, S issuer, 8 softmax warps, V producer, PV issuer
+constexpr int V_WARP = 10, PV_WARP = 11;
 constexpr int K_STAGES = 3, V_STAGES = 2;
 constexpr float RESCALE_LOG2 = 8.0f;     // lazy-rescale threshold (P <= 2^8)
 constexpr int SCHED_SLOTS = 4;           // work items published ahead to the consumer roles
-constexpr int SCHED_READERS = 10;        // V producer, MMA issuer, 8 softmax warps
+constexpr int SCHED_READERS = 11;        // V producer, the two MMA issuers, 8 softmax warps
 
 struct AttnArgs {
     int M;              // recomputed query rows
@@ -190,15 +197,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t* k_full = bars + 2;
     uint64_t* k_empty = k_full + K_STAGES;
     uint64_t* v_full = k_empty + K_STAGES;
-    uint64_t* v_empty = v_full + V_STAGES;
-    uint64_t* s_full = v_empty + V_STAGES;            // [buffer]: S written
+    uint64_t* s_full = v_full + V_STAGES;             // [buffer]: S written
     uint64_t* s_free = s_full + 2;                    // [buffer]: the PV MMAs reading its P are done
-    uint64_t* p_full = s_free + 2;                    // [buffer][half]
-    uint64_t* o_full = p_full + 4;                    // [half][block parity]
-    uint64_t* o_free = o_full + 4;
+    uint64_t* p_full = s_free + 2;                    // [buffer]: P written by the 8 softmax warps
+    uint64_t* o_free = p_full + 2;
     uint64_t* cmb_bar = o_free + 1;
-    uint64_t* drain = cmb_bar + 1;
-    uint64_t* sched_full = drain + 1;                 // [slot]: a work item (or -1: none left) published
+    uint64_t* drain = cmb_bar + 1;                    // [issuer]: its last MMAs are done
+    uint64_t* sched_full = drain + 2;                 // [slot]: a work item (or -1: none left) published
     uint64_t* sched_empty = sched_full + SCHED_SLOTS; // [slot]: every consumer role has read it
     int* sched_u = reinterpret_cast<int*>(sched_empty + SCHED_SLOTS);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sched_u + SCHED_SLOTS);
@@ -214,17 +219,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int i = 0; i < V_STAGES; ++i) {
             ptx::mbar_init(ptx::smem_u32(v_full + i), 1);
-            ptx::mbar_init(ptx::smem_u32(v_empty + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(ptx::smem_u32(s_full + i), 1);
             ptx::mbar_init(ptx::smem_u32(s_free + i), 1);
         }
-        for (int i = 0; i < 4; ++i) ptx::mbar_init(ptx::smem_u32(o_full + i), 1);
-        for (int i = 0; i < 4; ++i) ptx::mbar_init(ptx::smem_u32(p_full + i), 4);
+        for (int i = 0; i < 2; ++i) ptx::mbar_init(ptx::smem_u32(p_full + i), 8);
         ptx::mbar_init(ptx::smem_u32(o_free), 4);
         ptx::mbar_init(ptx::smem_u32(cmb_bar), 4);
         ptx::mbar_init(ptx::smem_u32(drain), 1);
+        ptx::mbar_init(ptx::smem_u32(drain + 1), 1);
         for (int i = 0; i < SCHED_SLOTS; ++i) {
             ptx::mbar_init(ptx::smem_u32(sched_full + i), 1);
             ptx::mbar_init(ptx::smem_u32(sched_empty + i), SCHED_READERS);
@@ -250,7 +254,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // first), by the Q/K producer, which skips empty items and publishes each claim through a ring of
     // SCHED_SLOTS shared-memory slots; every other role reads the same sequence from the ring.  Returns
     // the item, -1 when none is left, -2 when a wait gave up.  Called by a whole softmax warp or by the
-    // single thread of the V producer and the MMA issuer.
+    // single thread of the V producer and of each MMA issuer.
     uint32_t sched_cnt = 0;
     auto next_unit = [&](bool warp_wide) -> int {
         const uint32_t slot = sched_cnt % SCHED_SLOTS, par = (sched_cnt / SCHED_SLOTS) & 1u;
@@ -323,7 +327,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int i = 0; i < K_STAGES; ++i)
                 if (issued & (1u << i)) drain_wait(ptx::smem_u32(k_full + i), (issued_par >> i) & 1u, a.status);
         }
-    } else if (warp == NUM_THREADS / 32 - 1) {
+    } else if (warp == V_WARP) {
         // ---------------------------------------------------------------- TMA producer: V
         if (lane == 0) {
             uint32_t v_cnt = 0, issued = 0, issued_par = 0;
@@ -337,7 +341,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int b = b0; b < b1; ++b) {
                     const int st = v_cnt % V_STAGES;
                     const uint32_t par = (v_cnt / V_STAGES) & 1u;
-                    if (!await(ptx::smem_u32(v_empty + st), par ^ 1u, abort, a.status, 7, v_cnt, u)) { ok = false; break; }
+                    // V block v_cnt uses stage v_cnt % 2, as its S uses buffer v_cnt % 2: the stage is free
+                    // once that buffer's PV MMAs (two blocks back) are done
+                    if (!await(ptx::smem_u32(s_free + st), par ^ 1u, abort, a.status, 7, v_cnt, u)) { ok = false; break; }
                     const uint32_t fb = ptx::smem_u32(v_full + st);
                     ptx::mbar_arrive_expect_tx(fb, KB_BYTES);
                     for (int h = 0; h < HALVES; ++h)
@@ -351,38 +357,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int i = 0; i < V_STAGES; ++i)
                 if (issued & (1u << i)) drain_wait(ptx::smem_u32(v_full + i), (issued_par >> i) & 1u, a.status);
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
+    } else if (warp == PV_WARP) {
+        // ---------------------------------------------------------------- PV issuer
         if (lane == 0) {
-            uint32_t q_cnt = 0, k_cnt = 0, v_cnt = 0, s_cnt = 0, unit_cnt = 0;
+            uint32_t v_cnt = 0, sc = 0, unit_cnt = 0;
             bool ok = true;
-            // O_h += P_h V_h for the block whose S had counter `sc` (P in that S buffer)
-            auto pv = [&](uint32_t sc, bool first) -> bool {
-                const int buf = sc & 1;
-                const uint32_t par = (sc >> 1) & 1u;
-                const uint32_t st = v_cnt % V_STAGES, vpar = (v_cnt / V_STAGES) & 1u;
-                if (first && !await(ptx::smem_u32(o_free), (unit_cnt & 1u) ^ 1u, abort, a.status, 3, unit_cnt, -1)) return false;
-                if (!await(ptx::smem_u32(v_full + st), vpar, abort, a.status, 8, v_cnt, -1)) return false;
-                ++v_cnt;
-                const uint32_t va = ptx::smem_u32(sV + st * KB_BYTES);
-                const uint32_t pt = tmem + S_COL + buf * 128;
-                for (int h = 0; h < 2; ++h) {
-                    if (!await(ptx::smem_u32(p_full + buf * 2 + h), par, abort, a.status, 10 + h, sc, -1)) return false;
-                    ptx::tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < HK / 16; ++kk) {
-                        const int key = h * HK + kk * 16;
-                        const uint64_t vd = sdesc_mn_sw128(va + key * 128, BKV * 128);
-                        const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
-                        mma_bf16_tmem_a(tmem + O_COL + h * HD, pt + h * 64 + kk * 8, vd, a.idesc_pv, acc0);
-                        if (SPLIT) mma_bf16_tmem_a(tmem + O_COL + h * HD, pt + h * 64 + 32 + kk * 8, vd, a.idesc_pv, 1u);
+            while (ok) {
+                const int u = next_unit(false);
+                if (u < 0) break;
+                int qt, g, part, b0, b1;
+                unit_of(a, u, qt, g, part);
+                item_blocks(a, qt, part, b0, b1);
+                const int nb = b1 - b0;
+                // O_h += P_h V_h for each block (P in the block's S buffer)
+                for (int b = 0; b < nb; ++b, ++sc) {
+                    const bool first = b == 0;
+                    const int buf = sc & 1;
+                    const uint32_t par = (sc >> 1) & 1u;
+                    const uint32_t st = v_cnt % V_STAGES, vpar = (v_cnt / V_STAGES) & 1u;
+                    if (first && !await(ptx::smem_u32(o_free), (unit_cnt & 1u) ^ 1u, abort, a.status, 3, unit_cnt, u)) {
+                        ok = false;
+                        break;
                     }
-                    ptx::mma_commit(ptx::smem_u32(o_full + h * 2 + buf));
+                    if (!await(ptx::smem_u32(v_full + st), vpar, abort, a.status, 8, v_cnt, u) ||
+                        !await(ptx::smem_u32(p_full + buf), par, abort, a.status, 10, sc, u)) {
+                        ok = false;
+                        break;
+                    }
+                    ++v_cnt;
+                    ptx::tc_fence_after();
+                    const uint64_t vd0 = sdesc_mn_sw128(ptx::smem_u32(sV + st * KB_BYTES), BKV * 128);
+                    const uint32_t pt = tmem + S_COL + buf * 128;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                        for (int kk = 0; kk < HK / 16; ++kk) {
+                            const int key = h * HK + kk * 16;
+                            const uint64_t vd = vd0 + (uint64_t)((key * 128) >> 4);
+                            const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
+                            mma_bf16_tmem_a(tmem + O_COL + h * HD, pt + h * 64 + kk * 8, vd, a.idesc_pv, acc0);
+                            if (SPLIT)
+                                mma_bf16_tmem_a(tmem + O_COL + h * HD, pt + h * 64 + 32 + kk * 8, vd, a.idesc_pv, 1u);
+                        }
+                    }
+                    ptx::mma_commit(ptx::smem_u32(s_free + buf));
                 }
-                ptx::mma_commit(ptx::smem_u32(s_free + buf));
-                ptx::mma_commit(ptx::smem_u32(v_empty + st));
-                return true;
-            };
+                ++unit_cnt;
+            }
+            ptx::mma_commit(ptx::smem_u32(drain + 1));
+            drain_wait(ptx::smem_u32(drain + 1), 0, a.status);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- S issuer
+        if (lane == 0) {
+            uint32_t q_cnt = 0, k_cnt = 0, s_cnt = 0;
+            bool ok = true;
             while (ok) {
                 const int u = next_unit(false);
                 if (u < 0) break;
@@ -392,7 +421,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int nb = b1 - b0;
                 if (!await(ptx::smem_u32(q_full), q_cnt & 1u, abort, a.status, 4, q_cnt, u)) break;
                 ++q_cnt;
-                uint32_t prev_sc = 0;
                 for (int b = 0; b < nb; ++b) {
                     const uint32_t st = k_cnt % K_STAGES;
                     const uint32_t kpar = (k_cnt / K_STAGES) & 1u;
@@ -402,28 +430,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (!await(ptx::smem_u32(k_full + st), kpar, abort, a.status, 5, k_cnt, u) ||
                         !await(ptx::smem_u32(s_free + buf), spar ^ 1u, abort, a.status, 6, s_cnt, u)) { ok = false; break; }
                     ptx::tc_fence_after();
-                    const uint32_t qa = ptx::smem_u32(sQ), ka = ptx::smem_u32(sK + st * KB_BYTES);
+                    // descriptors of the tiles' first k-step; a k-step's start address is a constant offset (the
+                    // address field holds address / 16, and every address stays below 256 KB)
+                    const uint64_t qd0 = ptx::sdesc_sw128(ptx::smem_u32(sQ));
+                    const uint64_t kd0 = ptx::sdesc_sw128(ptx::smem_u32(sK + st * KB_BYTES));
 #pragma unroll
                     for (int kk = 0; kk < HD / 16; ++kk) {
                         const uint32_t off = (kk & 3) * 32;
-                        const uint64_t kd = ptx::sdesc_sw128(ka + (kk >> 2) * (BKV * 128) + off);
-                        ptx::mma_bf16(tmem + S_COL + buf * 128, ptx::sdesc_sw128(qa + (kk >> 2) * (ROWS * 128) + off),
-                                      kd, a.idesc_qk, kk > 0 ? 1u : 0u);
+                        const uint64_t kd = kd0 + (uint64_t)(((kk >> 2) * (BKV * 128) + off) >> 4);
+                        const uint64_t qd = qd0 + (uint64_t)(((kk >> 2) * (ROWS * 128) + off) >> 4);
+                        ptx::mma_bf16(tmem + S_COL + buf * 128, qd, kd, a.idesc_qk, kk > 0 ? 1u : 0u);
                         if (SPLIT)
-                            ptx::mma_bf16(tmem + S_COL + buf * 128,
-                                          ptx::sdesc_sw128(qa + Q_BYTES + (kk >> 2) * (ROWS * 128) + off), kd,
-                                          a.idesc_qk, 1u);
+                            ptx::mma_bf16(tmem + S_COL + buf * 128, qd + (uint64_t)(Q_BYTES >> 4), kd, a.idesc_qk, 1u);
                     }
                     ptx::mma_commit(ptx::smem_u32(s_full + buf));
                     ptx::mma_commit(ptx::smem_u32(k_empty + st));
                     if (b == nb - 1) ptx::mma_commit(ptx::smem_u32(q_empty));
-                    if (b > 0 && !pv(prev_sc, b == 1)) { ok = false; break; }
-                    prev_sc = s_cnt;
                     ++s_cnt;
                 }
-                if (!ok) break;
-                if (!pv(prev_sc, nb == 1)) break;
-                ++unit_cnt;
             }
             ptx::mma_commit(ptx::smem_u32(drain));
             drain_wait(ptx::smem_u32(drain), 0, a.status);
@@ -471,14 +495,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // rescale O_h when the running max outgrew the scale in use by more than 2^8.  The TMEM
                 // accesses are warp-collective (.sync.aligned), so when any lane needs it the whole warp
                 // rescales, each row by its own factor (rescaling to the current max is always valid).
-                // O_h must first hold block sc-1's update: o_full[hf][x] completes once per block of
-                // parity x, and block sc+1's update cannot complete before this warp writes its P.
+                // O_h must first hold block sc-1's update: s_free[x] completes once the PV MMAs of the
+                // last block on buffer x (and every MMA before them) are done, and block sc's cannot start
+                // before this warp writes its P.
                 const bool need = m_used != -INFINITY && m_run > m_used + RESCALE_LOG2;
                 if (__any_sync(0xffffffffu, need)) {
                     if (b > 0) {
                         const uint32_t pb = sc - 1;
-                        if (!await(ptx::smem_u32(o_full + hf * 2 + (pb & 1)), (pb >> 1) & 1u, abort, a.status, 35 + hf,
-                                   pb, u)) {
+                        if (!await(ptx::smem_u32(s_free + (pb & 1)), (pb >> 1) & 1u, abort, a.status, 35 + hf, pb,
+                                   u)) {
                             ok = false;
                             break;
                         }
@@ -528,14 +553,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(p_full + buf * 2 + hf));
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(p_full + buf));
                 ++sc;
             }
             if (!ok) break;
             // the last block's O_h update
             {
                 const uint32_t pb = sc - 1;
-                if (!await(ptx::smem_u32(o_full + hf * 2 + (pb & 1)), (pb >> 1) & 1u, abort, a.status, 40 + hf, pb, u))
+                if (!await(ptx::smem_u32(s_free + (pb & 1)), (pb >> 1) & 1u, abort, a.status, 40 + hf, pb, u))
                     break;
             }
             ptx::tc_fence_after();
