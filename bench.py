@@ -586,7 +586,7 @@ def load_traffic(kernel: str, workload_name: str):
         return None
     try:
         d = json.load(open(p))
-        ent = d.get(kernel)
+        ent = d.get(f"{kernel}@{workload_name}") or d.get(kernel)
         if not ent or ent.get("workload") != workload_name:
             return None
         import hashlib
