@@ -28,7 +28,7 @@ EXPORTED = ("cb_model_create", "cb_model_destroy", "cb_rerope", "cb_blend", "cb_
             "cb_blend_paged", "cb_kv_gather_pages", "cb_kv_scatter_pages", "cb_pages_create", "cb_pages_destroy",
             "cb_pages_alloc", "cb_pages_retain", "cb_pages_release", "cb_pages_plan_write", "cb_pages_count",
             "cb_pages_free", "cb_index_create", "cb_index_destroy", "cb_index_size", "cb_index_match",
-            "cb_select_hkvd", "cb_blend_hkvd")
+            "cb_select_hkvd", "cb_blend_hkvd", "cb_gradual_layout")
 CB_STATIC_MAX_CHUNKS = 256
 CB_STATUS_BAD_TOKEN, CB_STATUS_WAIT_TIMEOUT, CB_STATUS_BAD_ROW = 1, 2, 4
 
@@ -154,6 +154,8 @@ def lib() -> ctypes.CDLL:
         L.cb_index_match.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, vp, vp]
         L.cb_selected_count.restype = i32
         L.cb_selected_count.argtypes = [i32, ctypes.c_double]
+        L.cb_gradual_layout.restype = i32
+        L.cb_gradual_layout.argtypes = [i32, ctypes.POINTER(ctypes.c_double), i32, vp, vp, vp, i32]
         L.cb_select_hkvd.restype = ctypes.c_int
         L.cb_select_hkvd.argtypes = [vp, i32, i32, vp, vp]
         L.cb_blend_hkvd.restype = ctypes.c_int
@@ -186,6 +188,19 @@ def _check(code: int):
 
 def cb_selected_count(n_ctx: int, ratio: float) -> int:
     return int(lib().cb_selected_count(n_ctx, ratio))
+
+
+def cb_gradual_layout(n_ctx: int, ratios):
+    """The comparing layers of a gradual schedule as a list of (layer, kept rows, compared rows), in the order
+    cb_blend_gradual writes out_selected and out_dev.  Raises on an invalid schedule."""
+    r = (ctypes.c_double * len(ratios))(*[float(x) for x in ratios])
+    cap = len(ratios)
+    lay, kept, cmp_ = (ctypes.c_int32 * cap)(), (ctypes.c_int32 * cap)(), (ctypes.c_int32 * cap)()
+    n = int(lib().cb_gradual_layout(int(n_ctx), r, len(ratios), ctypes.addressof(lay), ctypes.addressof(kept),
+                                    ctypes.addressof(cmp_), cap))
+    if n < 0:
+        raise ValueError(f"cb_gradual_layout: invalid schedule (status {n})")
+    return [(int(lay[i]), int(kept[i]), int(cmp_[i])) for i in range(n)]
 
 
 def cb_select_hkvd(dev, n: int, k: int, out_rows, stream=None) -> None:
@@ -556,9 +571,9 @@ class BlendModel:
         n = int(tokens.shape[0])
         n_ctx = sum(c[2] for c in chunks)
         counts = [cb_selected_count(n_ctx, r) for r in ratios]
-        check = [1] + [l for l in range(2, len(ratios) + 1) if counts[l - 1] < counts[l - 2]]
-        n_sel = sum(counts[l - 1] for l in check)
-        n_dev = n_ctx + sum(counts[l - 2] for l in check[1:])
+        layout = cb_gradual_layout(n_ctx, ratios)          # the library's own order of the outputs
+        n_sel = sum(kept for _, kept, _ in layout)
+        n_dev = sum(cmp_ for _, _, cmp_ in layout)
         if out_kv is None:
             out_kv = self.kv_buffer(n)
         logits = torch.empty(self.shape["vocab"], dtype=torch.float32, device=self.device)
@@ -567,11 +582,10 @@ class BlendModel:
         st = cb_blend_gradual(self.handle, tokens, n, cached_kv, chunks, ratios, out_kv, logits,
                               sel if n_sel > 0 else None, dev, stream, stats)
         sets, devs, at, dat = {}, {}, 0, 0
-        for i, l in enumerate(check):
-            sets[l] = sel[at:at + counts[l - 1]]
-            at += counts[l - 1]
+        for l, kept, nd in layout:
+            sets[l] = sel[at:at + kept]
+            at += kept
             if want_dev:
-                nd = n_ctx if i == 0 else counts[l - 2]
                 devs[l] = dev[dat:dat + nd]
                 dat += nd
         out = dict(out_kv=out_kv, logits=logits, counts=counts, sets=sets)

@@ -68,6 +68,26 @@ int32_t cb_selected_count(int32_t n_ctx, double ratio) {
     return (int32_t)k;
 }
 
+int32_t cb_gradual_layout(int32_t n_ctx, const double* ratios, int32_t n_ratios, int32_t* out_layers,
+                          int32_t* out_kept, int32_t* out_compared, int32_t max_entries) {
+    if (n_ctx < 0 || n_ratios < 1 || !ratios || max_entries < 0) return CB_ERR_INVALID_ARG;
+    int n = 0, prev = 0;
+    for (int l = 1; l <= n_ratios; ++l) {
+        const int k = cb_selected_count(n_ctx, ratios[l - 1]);
+        if (k < 0 || (l >= 2 && k > prev)) return CB_ERR_INVALID_ARG;
+        // the rule blend_impl applies: layer 1 always compares, a later layer when its count shrinks
+        if (l == 1 || k < prev) {
+            if (n >= max_entries) return CB_ERR_INVALID_ARG;
+            if (out_layers) out_layers[n] = l;
+            if (out_kept) out_kept[n] = k;
+            if (out_compared) out_compared[n] = l == 1 ? n_ctx : prev;
+            ++n;
+        }
+        prev = k;
+    }
+    return n;
+}
+
 cb_status cb_model_create(const cb_config* cfg, const cb_weights* w, cb_model** out) {
     g_err[0] = 0;
     if (!cfg || !w || !out) return fail(CB_ERR_INVALID_ARG, "cb_model_create: null argument");

@@ -399,6 +399,18 @@ int32_t cb_pick_storage(const double* throughput_bytes_per_s, const double* cost
 /* k = ceil(ratio * n_ctx - 1e-9) clamped to [0, n_ctx]; -1 if ratio is outside [0, 1] or NaN. */
 int32_t cb_selected_count(int32_t n_ctx, double ratio);
 
+/* The layout of cb_blend_gradual's (and cb_blend_streamed's) out_selected and out_dev for a schedule
+ * (section "核心思想", Figure 9's funnel).  The comparing layers are the check layer 1 and every layer
+ * l >= 2 whose count shrinks (k_l < k_{l-1}); for the i-th of them, in layer order:
+ *   out_layers[i]   = l
+ *   out_kept[i]     = k_l       rows that layer adds to out_selected
+ *   out_compared[i] = n_ctx for the check layer, k_{l-1} for a shrinking layer: entries it adds to out_dev
+ * Host arrays of max_entries; any of them may be NULL.  Returns the number of comparing layers, or
+ * CB_ERR_INVALID_ARG (negative) for n_ctx < 0, n_ratios < 1, a ratio outside [0, 1], a growing schedule,
+ * or more comparing layers than max_entries.  Host only. */
+int32_t cb_gradual_layout(int32_t n_ctx, const double* ratios, int32_t n_ratios, int32_t* out_layers,
+                          int32_t* out_kept, int32_t* out_compared, int32_t max_entries);
+
 /* Description of the last error on the calling thread ("" if none). */
 const char* cb_last_error(void);
 

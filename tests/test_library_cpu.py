@@ -215,3 +215,35 @@ def test_page_bookkeeping_matches_reference(lib):
         P.release([n + 3])
     assert P.count(-1) == -1
     P.close()
+
+
+def test_gradual_layout_matches_oracle_sets(lib):
+    """cb_gradual_layout (the order of cb_blend_gradual's out_selected and out_dev) against the layers the
+    oracle's blend_gradual compares on a 5-layer fp32 model: its `devs` keys (the layers that rank rows) in
+    layer order, the size of each such layer's set and the length of its deviation vector.  Invalid
+    schedules are rejected."""
+    import numpy as np
+    import oracle
+    import workload
+    shape = workload.ModelShape(n_layers=5, d_model=256, n_heads=4, n_kv_heads=2, head_dim=64, ffn_hidden=512,
+                                vocab=1024, rope_theta=1e4, dtype="f32")
+    w = workload.make_weights(shape, 0)
+    chunk_tokens = [workload.tokens(0, 10 + c, 64, shape.vocab) for c in range(3)]
+    chunks = [(0, 64 * c, 64) for c in range(3)]
+    toks = np.concatenate(chunk_tokens + [workload.tokens(0, 99, 16, shape.vocab)])
+    caches = oracle.chunk_caches(shape.as_dict(), w, chunk_tokens, chunks, "f32")
+    n_ctx = 192
+    for ratios in ([0.5, 0.4, 0.4, 0.2], [0.3, 0.3, 0.3, 0.3], [0.5, 0.25, 0.0, 0.0], [1.0, 0.5, 0.5, 0.1]):
+        ref = oracle.blend_gradual(shape.as_dict(), w, toks, caches, chunks, ratios, "f32")
+        got = cb.cb_gradual_layout(n_ctx, ratios)
+        layers = sorted(ref["devs"])
+        assert [l for l, _, _ in got] == layers, ratios
+        assert [kept for _, kept, _ in got] == [len(ref["sets"][l]) for l in layers], ratios
+        assert [c for _, _, c in got] == [len(ref["devs"][l]) for l in layers], ratios
+    with pytest.raises(ValueError):
+        cb.cb_gradual_layout(n_ctx, [0.2, 0.3, 0.3, 0.3])          # growing
+    with pytest.raises(ValueError):
+        cb.cb_gradual_layout(n_ctx, [0.2, 1.5, 0.1, 0.1])          # ratio outside [0, 1]
+    r = (ctypes.c_double * 4)(0.5, 0.4, 0.3, 0.2)
+    assert lib.cb_gradual_layout(n_ctx, r, 4, None, None, None, 2) < 0   # more comparing layers than entries
+    assert lib.cb_gradual_layout(n_ctx, r, 4, None, None, None, 4) == 4

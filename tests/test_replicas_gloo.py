@@ -75,8 +75,12 @@ def test_traffic_lookup_needs_matching_workload_and_source():
     import os
     import bench
     d = json.load(open(os.path.join(bench.ROOT, "profiles", "ncu_traffic.json")))
-    for kernel, ent in d.items():
+    for key, ent in d.items():
+        kernel = key.split("@")[0]                  # "kernel" or "kernel@workload"
         got = bench.load_traffic(kernel, ent["workload"])
         assert got in (None, ent["dram_bytes_per_launch_full"])
-        assert bench.load_traffic(kernel, "llama8b-32k" if ent["workload"] != "llama8b-32k" else "llama8b-3k") is None
+        captured = {e["workload"] for k, e in d.items() if k.split("@")[0] == kernel}
+        for other in ("llama8b-3k", "llama8b-8k", "llama8b-32k"):
+            if other not in captured:
+                assert bench.load_traffic(kernel, other) is None
     assert bench.load_traffic("no-such-kernel", "llama8b-3k") is None
