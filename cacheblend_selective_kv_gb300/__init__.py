@@ -571,7 +571,10 @@ class BlendModel:
         n = int(tokens.shape[0])
         n_ctx = sum(c[2] for c in chunks)
         counts = [cb_selected_count(n_ctx, r) for r in ratios]
-        layout = cb_gradual_layout(n_ctx, ratios)          # the library's own order of the outputs
+        try:
+            layout = cb_gradual_layout(n_ctx, ratios)      # the library's own order of the outputs
+        except ValueError:
+            layout = []                                    # cb_blend_gradual below rejects it with its own error
         n_sel = sum(kept for _, kept, _ in layout)
         n_dev = sum(cmp_ for _, _, cmp_ in layout)
         if out_kv is None:

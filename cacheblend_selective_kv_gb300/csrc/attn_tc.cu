@@ -796,12 +796,12 @@ cudaError_t launch_attention_tc(const Model& m, const void* qmap, const void* qm
     if (e != cudaSuccess || a.parts == 1) return e;
     const int warps = M * c.n_heads;
     const int blocks = (warps + 7) / 8;
-    if (c.head_dim == 128)
-        attn_combine_kernel<128><<<blocks, 256, 0, s>>>(a);
-    else
-        attn_combine_kernel<64><<<blocks, 256, 0, s>>>(a);
+    // programmatic dependent launch: the merge's CTAs take the SMs the attention's tail leaves idle and wait
+    // (griddepcontrol.wait) for its partial results
+    e = c.head_dim == 128 ? launch_ex(m.pdl, attn_combine_kernel<128>, dim3(blocks), dim3(256), 0, s, a)
+                          : launch_ex(m.pdl, attn_combine_kernel<64>, dim3(blocks), dim3(256), 0, s, a);
     if (launches) *launches = 2;
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace cb
