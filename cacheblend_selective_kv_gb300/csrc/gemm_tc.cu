@@ -1043,19 +1043,28 @@ cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, c
         if (cap < 0) return cudaErrorInvalidConfiguration;
         workers = cap;
     }
-    // split K only where the epilogue accumulates (residual adds): pick the split that minimises
-    // waves x (k-blocks per unit + 2 blocks of per-unit latency)
+    // split K only where the epilogue accumulates (residual adds): pick the split that minimises the
+    // GEMM's waves x (k-blocks per unit + 2 blocks of per-unit latency), in microseconds, plus the time to
+    // write the S partial-sum slots and read them back in the next RMSNorm.  A k-block is 4 k-steps (8 MMAs
+    // split) of about 99 cycles up to N = 128 and 161 at N = 256 (linear between), at ~2 GHz; the slots move
+    // at ~20 TB/s while they fit in L2 next to the rest (48 MB) and at ~5 TB/s from HBM beyond.
     a.splits = 1;
     if (e.kind == EPI_RESID) {
         double best = 1e30;
         int smax = 8;
         if (const char* v = getenv("CB_TUNE_SPLITK")) smax = std::min(8, std::max(1, atoi(v)));   // 8 slots at most
+        const char* sm = getenv("CB_SPLIT_TRAFFIC");
+        const bool traffic = !(sm && sm[0] == '0');
+        const double mma = a.BN <= 128 ? 99.0 : 99.0 + (a.BN - 128) * (62.0 / 128.0);
+        const double t_kb = (split ? 8.0 : 4.0) * mma / 2000.0;                          // us per k-block
+        const double slot_mb = (double)M * N * 4.0 / 1e6;
         for (int S = 1; S <= smax; ++S) {
             if (a.kb_total / S < 4) break;
             if (S > 1 && (!e.part || (long long)S * M > e.part_rows)) break;   // the partial slots must fit
             const long long units = (long long)mtiles * a.ttiles * S;
             const long long waves = (units + workers - 1) / workers;
-            const double cost = waves * ((double)a.kb_total / S + 2.0);
+            double cost = waves * ((double)a.kb_total / S + 2.0) * t_kb;
+            if (traffic && S > 1) cost += 2.0 * S * slot_mb / (S * slot_mb <= 48.0 ? 20.0 : 5.0);   // MB / (TB/s) = us
             if (cost < best - 1e-9) { best = cost; a.splits = S; }
         }
     }
