@@ -1004,12 +1004,29 @@ cudaError_t launch_gemm_tc(const Model& m, int xbuf, int x_row0, int M, int K, c
     // whose gate and up accumulators share one TMEM buffer: 128), multiples of 16
     int bn_max = (swiglu && !pair) ? 128 : 256;
     if (const char* v = getenv("CB_TUNE_BN")) bn_max = std::min(bn_max, std::max(16, atoi(v)));
+    // The QKV and comparing GEMMs on CTA pairs run few waves, so there the split is the one with the fewest
+    // waves x MMA cycles at its tile width (about 99 cycles up to N = 128, 161 at N = 256, linear between),
+    // the fewest padded rows breaking ties.
     int best_T = 0, best_BN = 0;
-    for (int T0 = (M + bn_max - 1) / bn_max, T = T0; T <= T0 + 2; ++T) {
+    const char* twv = getenv("CB_TILE_WAVES");
+    const bool by_waves = pair && (e.kind == EPI_QKV || e.kind == EPI_KVCMP) && !(twv && twv[0] == '0');
+    double best_c = 1e30;
+    for (int T0 = (M + bn_max - 1) / bn_max, T = T0; T <= T0 + (by_waves ? 8 : 2); ++T) {
         int bn = ((M + T - 1) / T + 15) / 16 * 16;
         if (bn < 16) bn = 16;
         if (bn > bn_max) continue;
-        if (!best_T || (long long)T * bn < (long long)best_T * best_BN) { best_T = T; best_BN = bn; }
+        const long long pad = (long long)T * bn;
+        double c = 0.0;
+        if (by_waves) {
+            const long long w_est = std::max(1, m.num_sms / 2);
+            const long long waves = ((long long)mtiles * T + w_est - 1) / w_est;
+            c = waves * (bn <= 128 ? 99.0 : 99.0 + (bn - 128) * (62.0 / 128.0));
+        }
+        if (!best_T || c < best_c - 1e-9 || (c < best_c + 1e-9 && pad < (long long)best_T * best_BN)) {
+            best_T = T;
+            best_BN = bn;
+            best_c = c;
+        }
     }
     a.ttiles = best_T;
     a.BN = best_BN;
