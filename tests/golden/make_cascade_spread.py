@@ -10,7 +10,7 @@ rounding (the size of a float32 implementation's relative error; the re-RoPE'd c
 the recomputed set of the plain run, and records per layer the max-abs and
 the mean-abs distance of the perturbed run's stored values from the plain run's unrounded values, over
 the rows the configuration recomputes, and the logits' max-abs distance.  The GPU parity tests hold a
-configuration to the benchmark spec's bound (2e-2) where this spread stays below it, and to 1.5 times the spread
+configuration to the K/V tolerance of 2e-2 where this spread stays below it, and to 1.5 times the spread
 where even the oracle's own spread exceeds it.
 
 Written to ``cascade_spread.json`` (one entry per configuration).

@@ -93,7 +93,7 @@ def cascade_bounds(name: str):
     """Per-layer K/V bounds (max-abs, mean-abs) and the logits bound for a configuration whose recomputed rows
     are so many that the oracle's own spread under a rounding-sized perturbation of its stored values
     (tests/golden/cascade_spread.json, written by tests/golden/make_cascade_spread.py from the oracle alone)
-    exceeds the benchmark spec's bounds: max-abs max(2e-2, 1.5 x spread), mean-abs 1.5 x spread, logits
+    exceeds the tolerances (2e-2 K/V, 3e-2 logits): max-abs max(2e-2, 1.5 x spread), mean-abs 1.5 x spread, logits
     max(3e-2, 1.5 x spread)."""
     import json
     import os
