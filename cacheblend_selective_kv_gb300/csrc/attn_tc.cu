@@ -23,9 +23,10 @@
 // S and PV MMAs come from two threads (each one's waits and commits overlap the other's issue) and both
 // keep their per-block bookkeeping small: one wait for P (both halves' warps arrive on one barrier), no
 // barrier of their own for V stages or for O (the V producer and the softmax warps wait on the S/P
-// buffer's free barrier, which completes at the same point), and descriptors formed once per block.  V is consumed as an MN-major operand from its [key][dim]
-// layout.  The persistent CTAs claim units at run time (longest query tiles first) from a counter in
-// global memory; long key ranges are cut into parts merged by attn_combine_kernel.
+// buffer's free barrier, which completes at the same point), and descriptors formed once per block.
+// V is consumed as an MN-major operand from its [key][dim] layout.  The persistent CTAs claim units at
+// run time (longest query tiles first) from a counter in global memory; long key ranges are cut into
+// parts merged by attn_combine_kernel.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
